@@ -1,0 +1,415 @@
+"""Benchmark of the ZeRO partitioned optimizer step of one data-parallel rank.
+
+Metric: parameters updated per second (and achieved HBM GB/s against the
+measured GB300 copy bandwidth), 1 GPU per rank.  Default workload: the 7.5B
+model of the ZeRO Stage-3 memory table, Nd = 64, bf16 gradients, rank 0's
+shard of 117,187,500 parameters, fusion bucket 5e8 (one bucket); 64 gradient
+contributions (15 GB) resident in HBM.
+
+A step = the whole hot path: the fused reduce + AdamW + cast kernel over the
+shard, the read of the nonfinite flag, and the commit (or global skip).  Each
+step moves 18 GB, far more than the 129 MB L2, so no L2 flush is needed
+between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c4]
+    python bench.py --impl reference     # the CPU oracle on a bounded sample
+
+Under torchrun (N > 1) every process runs its own rank's shard (weak scaling;
+the only collective is the one-word OR of the skip flag) and rank 0 prints
+the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ZeRO shard step: params updated/s and HBM GB/s vs GB300 peak (1 GPU)"
+UNIT = "params/s"
+KERNEL_SRC = os.path.join(ROOT, "zero_sharded_optimizer_02_gb300", "csrc", "zero_kernels.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k_step_fused_traffic.txt")
+NOMINAL_HBM_GBS = 7900.0
+
+
+def measured_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return {}
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per parameter of the fused kernel from the committed ncu
+    summary, if it was taken on the current kernel source for this workload."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for ln in f:
+                if ":" in ln and not ln.startswith("#"):
+                    k, v = ln.split(":", 1)
+                    kv[k.strip()] = v.strip()
+    except OSError:
+        return None
+    if kv.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    if kv.get("workload") != workload:
+        return None
+    return float(kv["dram_bytes_per_param"])
+
+
+def smi_index(local: int) -> str:
+    """nvidia-smi's id of this process's device (honours CUDA_VISIBLE_DEVICES)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local < len(ids):
+            return ids[local]
+    return str(local)
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, max clock, throttle reasons) over a window."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = [r for (ts, r) in self.rows if t0 - 0.15 <= ts <= t1 + 0.15 and len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(rows[0][2]), "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args) -> None:
+    import torch
+    import torch.distributed as dist
+
+    import synth
+    from zero_sharded_optimizer_02_gb300 import build
+    from zero_sharded_optimizer_02_gb300.step import DataParallelStep
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        dist.barrier()
+        build.build()          # every rank loads the library (already built)
+
+    w = synth.WORKLOADS[args.config]
+    dp_rank = args.rank + rank             # this process's data-parallel rank
+    assert dp_rank < w.nd, "more processes than data-parallel ranks"
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        dps = DataParallelStep(w.psi, w.nd, [dp_rank], w.grad_dtype, w.hparams, w.loss_scale,
+                               w.bucket, dev, gathered="slot", fused=True,
+                               process_group=dist.group.WORLD if world > 1 else None,
+                               stream=stream)
+        L = dps.layouts[dp_rank]
+        n = int(L.length)
+        pitch = int(L.row_pitch)
+        st = dps.state[dp_rank]
+        for row, which in zip(st.bufs[st.cur], ("master", "m", "v")):
+            synth.fill_shard_state(w, dp_rank, which, row)
+        grads = torch.empty(w.nd, pitch, dtype=synth.WORKLOADS[args.config].torch_grad_dtype,
+                            device=dev)
+        synth.fill_shard_rows(w, 0, dp_rank, grads)
+        from zero_sharded_optimizer_02_gb300 import _abi
+        desc = {dp_rank: _abi.grads(grads, pitch, 0, w.nd, w.grad_dtype)}
+    torch.cuda.synchronize(dev)
+
+    # -- warm-up, then K timed steps ------------------------------------------
+    for _ in range(args.warmup):
+        dps.step(desc)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(smi_index(local)) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0.0)
+    launches = 0
+    skipped = 0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    t_start.record(stream)
+    for k in range(args.steps):
+        ev[k][0].record(stream)
+        launches += dps.launch(desc)
+        ev[k][1].record(stream)
+        s = dps.decide()
+        dps.commit(s)
+        skipped += int(s)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    kernel_ms = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    time.sleep(0.2 if sampler else 0.0)
+    clocks = None
+    if sampler:
+        sampler.stop()
+        clocks = sampler.summary(wall0, wall1)
+
+    # -- end to end through host buffers (pinned H2D of the step's gradients,
+    #    the step, D2H of the new parameters and the flag) ----------------------
+    e2e = None
+    if args.e2e_steps > 0:
+        host_grads = torch.empty(grads.shape, dtype=grads.dtype, pin_memory=True)
+        host_grads.copy_(grads)
+        host_params = torch.empty(n, dtype=grads.dtype, pin_memory=True)
+        for it in range(args.e2e_steps + 1):      # first iteration untimed
+            if it == 1:
+                if world > 1:
+                    dist.barrier()
+                torch.cuda.synchronize(dev)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            with torch.cuda.stream(stream):
+                grads.copy_(host_grads, non_blocking=True)
+            s = dps.step(desc)
+            with torch.cuda.stream(stream):
+                host_params.copy_(dps.gathered_view(dp_rank)[:n], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        if world > 1:
+            tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
+        e2e = {"value": world * n / (e2e_ms * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": host_grads.numel() * host_grads.element_size(),
+               "d2h_bytes_per_step": n * host_params.element_size() + 4,
+               "ms_per_step": e2e_ms, "steps": args.e2e_steps}
+        del host_grads, host_params
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    # -- report -----------------------------------------------------------------
+    peaks = measured_peaks()
+    ms_per_step = total_ms / args.steps
+    bytes_per_param = w.bytes_per_param
+    kern_avg_ms = statistics.fmean(kernel_ms)
+    achieved = bytes_per_param * n / (kern_avg_ms * 1e-3) / 1e9
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or 6800.0
+    traffic_pp = recorded_traffic(args.config)
+    line = {
+        "metric": METRIC,
+        "value": world * n / (ms_per_step * 1e-3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded counter-based generator; no dataset or weights)",
+        "config": {"workload": f"{args.config}: {w.title}", "psi": w.psi, "nd": w.nd,
+                   "rank": dp_rank, "shard_params": n, "grad_dtype": w.grad_dtype,
+                   "bucket": w.bucket, "loss_scale": w.loss_scale,
+                   "l2": f"inputs larger than L2 ({bytes_per_param * n / 1e9:.1f} GB per step),"
+                         " no flush",
+                   "parallelism": f"zero-dp{w.nd} emulated, {world} process(es)"},
+        "gbs": bytes_per_param * n / (ms_per_step * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_src,
+                     "frac_of_nominal_7900": achieved / NOMINAL_HBM_GBS,
+                     "traffic": None if traffic_pp is None else traffic_pp * n,
+                     "kernel": "k_step_fused", "kernel_ms": kern_avg_ms,
+                     "algorithmic_bytes_per_launch": bytes_per_param * n},
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "skipped_steps": skipped,
+        "clocks": clocks,
+        "wall_s_timed": wall1 - wall0,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, dp_rank, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle_sample(w, dp_rank: int, n_sample: int):
+    import numpy as np
+    import torch
+
+    import synth
+    s, begin, n = synth.shard_of(w.psi, w.nd, dp_rank)
+    n_sample = min(n_sample, n)
+    idx = torch.arange(begin, begin + n_sample, dtype=torch.int64)
+    rows = np.stack([synth.grad_values(w, 0, j, idx).view(torch.int16).numpy().view(np.uint16)
+                     for j in range(w.nd)])
+    st = [synth.state_values(w, k, idx).numpy() for k in ("master", "m", "v")]
+    return rows, st, n_sample
+
+
+def _oracle_step(orc, w, rows, st, n_sample, t):
+    import numpy as np
+    params = np.zeros(n_sample, np.uint16)
+    return orc.step_rank(rows, n_sample, 0, n_sample, w.nd, orc.dtype_code(w.grad_dtype),
+                         w.bucket, w.loss_scale, w.hparams, t, st[0], st[1], st[2], params, 0)
+
+
+def cpu_baseline(w, dp_rank: int, seconds: float) -> dict:
+    """The oracle as it stands (single-threaded C) on a contiguous sample of
+    this rank's shard, repeated for about ``seconds`` of CPU time."""
+    import oracle
+    oracle.build()
+    n_sample = 1 << 18
+    rows, st, n_sample = _oracle_sample(w, dp_rank, n_sample)
+    _oracle_step(oracle, w, rows, st, n_sample, 1)   # warm
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_step(oracle, w, rows, st, n_sample, 1 + reps)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    rate = reps * n_sample / el
+    return {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{reps} x {n_sample} contiguous params of rank {dp_rank}'s shard "
+                      f"({w.nd} contributions each), single-threaded C, {el:.1f} s",
+            "gbs": rate * w.bytes_per_param / 1e9}
+
+
+def run_reference(args) -> None:
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import synth
+    import oracle
+    oracle.build()
+    w = synth.WORKLOADS[args.config]
+    n_sample = args.ref_sample
+    rows, st, n_sample = _oracle_sample(w, args.rank, n_sample)
+    for k in range(args.warmup):
+        _oracle_step(oracle, w, rows, st, n_sample, 1 + k)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        _oracle_step(oracle, w, rows, st, n_sample, 1 + k)
+    el = time.perf_counter() - t0
+    ms = el * 1e3 / args.steps
+    value = n_sample / (ms * 1e-3)
+    sample = (f"each step: {n_sample} contiguous params of rank {args.rank}'s shard "
+              f"({w.nd} contributions each), single-threaded C oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": f"{args.config}: {w.title}", "psi": w.psi, "nd": w.nd,
+                   "rank": args.rank, "sample_params_per_step": n_sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__,
+                                 formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="c4", choices=["c1", "c2", "c3", "c4"])
+    ap.add_argument("--rank", type=int, default=0, help="first data-parallel rank to run")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-sample", type=int, default=1 << 16,
+                    help="params per step of the reference (oracle) arm")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

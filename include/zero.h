@@ -1,0 +1,201 @@
+/*
+ * zero.h -- C ABI of the ZeRO partitioned optimizer step on one GPU (sm_103a).
+ *
+ * One data-parallel rank of ZeRO ("ZeRO: Memory Optimizations Toward Training
+ * Trillion Parameter Models", section "ZeRO-DP", Stages 1-3) owns 1/Nd of the
+ * flat parameter vector.  For its shard it
+ *   (1) reduces the Nd ranks' fp16/bf16 gradient contributions in fixed rank
+ *       order (its half of the bucketed reduce-scatter, Stage 2), scaled by
+ *       1 / (Nd * loss_scale);
+ *   (2) applies mixed-precision AdamW to its fp32 master weights and Adam
+ *       moments (the 4 + K bytes per parameter of section "Quantifying memory
+ *       consumption", K = 12);
+ *   (3) casts the new weights to fp16/bf16 into its slot of the gathered
+ *       parameter buffer (the all-gather at the end of the step, Stage 1),
+ * bucket by bucket (section "ZeRO-R / CB": a constant-size fusion buffer).
+ * Nd ranks are emulated as Nd gradient rows in one GPU's memory.
+ *
+ * Conventions shared by every entry point:
+ *   - Ownership: the caller owns all memory.  The library borrows the pointers
+ *     for stream-ordered work and allocates nothing.  Every call is
+ *     thread-safe; calls on one stream execute in order.
+ *   - Pointers named d_* or documented "device" must be device memory of the
+ *     current CUDA device; structs passed by pointer are host memory and are
+ *     read before the call returns.
+ *   - Errors: every call validates its arguments on the host first and returns
+ *     a zero_status_t without launching anything if they are invalid.  Kernel
+ *     work is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream); ZERO_ERR_CUDA reports a launch error.  No exception
+ *     crosses the ABI.  A nonfinite gradient is not an error: it is reported
+ *     through a device flag word (see below).
+ *   - Element sizes: gradients and gathered parameters are 2-byte elements
+ *     (binary16 or bfloat16); optimizer state is fp32.
+ *   - Arithmetic: fp32 with every operation correctly rounded and no fused
+ *     multiply-add; the reduction is a sequential left fold over ranks
+ *     0..Nd-1, so results do not depend on bucket size or launch shape.
+ */
+#ifndef ZERO_H
+#define ZERO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum zero_status {
+    ZERO_OK = 0,
+    ZERO_ERR_INVALID_ARG = 1,  /* NULL pointer, bad size, overflow, bad enum, overlap */
+    ZERO_ERR_ALIGNMENT = 2,    /* a pointer or stride breaks the documented alignment */
+    ZERO_ERR_CUDA = 3,         /* the CUDA runtime reported an error */
+    ZERO_ERR_TIMEOUT = 4,      /* a bounded wait expired (reserved) */
+    ZERO_ERR_UNSUPPORTED = 5   /* valid request this build does not implement */
+} zero_status_t;
+
+typedef enum zero_dtype {
+    ZERO_F16 = 0,   /* IEEE 754 binary16 */
+    ZERO_BF16 = 1   /* bfloat16 */
+} zero_dtype_t;
+
+/* Partition of a flat buffer of psi parameters over nd ranks (ZeRO-DP: equal
+ * partitions, each rank holds and updates only its own).  The last shards are
+ * zero-padded: S = ceil(psi / nd), rank r owns flat indices [r*S, r*S + length). */
+typedef struct zero_layout {
+    uint64_t psi;          /* parameters in the flat buffer */
+    uint32_t nd;           /* data-parallel degree */
+    uint32_t rank;         /* this rank, 0 <= rank < nd */
+    uint64_t shard_elems;  /* S = ceil(psi / nd) */
+    uint64_t begin;        /* rank * S: first flat index owned (the gathered slot) */
+    uint64_t length;       /* n_r = max(0, min(S, psi - begin)); 0 is a legal no-op */
+    uint64_t padded_elems; /* nd * S: length of the padded flat buffer */
+    uint64_t row_pitch;    /* S rounded up to row_align_elems: the emulated row pitch */
+} zero_layout_t;
+
+/* The Nd gradient contributions to one rank's shard, in device memory.  The
+ * contribution of rank j to shard element i is the 2-byte element
+ *     base[j * row_stride + offset + i],   0 <= j < nd.
+ * Full emulation (every rank's whole gradient resident): row j is rank j's
+ * gradient in padded-partition layout, row_stride = nd * row_pitch,
+ * offset = rank * row_pitch.  Shard view: row j holds only this shard,
+ * row_stride = row_pitch, offset = 0.
+ * Alignment: base 16-byte aligned; row_stride and offset multiples of 8. */
+typedef struct zero_grads {
+    const void* base;     /* device, read-only */
+    uint64_t row_stride;  /* elements between consecutive ranks' rows */
+    uint64_t offset;      /* element offset of this shard within every row */
+    uint32_t nd;          /* number of contributions (>= 1) */
+    int32_t dtype;        /* zero_dtype_t */
+} zero_grads_t;
+
+/* fp32 optimizer state of one shard, device pointers, each 16-byte aligned:
+ * master weights, Adam first moment m and second moment v. */
+typedef struct zero_state {
+    float* master;
+    float* m;
+    float* v;
+} zero_state_t;
+
+/* AdamW hyperparameters (Adam with bias correction and eps outside the square
+ * root; decoupled weight decay applied as p * (1 - lr * weight_decay)).  The
+ * step scalars are formed in fp64 from these values and rounded once to fp32:
+ * 1-beta1, 1-beta2, 1-beta1^t, 1-beta2^t, 1-lr*weight_decay. */
+typedef struct zero_adamw {
+    double lr;
+    double beta1;         /* in [0, 1) */
+    double beta2;         /* in [0, 1) */
+    double eps;           /* >= 0 */
+    double weight_decay;  /* >= 0 */
+    uint64_t step;        /* t >= 1, the step being taken */
+} zero_adamw_t;
+
+/* Text of a status code (static storage; never NULL). */
+const char* zero_status_string(zero_status_t status);
+
+/* The ZeRO-DP partition of rank `rank` ("ZeRO-DP", Stage 1: the state is split
+ * into Nd equal partitions).  row_align_elems (>= 1) rounds the emulated row
+ * pitch up to a multiple (8 keeps 2-byte rows 16-byte aligned).
+ * Host only.  ZERO_ERR_INVALID_ARG if out is NULL, nd == 0, rank >= nd,
+ * row_align_elems == 0 or nd * S overflows. */
+zero_status_t zero_partition_layout(uint64_t psi, uint32_t nd, uint32_t rank,
+                                    uint32_t row_align_elems, zero_layout_t* out);
+
+/* Per-rank model-state bytes of mixed-precision Adam ("Quantifying memory
+ * consumption": fp16 params 2, fp16 grads 2, K bytes of optimizer state per
+ * parameter, 16 bytes when K = 12) under stage 0 (plain data parallel),
+ * 1 (P_os: 4*psi + K*S), 2 (P_os+g: 2*psi + (2+K)*S) or 3 (P_os+g+p:
+ * (4+K)*S), with S = ceil(psi / nd) the parameters a rank holds; equal to
+ * the pages' formulas whenever nd divides psi.  Host only.
+ * Returns UINT64_MAX if nd == 0, stage > 3 or the result overflows. */
+uint64_t zero_model_state_bytes(uint64_t psi, uint32_t nd, uint32_t stage, uint32_t k);
+
+/* Reduce-scatter of one bucket (Stage 2, bucketed): for i in [0, bucket_len),
+ *     s_i = (((c_0 + c_1) + c_2) + ... + c_{nd-1})   in fp32, c_j at
+ *           g->base[j*row_stride + offset + bucket_begin + i],
+ *     cb_out[i] = s_i * inv_scale,
+ * and sets *d_nonfinite |= 1 if any s_i is inf or NaN (never clears it).
+ * cb_out: device fp32[bucket_len], 4-byte aligned, the constant-size fusion
+ * buffer; d_nonfinite: device uint32.  bucket_len == 0 is a no-op. */
+zero_status_t zero_reduce_scatter_bucket(const zero_grads_t* g, uint64_t bucket_begin,
+                                         uint64_t bucket_len, float inv_scale, float* cb_out,
+                                         uint32_t* d_nonfinite, void* stream);
+
+/* AdamW on n fp32 elements from an already reduced and scaled gradient:
+ *     m' = b1 m + (1-b1) g;  v' = b2 v + (1-b2) g^2;
+ *     p' = p (1 - lr wd) - lr (m'/(1-b1^t)) / (sqrt(v'/(1-b2^t)) + eps).
+ * grad: device fp32[n], 4-byte aligned.  in/out state: 16-byte aligned;
+ * out may equal in (in place) but may not partially overlap it. */
+zero_status_t zero_adam_step_shard(const float* grad, const zero_state_t* in,
+                                   const zero_state_t* out, uint64_t n,
+                                   const zero_adamw_t* h, void* stream);
+
+/* Cast of a shard's fp32 master weights into its slot of the gathered
+ * parameter buffer (the local part of the Stage-1 all-gather):
+ *     gathered[slot_offset_elems + i] = round_to_nearest_even(master[i]).
+ * master: device fp32[n], 4-byte aligned; gathered: device, 2-byte aligned
+ * (any slot phase; the store width follows it). */
+zero_status_t zero_gather_params_shard(const float* master, uint64_t n, void* gathered,
+                                       uint64_t slot_offset_elems, zero_dtype_t dtype,
+                                       void* stream);
+
+/* The fused shard step: reduce (1) + scale + AdamW (2) + cast into the
+ * gathered slot (3) in one pass per bucket, with the reduced gradient kept in
+ * registers (never materialised).  Shard length and Nd come from L (L->nd must
+ * equal g->nd).  The shard is walked in buckets of bucket_elems elements, one
+ * launch per bucket; results do not depend on bucket_elems.
+ * The new state goes to `out` and the cast parameters to
+ * gathered[gathered_offset_elems + i].  *d_nonfinite |= 1 if any reduced sum
+ * is nonfinite; the step is then to be skipped on every shard: with out != in
+ * the caller simply keeps `in` (and its previous gathered buffer).  With
+ * out == in the update happens in place and cannot be rolled back: run
+ * zero_check_nonfinite first.  loss_scale > 0 and finite; the gradient scale
+ * is fp32(1 / (nd * loss_scale)). */
+zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layout_t* L,
+                              const zero_state_t* in, const zero_state_t* out, void* gathered,
+                              uint64_t gathered_offset_elems, uint64_t bucket_elems,
+                              double loss_scale, const zero_adamw_t* h, uint32_t* d_nonfinite,
+                              void* stream);
+
+/* The same step unfused, through the constant-size fusion buffer: per bucket,
+ * zero_reduce_scatter_bucket into cb, then zero_adam_step_shard from cb, then
+ * zero_gather_params_shard.  cb: device fp32 workspace of cb_elems >=
+ * min(bucket_elems, L->length) + 4 elements, 16-byte aligned, owned by the
+ * caller and overwritten.  Bitwise identical results to zero_step_shard. */
+zero_status_t zero_step_shard_unfused(const zero_grads_t* g, const zero_layout_t* L,
+                                      const zero_state_t* in, const zero_state_t* out,
+                                      void* gathered, uint64_t gathered_offset_elems,
+                                      uint64_t bucket_elems, double loss_scale,
+                                      const zero_adamw_t* h, float* cb, uint64_t cb_elems,
+                                      uint32_t* d_nonfinite, void* stream);
+
+/* Pre-pass for in-place stepping: *d_nonfinite |= 1 if any reduced sum
+ * s_i (as in zero_reduce_scatter_bucket) over shard elements [begin, begin+n)
+ * is nonfinite.  Reads only the gradients (2 * nd bytes per element). */
+zero_status_t zero_check_nonfinite(const zero_grads_t* g, uint64_t begin, uint64_t n,
+                                   uint32_t* d_nonfinite, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO_H */

@@ -77,6 +77,9 @@ def _bind(L: C.CDLL) -> C.CDLL:
     L.orc_step_sharded.restype = i32
     L.orc_step_unsharded_f64.argtypes = [u64, u32, i32, vp, u64, dbl, C.POINTER(Hparams),
                                          u64, vp, vp, vp, vp, vp, vp]
+    L.orc_reduce_scaled.argtypes = [vp, i32, u32, u64, u64, u64, C.c_float, vp]
+    L.orc_reduce_scaled.restype = i32
+    L.orc_adamw_from_grad.argtypes = [u64, vp, C.POINTER(Hparams), u64, vp, vp, vp, vp, vp, vp]
     return L
 
 
@@ -167,6 +170,30 @@ def fold(grads: np.ndarray, dtype: int) -> np.ndarray:
     L = lib()
     return np.array([L.orc_fold(_p(grads), dtype, nd, n, i) for i in range(n)],
                     dtype=np.float32)
+
+
+def reduce_scaled(grads: np.ndarray, dtype: int, row_stride: int, offset: int, n: int,
+                  nd: int, inv_scale: float):
+    """(flag, out) of the reduce-scatter of shard window [offset, offset+n).
+    ``grads`` is a flat uint16 array; contributor j's element i is at
+    grads[j*row_stride + offset + i]."""
+    grads = np.ascontiguousarray(grads, dtype=np.uint16)
+    assert n == 0 or (nd - 1) * row_stride + offset + n <= grads.size
+    out = np.empty(max(n, 1), np.float32)
+    f = lib().orc_reduce_scaled(_p(grads), dtype, nd, row_stride, offset, n,
+                                float(np.float32(inv_scale)), _p(out))
+    return f, out[:n]
+
+
+def adamw_from_grad(g: np.ndarray, h: dict, t: int, p, m, v):
+    """(p', m', v') of AdamW from an fp32 reduced, scaled gradient."""
+    g, p, m, v = (np.ascontiguousarray(a, np.float32) for a in (g, p, m, v))
+    n = g.size
+    po, mo, vo = (np.empty(n, np.float32) for _ in range(3))
+    hp = hparams(h)
+    lib().orc_adamw_from_grad(n, _p(g), C.byref(hp), t, _p(p), _p(m), _p(v), _p(po), _p(mo),
+                              _p(vo))
+    return po, mo, vo
 
 
 def step_unsharded(grads: np.ndarray, dtype: int, loss_scale: float, h: dict, t: int,

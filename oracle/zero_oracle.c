@@ -249,6 +249,33 @@ static void adamw_elem(const orc_scalars_t* k, float g, float p, float m, float 
     *v_out = v1;
 }
 
+/* The reduce-scatter of one window: out[i] = fold(i) * fp32(inv_scale) for
+ * shard elements [offset, offset + n) of each row (inv_scale is given as the
+ * fp32 value the caller uses).  Returns 1 if any sum is nonfinite, else 0. */
+int orc_reduce_scaled(const void* grads, int dtype, uint32_t nd, uint64_t row_stride,
+                      uint64_t offset, uint64_t n, float inv_scale, float* out)
+{
+    int flag = 0;
+    for (uint64_t i = 0; i < n; ++i) {
+        float s = orc_fold(grads, dtype, nd, row_stride, offset + i);
+        if (!isfinite(s))
+            flag = 1;
+        out[i] = s * inv_scale;
+    }
+    return flag;
+}
+
+/* AdamW on n elements from an already reduced and scaled fp32 gradient. */
+void orc_adamw_from_grad(uint64_t n, const float* g, const orc_hparams_t* h, uint64_t t,
+                         const float* p, const float* m, const float* v, float* p_out,
+                         float* m_out, float* v_out)
+{
+    orc_scalars_t k;
+    orc_scalars(h, t, 1, 1.0, &k);
+    for (uint64_t i = 0; i < n; ++i)
+        adamw_elem(&k, g[i], p[i], m[i], v[i], &p_out[i], &m_out[i], &v_out[i]);
+}
+
 /* Unsharded data-parallel step over all Psi parameters.
  * grads: Nd rows, contributor j's gradient of element i at base[j*row_stride + i].
  * Returns 1 (and writes nothing) when any reduced sum is nonfinite; else 0,

@@ -302,6 +302,25 @@ def check_f64_shadow(orc):
         assert np.all(np.abs(v1 - vv) <= ev)
 
 
+def check_primitives_compose(orc):
+    """The bucket reduce and AdamW-from-gradient primitives compose to the
+    unsharded step (which the pins above tie to the library references)."""
+    rng = np.random.default_rng(23)
+    for dt, ls, nd in ((F16, 1024.0, 5), (BF16, 1.0, 64)):
+        n = 777
+        bits, p, m, v = _random_case(rng, nd, n, dt, ls)
+        _, p1, m1, v1, _ = orc.step_unsharded(bits, dt, ls, H, 7, p, m, v)
+        inv = orc.scalars(H, 7, nd, ls).inv
+        f, g = orc.reduce_scaled(bits.reshape(-1), dt, n, 0, n, nd, inv)
+        assert f == 0
+        q, mm, vv = orc.adamw_from_grad(g, H, 7, p, m, v)
+        for a, b in ((p1, q), (m1, mm), (v1, vv)):
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+        # a window in the middle of the rows
+        f, gw = orc.reduce_scaled(bits.reshape(-1), dt, n, 100, 50, nd, inv)
+        assert np.array_equal(gw.view(np.uint32), g[100:150].view(np.uint32))
+
+
 ALL = [check_codec, check_layout, check_accounting, check_fold, check_adamw_vs_torch,
        check_closed_forms, check_shard_invariant, check_bucket_invariance, check_skip,
-       check_f64_shadow]
+       check_f64_shadow, check_primitives_compose]

@@ -1,0 +1,188 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol declared in
+include/zero.h, its host-only entry points agree with the oracle, and invalid
+arguments are rejected on the host before anything is launched."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="session")
+def z():
+    from zero_sharded_optimizer_02_gb300 import build
+    build.build()
+    import zero_sharded_optimizer_02_gb300 as z
+    return z
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(zero_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_exports_every_declared_symbol(z):
+    names = declared_functions()
+    assert len(names) >= 9
+    raw = C.CDLL(z._abi.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+    assert set(z.exported_names()) == set(names)
+
+
+def test_layout_matches_oracle(z, orc):
+    for psi in list(range(0, 60)) + [350_000_017, 7_500_000_000]:
+        for nd in (1, 2, 3, 7, 16, 64):
+            for r in sorted({0, nd // 2, nd - 1}):
+                L = z.zero_partition_layout(psi, nd, r, 8)
+                s, b, n = orc.layout(psi, nd, r)
+                assert (L.shard_elems, L.begin, L.length) == (s, b, n)
+                assert L.padded_elems == nd * s and L.row_pitch == -(-s // 8) * 8
+                assert (L.psi, L.nd, L.rank) == (psi, nd, r)
+
+
+def test_layout_invalid(z):
+    for args in ((10, 0, 0, 8), (10, 4, 4, 8), (10, 4, 0, 0), (2 ** 64 - 1, 2, 0, 8)):
+        with pytest.raises(z.ZeroError) as e:
+            z.zero_partition_layout(*args)
+        assert e.value.status == z.ZERO_ERR_INVALID_ARG
+
+
+def test_accounting_matches_oracle_and_table(z, orc):
+    for psi in (0, 1, 5, 1_000_003, 1_500_000_000, 7_500_000_000):
+        for nd in (1, 3, 64, 1024):
+            for st in range(4):
+                for k in (12, 8):
+                    assert z.zero_model_state_bytes(psi, nd, st, k) == \
+                        orc.model_state_bytes(psi, nd, st, k)
+    assert z.zero_model_state_bytes(1_500_000_000, 1, 0, 12) == 24 * 10 ** 9
+    exp = {(64, 1): 31.4, (64, 2): 16.6, (64, 3): 1.88, (1024, 1): 30.1, (1024, 2): 15.1,
+           (1024, 3): 0.12}
+    for (nd, st), gb in exp.items():
+        dec = len(str(gb).split(".")[1])
+        assert round(z.zero_model_state_bytes(7_500_000_000, nd, st, 12) / 1e9, dec) == gb
+    assert z.zero_model_state_bytes(1, 0, 0, 12) == 2 ** 64 - 1
+    assert z.zero_model_state_bytes(1, 1, 4, 12) == 2 ** 64 - 1
+
+
+def test_status_strings(z):
+    for code in range(6):
+        assert z.zero_status_string(code).startswith("ZERO_")
+    assert "UNKNOWN" in z.zero_status_string(99)
+
+
+# Fake, never dereferenced device addresses: every call below fails host-side
+# validation before any CUDA call.
+A = 1 << 20   # 16-byte aligned
+
+
+def _h(z, step=1):
+    return z.adamw(1e-4, 0.9, 0.999, 1e-8, 0.01, step)
+
+
+def _state(z, base):
+    return z.state(base, base + (1 << 16), base + (2 << 16))
+
+
+@pytest.mark.parametrize("case,status", [
+    ("null_base", "ZERO_ERR_INVALID_ARG"), ("misaligned_base", "ZERO_ERR_ALIGNMENT"),
+    ("odd_row_stride", "ZERO_ERR_ALIGNMENT"), ("odd_offset", "ZERO_ERR_ALIGNMENT"),
+    ("bad_dtype", "ZERO_ERR_INVALID_ARG"), ("nd_zero", "ZERO_ERR_INVALID_ARG"),
+    ("nd_mismatch", "ZERO_ERR_INVALID_ARG"), ("misaligned_state", "ZERO_ERR_ALIGNMENT"),
+    ("overlap_state", "ZERO_ERR_INVALID_ARG"), ("bucket_zero", "ZERO_ERR_INVALID_ARG"),
+    ("step_zero", "ZERO_ERR_INVALID_ARG"), ("bad_beta", "ZERO_ERR_INVALID_ARG"),
+    ("bad_loss_scale", "ZERO_ERR_INVALID_ARG"), ("odd_gathered", "ZERO_ERR_ALIGNMENT"),
+    ("null_flag", "ZERO_ERR_INVALID_ARG"), ("row_overflow", "ZERO_ERR_INVALID_ARG"),
+])
+def test_step_shard_rejects(z, case, status):
+    L = z.zero_partition_layout(1000, 4, 1, 8)
+    g = z.grads(A, 4 * 256, 256, 4, "f16")
+    s_in, s_out = _state(z, 2 * A), _state(z, 4 * A)
+    gathered, flag, bucket, ls, h = 8 * A, 9 * A, 64, 1024.0, _h(z)
+    if case == "null_base":
+        g.base = None
+    elif case == "misaligned_base":
+        g.base = A + 8
+    elif case == "odd_row_stride":
+        g.row_stride = 1020
+    elif case == "odd_offset":
+        g.offset = 252
+    elif case == "bad_dtype":
+        g.dtype = 7
+    elif case == "nd_zero":
+        g.nd = 0
+    elif case == "nd_mismatch":
+        g.nd = 3
+    elif case == "misaligned_state":
+        s_out.m = s_out.m + 4
+    elif case == "overlap_state":
+        s_out.m = s_in.m + 16
+    elif case == "bucket_zero":
+        bucket = 0
+    elif case == "step_zero":
+        h = _h(z, 0)
+    elif case == "bad_beta":
+        h.beta1 = 1.0
+    elif case == "bad_loss_scale":
+        ls = 0.0
+    elif case == "odd_gathered":
+        gathered += 1
+    elif case == "null_flag":
+        flag = None
+    elif case == "row_overflow":
+        g.row_stride = 1 << 62
+    with pytest.raises(z.ZeroError) as e:
+        z.zero_step_shard(g, L, s_in, s_out, gathered, L.begin, bucket, ls, h, flag)
+    assert e.value.status == getattr(z, status)
+    # the unfused variant validates the same way, plus its workspace
+    if case in ("misaligned_base", "overlap_state", "bucket_zero"):
+        with pytest.raises(z.ZeroError) as e:
+            z.zero_step_shard_unfused(g, L, s_in, s_out, gathered, L.begin, bucket, ls, h,
+                                      10 * A, 1 << 20, flag)
+        assert e.value.status == getattr(z, status)
+
+
+def test_primitives_reject(z):
+    g = z.grads(A, 1024, 0, 4, "bf16")
+    with pytest.raises(z.ZeroError) as e:
+        z.zero_reduce_scatter_bucket(g, 0, 100, 1.0, A + 2, 9 * A)
+    assert e.value.status == z.ZERO_ERR_ALIGNMENT
+    with pytest.raises(z.ZeroError) as e:
+        z.zero_reduce_scatter_bucket(g, 0, 100, 1.0, None, 9 * A)
+    assert e.value.status == z.ZERO_ERR_INVALID_ARG
+    with pytest.raises(z.ZeroError) as e:
+        z.zero_check_nonfinite(z.grads(A + 4, 1024, 0, 4, "bf16"), 0, 10, 9 * A)
+    assert e.value.status == z.ZERO_ERR_ALIGNMENT
+    with pytest.raises(z.ZeroError) as e:
+        z.zero_adam_step_shard(A + 2, _state(z, 2 * A), _state(z, 4 * A), 10, _h(z))
+    assert e.value.status == z.ZERO_ERR_ALIGNMENT
+    with pytest.raises(z.ZeroError) as e:   # gradient overlapping an output
+        z.zero_adam_step_shard(4 * A, _state(z, 2 * A), _state(z, 4 * A), 10, _h(z))
+    assert e.value.status == z.ZERO_ERR_INVALID_ARG
+    with pytest.raises(z.ZeroError) as e:
+        z.zero_gather_params_shard(A, 10, A + 1, 0, "f16")
+    assert e.value.status == z.ZERO_ERR_ALIGNMENT
+    with pytest.raises(z.ZeroError) as e:
+        z.zero_gather_params_shard(A, 10, 2 * A, 0, 5)
+    assert e.value.status == z.ZERO_ERR_INVALID_ARG
+    with pytest.raises(z.ZeroError) as e:   # workspace too small
+        L = z.zero_partition_layout(1000, 4, 1, 8)
+        z.zero_step_shard_unfused(z.grads(A, 4 * 256, 256, 4, "f16"), L, _state(z, 2 * A),
+                                  _state(z, 4 * A), 8 * A, L.begin, 64, 1024.0, _h(z), 10 * A,
+                                  60, 9 * A)
+    assert e.value.status == z.ZERO_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    import zero_sharded_optimizer_02_gb300._abi as abi
+    monkeypatch.setattr(abi, "_lib", None)
+    monkeypatch.setattr(abi, "LIB_PATH", str(tmp_path / "libzero.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        abi.lib()

@@ -1,0 +1,106 @@
+"""Full-size workloads on the GPU in the launch configuration the benchmark
+times, checked against the oracle on sampled elements (the oracle computes
+any element on its own from the seeded generator) and through properties that
+hold at any size (padding untouched, skip decisions, step count).
+
+Workloads: GPT-2-small-sized ZeRO-2 shard (psi = 124,439,808, Nd = 8, bf16,
+10 steps); padding and overflow (psi = 350,000,017, Nd = 16, fp16 x 1024,
+all 16 ranks, +inf planted at step 5); GPT-2 1.5B shard view (Nd = 64, fp16,
+20 steps); 7.5B shard view (Nd = 64, bf16, bucket 5e8, 20 steps).
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import (assert_params_close, assert_state_close, f32, full_rows, make_group,
+                      oracle_trajectory, sample_indices, shard_rows, u16)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from zero_sharded_optimizer_02_gb300 import build
+    build.build()
+    oracle.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+@pytest.fixture(autouse=True)
+def free_memory():
+    yield
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def _sampled_state(dps, idx):
+    """Current state and gathered params of the group at flat indices idx."""
+    s = int(dps.layouts[dps.ranks[0]].shard_elems)
+    out = [np.empty(idx.size, np.float32) for _ in range(3)]
+    params = u16(dps.gathered_view()[torch.from_numpy(idx).to(dps.device)])
+    for r in dps.ranks:
+        sel = (idx // s) == r
+        if not sel.any():
+            continue
+        local = torch.from_numpy(idx[sel] - r * s).to(dps.device)
+        for i, t in enumerate(dps.state[r].tensors("cur")):
+            out[i][sel] = f32(t[local])
+    return out, params
+
+
+def _check(dps, idx, entry, what):
+    p, m, v, params, t = entry
+    (gp, gm, gv), gparams = _sampled_state(dps, idx)
+    assert_state_close(gp, p, 1e-12, f"{what} master")
+    assert_state_close(gm, m, 1e-20, f"{what} m")
+    assert_state_close(gv, v, 1e-20, f"{what} v")
+    if params is not None:
+        assert_params_close(gparams, params, f"{what} params")
+    assert dps.t == t, what
+
+
+@pytest.mark.parametrize("key,rank", [("c1", 0), ("c1", 5), ("c3", 0), ("c3", 1), ("c4", 0),
+                                      ("c4", 63)])
+def test_shard_view_sampled(key, rank):
+    w = synth.WORKLOADS[key]
+    dps = make_group(w, ranks=[rank])
+    idx = sample_indices(w.psi, w.nd, [rank], 2048, seed=rank + 17)
+    _, hist = oracle_trajectory(w, idx, w.steps)
+    buf = None
+    for k in range(w.steps):
+        if buf is None or w.fresh_grads:
+            buf, desc = shard_rows(w, dps, rank, k, buf)
+        assert not dps.step(desc)
+        if k in (0, w.steps - 1) or w.fresh_grads:
+            _check(dps, idx, hist[k], f"{key} rank {rank} step {k}")
+    L = dps.layouts[rank]
+    n = int(L.length)
+    for b in dps.state[rank].bufs:
+        assert not b[:, n:].any()
+
+
+def test_c2_padding_and_overflow_all_ranks():
+    w = synth.WORKLOADS["c2"]
+    step_plant, j_plant, flat_plant = w.plant
+    dps = make_group(w)
+    idx = sample_indices(w.psi, w.nd, range(w.nd), 512, seed=2, extra=[flat_plant])
+    _, hist = oracle_trajectory(w, idx, w.steps)
+    s = int(dps.layouts[0].shard_elems)
+    pitch = int(dps.layouts[0].row_pitch)
+    buf, desc = full_rows(w, dps, 0)
+    for k in range(w.steps):
+        if k == step_plant:
+            buf[j_plant, (flat_plant // s) * pitch + flat_plant % s] = float("inf")
+        skipped = dps.step(desc)
+        assert skipped == (k == step_plant), k
+        _check(dps, idx, hist[k], f"c2 step {k}")
+    assert dps.t == step_plant and dps.skipped_steps == [False] * step_plant + [True]
+    # the 15 padding parameters of the last shard are never written
+    for g in dps.gathered:
+        assert not g[w.psi:].view(torch.int16).any()
+    last = dps.layouts[w.nd - 1]
+    assert int(last.length) == 21_874_987 and w.nd * s - w.psi == 15

@@ -1,0 +1,13 @@
+"""GB300-native ZeRO partitioned optimizer step (one data-parallel rank).
+
+The compute path is ``libzero.so`` (CUDA kernels for sm_103a behind the C ABI
+of ``include/zero.h``); ``_abi`` binds it with the same function names and
+``step`` drives it with the global skip/commit rule.  There is no CPU
+fallback: without the built library every entry point raises.
+"""
+from ._abi import (  # noqa: F401
+    ZERO_BF16, ZERO_ERR_ALIGNMENT, ZERO_ERR_CUDA, ZERO_ERR_INVALID_ARG, ZERO_ERR_TIMEOUT,
+    ZERO_ERR_UNSUPPORTED, ZERO_F16, ZERO_OK, AdamW, Grads, Layout, State, ZeroError, adamw,
+    exported_names, grads, lib, state, zero_adam_step_shard, zero_check_nonfinite,
+    zero_gather_params_shard, zero_model_state_bytes, zero_partition_layout,
+    zero_reduce_scatter_bucket, zero_status_string, zero_step_shard, zero_step_shard_unfused)

@@ -1,0 +1,186 @@
+"""ctypes binding of libzero.so: the C ABI of ``include/zero.h``, same names.
+
+Argument marshalling only: every step of the optimizer runs in the library's
+CUDA kernels.  Pointer arguments accept an int address or any object with a
+``data_ptr()`` method (a torch tensor); ``stream`` accepts an int handle, a
+``torch.cuda.Stream`` or None (the legacy default stream).  A non-OK status
+raises ``ZeroError``.  There is no fallback: if the library is missing, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libzero.so")
+
+ZERO_OK, ZERO_ERR_INVALID_ARG, ZERO_ERR_ALIGNMENT, ZERO_ERR_CUDA = 0, 1, 2, 3
+ZERO_ERR_TIMEOUT, ZERO_ERR_UNSUPPORTED = 4, 5
+ZERO_F16, ZERO_BF16 = 0, 1
+DTYPES = {"f16": ZERO_F16, "bf16": ZERO_BF16}
+UINT64_MAX = (1 << 64) - 1
+
+u64, u32, i32, vp, dbl = C.c_uint64, C.c_uint32, C.c_int32, C.c_void_p, C.c_double
+
+
+class ZeroError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {zero_status_string(status)} ({status})")
+
+
+class Layout(C.Structure):
+    _fields_ = [("psi", u64), ("nd", u32), ("rank", u32), ("shard_elems", u64), ("begin", u64),
+                ("length", u64), ("padded_elems", u64), ("row_pitch", u64)]
+
+
+class Grads(C.Structure):
+    _fields_ = [("base", vp), ("row_stride", u64), ("offset", u64), ("nd", u32), ("dtype", i32)]
+
+
+class State(C.Structure):
+    _fields_ = [("master", vp), ("m", vp), ("v", vp)]
+
+
+class AdamW(C.Structure):
+    _fields_ = [("lr", dbl), ("beta1", dbl), ("beta2", dbl), ("eps", dbl),
+                ("weight_decay", dbl), ("step", u64)]
+
+
+_lib: C.CDLL | None = None
+
+_SIGNATURES = {
+    "zero_status_string": ([i32], C.c_char_p),
+    "zero_partition_layout": ([u64, u32, u32, u32, C.POINTER(Layout)], i32),
+    "zero_model_state_bytes": ([u64, u32, u32, u32], u64),
+    "zero_reduce_scatter_bucket": ([C.POINTER(Grads), u64, u64, C.c_float, vp, vp, vp], i32),
+    "zero_adam_step_shard": ([vp, C.POINTER(State), C.POINTER(State), u64, C.POINTER(AdamW),
+                              vp], i32),
+    "zero_gather_params_shard": ([vp, u64, vp, u64, i32, vp], i32),
+    "zero_step_shard": ([C.POINTER(Grads), C.POINTER(Layout), C.POINTER(State),
+                         C.POINTER(State), vp, u64, u64, dbl, C.POINTER(AdamW), vp, vp], i32),
+    "zero_step_shard_unfused": ([C.POINTER(Grads), C.POINTER(Layout), C.POINTER(State),
+                                 C.POINTER(State), vp, u64, u64, dbl, C.POINTER(AdamW), vp, u64,
+                                 vp, vp], i32),
+    "zero_check_nonfinite": ([C.POINTER(Grads), u64, u64, vp, vp], i32),
+}
+
+
+def lib() -> C.CDLL:
+    """The loaded library (raises if it was not built: there is no fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libzero.so not found at {LIB_PATH}; build it with "
+                "zero_sharded_optimizer_02_gb300.build.build() (there is no CPU fallback)")
+        L = C.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def exported_names() -> list[str]:
+    return list(_SIGNATURES)
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != ZERO_OK:
+        raise ZeroError(status, where)
+
+
+# -- descriptors -------------------------------------------------------------
+
+def grads(base, row_stride: int, offset: int, nd: int, dtype) -> Grads:
+    dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+    return Grads(_ptr(base), row_stride, offset, nd, dt)
+
+
+def state(master, m, v) -> State:
+    return State(_ptr(master), _ptr(m), _ptr(v))
+
+
+def adamw(lr: float, beta1: float, beta2: float, eps: float, weight_decay: float,
+          step: int) -> AdamW:
+    return AdamW(lr, beta1, beta2, eps, weight_decay, step)
+
+
+# -- entry points ------------------------------------------------------------
+
+def zero_status_string(status: int) -> str:
+    return lib().zero_status_string(status).decode()
+
+
+def zero_partition_layout(psi: int, nd: int, rank: int, row_align_elems: int = 8) -> Layout:
+    out = Layout()
+    _check(lib().zero_partition_layout(psi, nd, rank, row_align_elems, C.byref(out)),
+           "zero_partition_layout")
+    return out
+
+
+def zero_model_state_bytes(psi: int, nd: int, stage: int, k: int = 12) -> int:
+    return int(lib().zero_model_state_bytes(psi, nd, stage, k))
+
+
+def zero_reduce_scatter_bucket(g: Grads, bucket_begin: int, bucket_len: int, inv_scale: float,
+                               cb_out, d_nonfinite, stream=None) -> None:
+    _check(lib().zero_reduce_scatter_bucket(C.byref(g), bucket_begin, bucket_len, inv_scale,
+                                            _ptr(cb_out), _ptr(d_nonfinite), _stream(stream)),
+           "zero_reduce_scatter_bucket")
+
+
+def zero_adam_step_shard(grad, s_in: State, s_out: State, n: int, h: AdamW,
+                         stream=None) -> None:
+    _check(lib().zero_adam_step_shard(_ptr(grad), C.byref(s_in), C.byref(s_out), n, C.byref(h),
+                                      _stream(stream)), "zero_adam_step_shard")
+
+
+def zero_gather_params_shard(master, n: int, gathered, slot_offset_elems: int, dtype,
+                             stream=None) -> None:
+    dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+    _check(lib().zero_gather_params_shard(_ptr(master), n, _ptr(gathered), slot_offset_elems,
+                                          dt, _stream(stream)), "zero_gather_params_shard")
+
+
+def zero_step_shard(g: Grads, L: Layout, s_in: State, s_out: State, gathered,
+                    gathered_offset_elems: int, bucket_elems: int, loss_scale: float, h: AdamW,
+                    d_nonfinite, stream=None) -> None:
+    _check(lib().zero_step_shard(C.byref(g), C.byref(L), C.byref(s_in), C.byref(s_out),
+                                 _ptr(gathered), gathered_offset_elems, bucket_elems, loss_scale,
+                                 C.byref(h), _ptr(d_nonfinite), _stream(stream)),
+           "zero_step_shard")
+
+
+def zero_step_shard_unfused(g: Grads, L: Layout, s_in: State, s_out: State, gathered,
+                            gathered_offset_elems: int, bucket_elems: int, loss_scale: float,
+                            h: AdamW, cb, cb_elems: int, d_nonfinite, stream=None) -> None:
+    _check(lib().zero_step_shard_unfused(C.byref(g), C.byref(L), C.byref(s_in), C.byref(s_out),
+                                         _ptr(gathered), gathered_offset_elems, bucket_elems,
+                                         loss_scale, C.byref(h), _ptr(cb), cb_elems,
+                                         _ptr(d_nonfinite), _stream(stream)),
+           "zero_step_shard_unfused")
+
+
+def zero_check_nonfinite(g: Grads, begin: int, n: int, d_nonfinite, stream=None) -> None:
+    _check(lib().zero_check_nonfinite(C.byref(g), begin, n, _ptr(d_nonfinite), _stream(stream)),
+           "zero_check_nonfinite")

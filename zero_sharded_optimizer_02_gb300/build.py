@@ -1,0 +1,77 @@
+"""Builds libzero.so in-tree: the CUDA kernels for sm_103a plus the host C++.
+
+Two translation units are compiled in parallel and linked with the static
+CUDA runtime, so the library loads without a GPU (symbol checks) and needs no
+library path at run time.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+OUT = os.path.join(PKG, "libzero.so")
+BUILD = os.path.join(PKG, "_build")
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+SOURCES = {
+    "zero_kernels.cu": ["nvcc", "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC",
+                        "-Xptxas", "-v", "-I", INCLUDE, "-c"],
+    "zero_host.cpp": ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-Wextra", "-I", INCLUDE,
+                      "-c"],
+}
+
+
+def _nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    return "nvcc"
+
+
+def _stale(target: str, deps: list[str]) -> bool:
+    if not os.path.exists(target):
+        return True
+    t = os.path.getmtime(target)
+    return any(os.path.getmtime(d) > t for d in deps)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    os.makedirs(BUILD, exist_ok=True)
+    headers = [os.path.join(INCLUDE, "zero.h"), os.path.join(CSRC, "zero_internal.h")]
+    objs, procs = [], []
+    for src, cmd in SOURCES.items():
+        path = os.path.join(CSRC, src)
+        obj = os.path.join(BUILD, src + ".o")
+        objs.append(obj)
+        if force or _stale(obj, [path, *headers, __file__]):
+            cmd = list(cmd)
+            if cmd[0] == "nvcc":
+                cmd[0] = _nvcc()
+            log = open(obj + ".log", "w")
+            procs.append((src, obj, log, subprocess.Popen(cmd + [path, "-o", obj], stdout=log,
+                                                          stderr=subprocess.STDOUT)))
+    failed = []
+    for src, obj, log, p in procs:
+        rc = p.wait()
+        log.close()
+        text = open(obj + ".log").read()
+        if verbose or rc != 0:
+            sys.stderr.write(f"--- {src} ---\n{text}")
+        if rc != 0:
+            failed.append(src)
+    if failed:
+        raise RuntimeError(f"compilation failed: {failed}")
+    if force or _stale(OUT, objs):
+        tmp = OUT + f".tmp{os.getpid()}"
+        subprocess.check_call([_nvcc(), "-shared", *ARCH, "-o", tmp, *objs])
+        os.replace(tmp, OUT)
+    return OUT
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose=True))

@@ -1,0 +1,34 @@
+// Internal declarations shared by the host and device translation units of
+// the ZeRO shard-step library.  Not part of the public ABI (see zero.h).
+#pragma once
+
+#include <stdint.h>
+
+#include "zero.h"
+
+namespace zero {
+
+// fp32 step scalars.  Each is formed in fp64 from the caller's
+// hyperparameters and rounded once to fp32, so the device arithmetic sees
+// exactly these values.
+struct StepScalars {
+    float inv;   // 1 / (nd * loss_scale): gradient scale
+    float b1;    // beta1
+    float b2;    // beta2
+    float c1;    // 1 - beta1
+    float c2;    // 1 - beta2
+    float bc1;   // 1 - beta1^t
+    float bc2;   // 1 - beta2^t
+    float lr;
+    float eps;
+    float wdf;   // 1 - lr * weight_decay
+};
+
+// Validates h (t >= 1, betas in [0,1), lr, eps, wd finite and >= 0).
+bool adamw_valid(const zero_adamw_t* h);
+
+// Scalars of step h->step; nd and loss_scale give the gradient scale
+// (pass nd = 1, loss_scale = 1 when the gradient is already scaled).
+StepScalars make_scalars(const zero_adamw_t* h, uint32_t nd, double loss_scale);
+
+}  // namespace zero

@@ -1,0 +1,785 @@
+// Device kernels and launchers of the ZeRO shard-step C ABI (sm_103a).
+//
+// One data-parallel rank's partitioned optimizer step ("ZeRO: Memory
+// Optimizations Toward Training Trillion Parameter Models", section "ZeRO-DP":
+// Stage 2 reduce-scatters gradients bucket by bucket, each rank updates only
+// its 1/Nd of the fp32 optimizer state, Stage 1 all-gathers the parameters),
+// with the Nd ranks' gradients emulated as Nd rows in this GPU's memory.
+//
+// The step is elementwise and HBM-bound: at Nd = 64 a parameter costs
+// 2*Nd + 26 bytes (Nd 2-byte gradient reads, 12 B of fp32 state read, 12 B
+// written, 2 B cast out) for ~Nd + 30 flops, so the kernels are 128-bit
+// streaming loops over a grid sized to the SM count, not tensor-core work.
+//
+// Bit-exactness: every fp32 operation is an explicit correctly rounded
+// intrinsic (__fadd_rn/__fmul_rn/__fdiv_rn/__fsqrt_rn), so no multiply-add is
+// contracted, and the reduction is a per-element sequential fold over ranks
+// 0..Nd-1.  Warp votes are used only for the nonfinite flag.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zero.h"
+#include "zero_internal.h"
+
+namespace zero {
+namespace {
+
+constexpr int kThreads = 256;       // threads per CTA
+#ifndef ZERO_CTAS_PER_SM
+#define ZERO_CTAS_PER_SM 2
+#endif
+#ifndef ZERO_RANK_UNROLL
+#define ZERO_RANK_UNROLL 8
+#endif
+// Reduction kernels: resident CTAs per SM (2 x 256 threads leaves ~114
+// registers a thread, enough for 8 rows of 16-byte loads in flight with no
+// spills) and rank rows loaded back to back per thread.
+constexpr int kCtasPerSm = ZERO_CTAS_PER_SM;
+constexpr int kRankUnroll = ZERO_RANK_UNROLL;
+// Elementwise kernels (AdamW from fp32, cast): full occupancy.
+constexpr int kCtasPerSmLight = 8;
+
+// ---------------------------------------------------------------------------
+// Memory access helpers
+// ---------------------------------------------------------------------------
+
+// 16-byte read of gradient data that is used once: bypass L1, hint the L2
+// to fetch the whole 256-byte sector group.
+__device__ __forceinline__ uint4 ld_grad16(const uint16_t* p)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint16_t ld_grad2(const uint16_t* p)
+{
+    uint16_t r;
+    asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
+    return r;
+}
+
+// Two 16-bit elements packed in a word (element 0 in the low half) to fp32;
+// both conversions are exact.
+template <int DT>
+__device__ __forceinline__ float2 widen2(uint32_t w)
+{
+    if (DT == ZERO_F16) {
+        __half2 h;
+        static_assert(sizeof(h) == sizeof(w), "half2 is one word");
+        memcpy(&h, &w, sizeof(w));
+        return __half22float2(h);
+    } else {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ float widen1(uint16_t b)
+{
+    if (DT == ZERO_F16)
+        return __half2float(__ushort_as_half(b));
+    return __uint_as_float((uint32_t)b << 16);
+}
+
+// Round-to-nearest-even fp32 -> fp16/bf16 bits.
+template <int DT>
+__device__ __forceinline__ uint16_t narrow1(float x)
+{
+    if (DT == ZERO_F16)
+        return __half_as_ushort(__float2half_rn(x));
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ bool nonfinite(float x)
+{
+    return (__float_as_uint(x) & 0x7F800000u) == 0x7F800000u;   // exponent all ones
+}
+
+template <int DT>
+__device__ __forceinline__ void set8(float (&a)[8], uint4 w)
+{
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = widen2<DT>(ws[i]);
+        a[2 * i] = f.x;
+        a[2 * i + 1] = f.y;
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ void add8(float (&a)[8], uint4 w)
+{
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = widen2<DT>(ws[i]);
+        a[2 * i] = __fadd_rn(a[2 * i], f.x);
+        a[2 * i + 1] = __fadd_rn(a[2 * i + 1], f.y);
+    }
+}
+
+// Rank-ordered fold of 8 consecutive elements: acc = ((c_0 + c_1) + ...) +
+// c_{nd-1}.  Rows are loaded kRankUnroll at a time so that many 16-byte
+// reads are in flight per thread; the adds still run in rank order.
+template <int DT>
+__device__ __forceinline__ void fold8(const uint16_t* gp, uint64_t row_stride, uint32_t nd,
+                                      float (&acc)[8])
+{
+    set8<DT>(acc, ld_grad16(gp));
+    for (uint32_t j0 = 1; j0 < nd; j0 += kRankUnroll) {
+        uint4 w[kRankUnroll];
+#pragma unroll
+        for (int u = 0; u < kRankUnroll; ++u)
+            if (j0 + u < nd)
+                w[u] = ld_grad16(gp + (uint64_t)(j0 + u) * row_stride);
+#pragma unroll
+        for (int u = 0; u < kRankUnroll; ++u)
+            if (j0 + u < nd)
+                add8<DT>(acc, w[u]);
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ float fold1(const uint16_t* gp, uint64_t row_stride, uint32_t nd)
+{
+    float s = widen1<DT>(ld_grad2(gp));
+    for (uint32_t j = 1; j < nd; ++j)
+        s = __fadd_rn(s, widen1<DT>(ld_grad2(gp + (uint64_t)j * row_stride)));
+    return s;
+}
+
+// AdamW on one element (decoupled weight decay, bias correction, eps outside
+// the square root), every operation correctly rounded.
+__device__ __forceinline__ void adamw1(const StepScalars& k, float g, float& p, float& m,
+                                       float& v)
+{
+    const float m1 = __fadd_rn(__fmul_rn(k.b1, m), __fmul_rn(k.c1, g));
+    const float v1 = __fadd_rn(__fmul_rn(k.b2, v), __fmul_rn(k.c2, __fmul_rn(g, g)));
+    const float m_hat = __fdiv_rn(m1, k.bc1);
+    const float v_hat = __fdiv_rn(v1, k.bc2);
+    const float u = __fdiv_rn(m_hat, __fadd_rn(__fsqrt_rn(v_hat), k.eps));
+    p = __fsub_rn(__fmul_rn(p, k.wdf), __fmul_rn(k.lr, u));
+    m = m1;
+    v = v1;
+}
+
+// Store 8 consecutive 16-bit values (packed in 4 words) at q, using the
+// widest stores the address phase allows (W = 16, 8, 4 or 2 bytes).
+template <int W>
+__device__ __forceinline__ void store8(uint16_t* q, const uint32_t (&w)[4])
+{
+    if (W == 16) {
+        __stcs(reinterpret_cast<uint4*>(q), make_uint4(w[0], w[1], w[2], w[3]));
+    } else if (W == 8) {
+        __stcs(reinterpret_cast<uint2*>(q), make_uint2(w[0], w[1]));
+        __stcs(reinterpret_cast<uint2*>(q + 4), make_uint2(w[2], w[3]));
+    } else if (W == 4) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            __stcs(reinterpret_cast<unsigned int*>(q + 2 * i), w[i]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __stcs(reinterpret_cast<unsigned short*>(q + 2 * i), (unsigned short)(w[i] & 0xFFFF));
+            __stcs(reinterpret_cast<unsigned short*>(q + 2 * i + 1), (unsigned short)(w[i] >> 16));
+        }
+    }
+}
+
+__device__ __forceinline__ void flag_if_any(bool bad, uint32_t* flag)
+{
+    if (__any_sync(0xFFFFFFFFu, bad) && (threadIdx.x & 31) == 0)
+        atomicOr(flag, 1u);
+}
+
+// ---------------------------------------------------------------------------
+// Kernels
+// ---------------------------------------------------------------------------
+
+// Element split of a window [0, len): `head` scalar elements up to the first
+// 16-byte aligned gradient element, `nvec` 8-element vectors, then a scalar
+// tail.  Scalar elements are handled by the first threads of the grid.
+struct Split {
+    uint64_t len;
+    uint64_t head;
+    uint64_t nvec;
+    __host__ __device__ __forceinline__ uint64_t nscalar() const { return len - 8 * nvec; }
+    __host__ __device__ __forceinline__ uint64_t scalar_elem(uint64_t t) const
+    {
+        return t < head ? t : head + 8 * nvec + (t - head);
+    }
+};
+
+struct FusedArgs {
+    const uint16_t* g;     // element 0 of the window in row 0
+    uint64_t row_stride;   // elements
+    uint32_t nd;
+    Split sp;
+    const float* p_in;
+    const float* m_in;
+    const float* v_in;
+    float* p_out;
+    float* m_out;
+    float* v_out;
+    uint16_t* gath;        // gathered element of window element 0
+    StepScalars k;
+    uint32_t* flag;
+};
+
+// K4: fused reduce + scale + AdamW + cast, one pass over the window.
+template <int DT, int W>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) k_step_fused(const FusedArgs a)
+{
+    bool bad = false;
+    const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
+    const uint64_t nthr = (uint64_t)gridDim.x * kThreads;
+
+    if (tid < a.sp.nscalar()) {
+        const uint64_t e = a.sp.scalar_elem(tid);
+        const float s = fold1<DT>(a.g + e, a.row_stride, a.nd);
+        bad |= nonfinite(s);
+        float p = a.p_in[e], m = a.m_in[e], v = a.v_in[e];
+        adamw1(a.k, __fmul_rn(s, a.k.inv), p, m, v);
+        a.p_out[e] = p;
+        a.m_out[e] = m;
+        a.v_out[e] = v;
+        a.gath[e] = narrow1<DT>(p);
+    }
+
+    for (uint64_t q = tid; q < a.sp.nvec; q += nthr) {
+        const uint64_t e = a.sp.head + 8 * q;
+        float s[8];
+        fold8<DT>(a.g + e, a.row_stride, a.nd, s);
+        uint32_t out16[4];
+        // Epilogue in two halves of 4 elements to bound live registers.
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float4 pp = __ldcs(reinterpret_cast<const float4*>(a.p_in + e) + h);
+            const float4 mm = __ldcs(reinterpret_cast<const float4*>(a.m_in + e) + h);
+            const float4 vv = __ldcs(reinterpret_cast<const float4*>(a.v_in + e) + h);
+            float p[4] = {pp.x, pp.y, pp.z, pp.w};
+            float m[4] = {mm.x, mm.y, mm.z, mm.w};
+            float v[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                bad |= nonfinite(s[4 * h + i]);
+                adamw1(a.k, __fmul_rn(s[4 * h + i], a.k.inv), p[i], m[i], v[i]);
+            }
+            __stcs(reinterpret_cast<float4*>(a.p_out + e) + h, make_float4(p[0], p[1], p[2], p[3]));
+            __stcs(reinterpret_cast<float4*>(a.m_out + e) + h, make_float4(m[0], m[1], m[2], m[3]));
+            __stcs(reinterpret_cast<float4*>(a.v_out + e) + h, make_float4(v[0], v[1], v[2], v[3]));
+            out16[2 * h] = (uint32_t)narrow1<DT>(p[0]) | ((uint32_t)narrow1<DT>(p[1]) << 16);
+            out16[2 * h + 1] = (uint32_t)narrow1<DT>(p[2]) | ((uint32_t)narrow1<DT>(p[3]) << 16);
+        }
+        store8<W>(a.gath + e, out16);
+    }
+    flag_if_any(bad, a.flag);
+}
+
+struct ReduceArgs {
+    const uint16_t* g;
+    uint64_t row_stride;
+    uint32_t nd;
+    Split sp;
+    float inv;
+    float* cb;             // cb[i] for window element i (nullptr: check only)
+    uint32_t* flag;
+};
+
+// K1 (cb != nullptr): reduce-scatter of one bucket into the fusion buffer.
+// K5 (cb == nullptr): the nonfinite pre-check, gradients read only.
+// VEC: cb + head is 16-byte aligned, so the body stores float4s.
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) k_reduce(const ReduceArgs a)
+{
+    bool bad = false;
+    const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
+    const uint64_t nthr = (uint64_t)gridDim.x * kThreads;
+    if (tid < a.sp.nscalar()) {
+        const uint64_t e = a.sp.scalar_elem(tid);
+        const float s = fold1<DT>(a.g + e, a.row_stride, a.nd);
+        bad |= nonfinite(s);
+        if (a.cb)
+            a.cb[e] = __fmul_rn(s, a.inv);
+    }
+    for (uint64_t q = tid; q < a.sp.nvec; q += nthr) {
+        const uint64_t e = a.sp.head + 8 * q;
+        float s[8];
+        fold8<DT>(a.g + e, a.row_stride, a.nd, s);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            bad |= nonfinite(s[i]);
+            s[i] = __fmul_rn(s[i], a.inv);
+        }
+        if (a.cb) {
+            if (VEC) {
+                __stcg(reinterpret_cast<float4*>(a.cb + e), make_float4(s[0], s[1], s[2], s[3]));
+                __stcg(reinterpret_cast<float4*>(a.cb + e) + 1, make_float4(s[4], s[5], s[6], s[7]));
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    __stcg(a.cb + e + i, s[i]);
+            }
+        }
+    }
+    flag_if_any(bad, a.flag);
+}
+
+struct AdamArgs {
+    const float* g;
+    const float* p_in;
+    const float* m_in;
+    const float* v_in;
+    float* p_out;
+    float* m_out;
+    float* v_out;
+    uint64_t n;
+    uint64_t head;         // scalar elements before the common 16-byte phase (VEC)
+    uint64_t nvec;         // 4-element vectors (VEC)
+    StepScalars k;
+};
+
+// K2: AdamW from an fp32 reduced gradient.  VEC: every pointer shares one
+// 16-byte phase, so the body runs on float4s; otherwise all elements scalar.
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads, kCtasPerSmLight) k_adam(const AdamArgs a)
+{
+    const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
+    const uint64_t nthr = (uint64_t)gridDim.x * kThreads;
+    if (!VEC) {
+        for (uint64_t e = tid; e < a.n; e += nthr) {
+            float p = a.p_in[e], m = a.m_in[e], v = a.v_in[e];
+            adamw1(a.k, a.g[e], p, m, v);
+            a.p_out[e] = p;
+            a.m_out[e] = m;
+            a.v_out[e] = v;
+        }
+        return;
+    }
+    const uint64_t nscalar = a.n - 4 * a.nvec;
+    if (tid < nscalar) {
+        const uint64_t e = tid < a.head ? tid : a.head + 4 * a.nvec + (tid - a.head);
+        float p = a.p_in[e], m = a.m_in[e], v = a.v_in[e];
+        adamw1(a.k, a.g[e], p, m, v);
+        a.p_out[e] = p;
+        a.m_out[e] = m;
+        a.v_out[e] = v;
+    }
+    for (uint64_t q = tid; q < a.nvec; q += nthr) {
+        const uint64_t e = a.head + 4 * q;
+        const float4 gg = __ldcs(reinterpret_cast<const float4*>(a.g + e));
+        float4 pp = __ldcs(reinterpret_cast<const float4*>(a.p_in + e));
+        float4 mm = __ldcs(reinterpret_cast<const float4*>(a.m_in + e));
+        float4 vv = __ldcs(reinterpret_cast<const float4*>(a.v_in + e));
+        adamw1(a.k, gg.x, pp.x, mm.x, vv.x);
+        adamw1(a.k, gg.y, pp.y, mm.y, vv.y);
+        adamw1(a.k, gg.z, pp.z, mm.z, vv.z);
+        adamw1(a.k, gg.w, pp.w, mm.w, vv.w);
+        __stcs(reinterpret_cast<float4*>(a.p_out + e), pp);
+        __stcs(reinterpret_cast<float4*>(a.m_out + e), mm);
+        __stcs(reinterpret_cast<float4*>(a.v_out + e), vv);
+    }
+}
+
+struct CastArgs {
+    const float* master;
+    uint16_t* gath;        // gathered element of master[0]
+    uint64_t n;
+    uint64_t head;         // scalar elements until master is 16-byte aligned
+    uint64_t nvec;         // 8-element vectors
+};
+
+// K3: round-to-nearest-even cast of master weights into the gathered slot.
+template <int DT, int W>
+__global__ void __launch_bounds__(kThreads, kCtasPerSmLight) k_cast(const CastArgs a)
+{
+    const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
+    const uint64_t nthr = (uint64_t)gridDim.x * kThreads;
+    const uint64_t nscalar = a.n - 8 * a.nvec;
+    if (tid < nscalar) {
+        const uint64_t e = tid < a.head ? tid : a.head + 8 * a.nvec + (tid - a.head);
+        a.gath[e] = narrow1<DT>(a.master[e]);
+    }
+    for (uint64_t q = tid; q < a.nvec; q += nthr) {
+        const uint64_t e = a.head + 8 * q;
+        const float4 x0 = __ldcs(reinterpret_cast<const float4*>(a.master + e));
+        const float4 x1 = __ldcs(reinterpret_cast<const float4*>(a.master + e) + 1);
+        const uint32_t w[4] = {
+            (uint32_t)narrow1<DT>(x0.x) | ((uint32_t)narrow1<DT>(x0.y) << 16),
+            (uint32_t)narrow1<DT>(x0.z) | ((uint32_t)narrow1<DT>(x0.w) << 16),
+            (uint32_t)narrow1<DT>(x1.x) | ((uint32_t)narrow1<DT>(x1.y) << 16),
+            (uint32_t)narrow1<DT>(x1.z) | ((uint32_t)narrow1<DT>(x1.w) << 16)};
+        store8<W>(a.gath + e, w);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host-side helpers
+// ---------------------------------------------------------------------------
+
+bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+// Widest store (16/8/4/2 bytes) that a 16-bit element address allows.
+int store_width(const void* p)
+{
+    const uintptr_t x = (uintptr_t)p;
+    if ((x & 15) == 0) return 16;
+    if ((x & 7) == 0) return 8;
+    if ((x & 3) == 0) return 4;
+    return 2;
+}
+
+unsigned grid_for(uint64_t work_items, int ctas_per_sm = kCtasPerSm)
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+        sms = 1;
+    const uint64_t want = (work_items + kThreads - 1) / kThreads;
+    const uint64_t cap = (uint64_t)sms * ctas_per_sm;
+    const uint64_t g = want < cap ? want : cap;
+    return (unsigned)(g == 0 ? 1 : g);
+}
+
+zero_status_t launch_status()
+{
+    return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ERR_CUDA;
+}
+
+// Window split for 2-byte gradient rows whose element 0 has phase `phase`
+// (elements past a 16-byte boundary).
+Split split_window(uint64_t phase, uint64_t len)
+{
+    Split s;
+    s.len = len;
+    uint64_t head = (8 - (phase & 7)) & 7;
+    s.head = head < len ? head : len;
+    s.nvec = (len - s.head) / 8;
+    return s;
+}
+
+bool mul_overflows(uint64_t a, uint64_t b) { return a != 0 && b > UINT64_MAX / a; }
+
+// Validates a gradient descriptor for elements [begin, begin + n) of the shard.
+zero_status_t check_grads(const zero_grads_t* g, uint64_t begin, uint64_t n)
+{
+    if (!g || !g->base || g->nd == 0 || (g->dtype != ZERO_F16 && g->dtype != ZERO_BF16))
+        return ZERO_ERR_INVALID_ARG;
+    if (!aligned(g->base, 16) || (g->row_stride & 7) != 0 || (g->offset & 7) != 0)
+        return ZERO_ERR_ALIGNMENT;
+    // the last element read, (nd-1)*row_stride + offset + begin + n, must fit
+    if (mul_overflows(g->nd - 1, g->row_stride))
+        return ZERO_ERR_INVALID_ARG;
+    const uint64_t last_row = (uint64_t)(g->nd - 1) * g->row_stride;
+    if (g->offset > UINT64_MAX - last_row || begin > UINT64_MAX - last_row - g->offset ||
+        n > UINT64_MAX - last_row - g->offset - begin)
+        return ZERO_ERR_INVALID_ARG;
+    const uint64_t end = last_row + g->offset + begin + n;
+    if (end > (UINT64_MAX >> 1))
+        return ZERO_ERR_INVALID_ARG;
+    return ZERO_OK;
+}
+
+bool ranges_overlap(const void* a, const void* b, uint64_t bytes)
+{
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + bytes && y < x + bytes;
+}
+
+// in/out state checks: non-null, 16-byte aligned; each output equal to its
+// input or disjoint from every input; outputs pairwise disjoint.
+zero_status_t check_state(const zero_state_t* in, const zero_state_t* out, uint64_t n,
+                          uintptr_t align)
+{
+    if (!in || !out || !in->master || !in->m || !in->v || !out->master || !out->m || !out->v)
+        return ZERO_ERR_INVALID_ARG;
+    const float* ins[3] = {in->master, in->m, in->v};
+    const float* outs[3] = {out->master, out->m, out->v};
+    for (int i = 0; i < 3; ++i)
+        if (!aligned(ins[i], align) || !aligned(outs[i], align))
+            return ZERO_ERR_ALIGNMENT;
+    if (mul_overflows(n, 4))
+        return ZERO_ERR_INVALID_ARG;
+    const uint64_t bytes = n * 4;
+    for (int i = 0; i < 3; ++i) {
+        for (int j = 0; j < 3; ++j) {
+            if (i == j && outs[i] == ins[j])
+                continue;
+            if (ranges_overlap(outs[i], ins[j], bytes))
+                return ZERO_ERR_INVALID_ARG;
+        }
+        for (int j = i + 1; j < 3; ++j)
+            if (ranges_overlap(outs[i], outs[j], bytes))
+                return ZERO_ERR_INVALID_ARG;
+    }
+    return ZERO_OK;
+}
+
+template <int DT>
+void launch_fused_dt(const FusedArgs& a, int width, cudaStream_t s)
+{
+    const unsigned grid = grid_for(a.sp.nvec > a.sp.nscalar() ? a.sp.nvec : a.sp.nscalar());
+    switch (width) {
+    case 16: k_step_fused<DT, 16><<<grid, kThreads, 0, s>>>(a); break;
+    case 8: k_step_fused<DT, 8><<<grid, kThreads, 0, s>>>(a); break;
+    case 4: k_step_fused<DT, 4><<<grid, kThreads, 0, s>>>(a); break;
+    default: k_step_fused<DT, 2><<<grid, kThreads, 0, s>>>(a); break;
+    }
+}
+
+void launch_reduce(const ReduceArgs& a, int dtype, cudaStream_t s)
+{
+    const unsigned grid = grid_for(a.sp.nvec > a.sp.nscalar() ? a.sp.nvec : a.sp.nscalar());
+    const bool vec = a.cb == nullptr || aligned(a.cb + a.sp.head, 16);
+    if (dtype == ZERO_F16) {
+        if (vec) k_reduce<ZERO_F16, true><<<grid, kThreads, 0, s>>>(a);
+        else k_reduce<ZERO_F16, false><<<grid, kThreads, 0, s>>>(a);
+    } else {
+        if (vec) k_reduce<ZERO_BF16, true><<<grid, kThreads, 0, s>>>(a);
+        else k_reduce<ZERO_BF16, false><<<grid, kThreads, 0, s>>>(a);
+    }
+}
+
+void launch_adam(const float* grad, const zero_state_t* in, const zero_state_t* out, uint64_t n,
+                 const StepScalars& k, cudaStream_t s)
+{
+    AdamArgs a{grad, in->master, in->m, in->v, out->master, out->m, out->v, n, 0, 0, k};
+    const uintptr_t ph = (uintptr_t)grad & 15;
+    const void* ptrs[6] = {in->master, in->m, in->v, out->master, out->m, out->v};
+    bool vec = (ph & 3) == 0;
+    for (const void* p : ptrs)
+        vec = vec && (((uintptr_t)p & 15) == ph);
+    if (vec) {
+        const uint64_t head = ((16 - ph) & 15) / 4;
+        a.head = head < n ? head : n;
+        a.nvec = (n - a.head) / 4;
+        const uint64_t ns = n - 4 * a.nvec;
+        k_adam<true><<<grid_for(a.nvec > ns ? a.nvec : ns, kCtasPerSmLight), kThreads, 0, s>>>(a);
+    } else {
+        k_adam<false><<<grid_for(n, kCtasPerSmLight), kThreads, 0, s>>>(a);
+    }
+}
+
+void launch_cast(const float* master, uint64_t n, uint16_t* gath, int dtype, cudaStream_t s)
+{
+    CastArgs a{master, gath, n, 0, 0};
+    const uint64_t head = (((16 - ((uintptr_t)master & 15)) & 15) / 4);
+    a.head = head < n ? head : n;
+    a.nvec = (n - a.head) / 8;
+    const uint64_t ns = n - 8 * a.nvec;
+    const unsigned grid = grid_for(a.nvec > ns ? a.nvec : ns, kCtasPerSmLight);
+    const int w = store_width(gath + a.head);
+#define ZERO_CAST_CASE(DT)                                                   \
+    switch (w) {                                                             \
+    case 16: k_cast<DT, 16><<<grid, kThreads, 0, s>>>(a); break;             \
+    case 8: k_cast<DT, 8><<<grid, kThreads, 0, s>>>(a); break;               \
+    case 4: k_cast<DT, 4><<<grid, kThreads, 0, s>>>(a); break;               \
+    default: k_cast<DT, 2><<<grid, kThreads, 0, s>>>(a); break;              \
+    }
+    if (dtype == ZERO_F16) {
+        ZERO_CAST_CASE(ZERO_F16)
+    } else {
+        ZERO_CAST_CASE(ZERO_BF16)
+    }
+#undef ZERO_CAST_CASE
+}
+
+bool loss_scale_valid(double ls) { return ls > 0.0 && ls <= 1.0e300; }
+
+zero_status_t check_step_common(const zero_grads_t* g, const zero_layout_t* L,
+                                const zero_state_t* in, const zero_state_t* out,
+                                const void* gathered, uint64_t bucket_elems, double loss_scale,
+                                const zero_adamw_t* h, const uint32_t* flag)
+{
+    if (!L || !gathered || !flag || bucket_elems == 0 || !loss_scale_valid(loss_scale) ||
+        !adamw_valid(h))
+        return ZERO_ERR_INVALID_ARG;
+    if (L->nd == 0 || L->length > L->shard_elems)
+        return ZERO_ERR_INVALID_ARG;
+    zero_status_t st = check_grads(g, 0, L->length);
+    if (st != ZERO_OK)
+        return st;
+    if (g->nd != L->nd)
+        return ZERO_ERR_INVALID_ARG;
+    if (!aligned(gathered, 2) || !aligned(flag, 4))
+        return ZERO_ERR_ALIGNMENT;
+    return check_state(in, out, L->length, 16);
+}
+
+}  // namespace
+}  // namespace zero
+
+using namespace zero;
+
+// ---------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------
+
+extern "C" zero_status_t zero_reduce_scatter_bucket(const zero_grads_t* g, uint64_t bucket_begin,
+                                                    uint64_t bucket_len, float inv_scale,
+                                                    float* cb_out, uint32_t* d_nonfinite,
+                                                    void* stream)
+{
+    zero_status_t st = check_grads(g, bucket_begin, bucket_len);
+    if (st != ZERO_OK)
+        return st;
+    if (!cb_out || !d_nonfinite)
+        return ZERO_ERR_INVALID_ARG;
+    if (!aligned(cb_out, 4) || !aligned(d_nonfinite, 4))
+        return ZERO_ERR_ALIGNMENT;
+    if (bucket_len == 0)
+        return ZERO_OK;
+    const uint16_t* first = static_cast<const uint16_t*>(g->base) + g->offset + bucket_begin;
+    ReduceArgs a{first, g->row_stride, g->nd, split_window(g->offset + bucket_begin, bucket_len),
+                 inv_scale, cb_out, d_nonfinite};
+    launch_reduce(a, g->dtype, static_cast<cudaStream_t>(stream));
+    return launch_status();
+}
+
+extern "C" zero_status_t zero_check_nonfinite(const zero_grads_t* g, uint64_t begin, uint64_t n,
+                                              uint32_t* d_nonfinite, void* stream)
+{
+    zero_status_t st = check_grads(g, begin, n);
+    if (st != ZERO_OK)
+        return st;
+    if (!d_nonfinite)
+        return ZERO_ERR_INVALID_ARG;
+    if (!aligned(d_nonfinite, 4))
+        return ZERO_ERR_ALIGNMENT;
+    if (n == 0)
+        return ZERO_OK;
+    const uint16_t* first = static_cast<const uint16_t*>(g->base) + g->offset + begin;
+    ReduceArgs a{first, g->row_stride, g->nd, split_window(g->offset + begin, n), 1.0f, nullptr,
+                 d_nonfinite};
+    launch_reduce(a, g->dtype, static_cast<cudaStream_t>(stream));
+    return launch_status();
+}
+
+extern "C" zero_status_t zero_adam_step_shard(const float* grad, const zero_state_t* in,
+                                              const zero_state_t* out, uint64_t n,
+                                              const zero_adamw_t* h, void* stream)
+{
+    if (!grad || !adamw_valid(h))
+        return ZERO_ERR_INVALID_ARG;
+    if (!aligned(grad, 4))
+        return ZERO_ERR_ALIGNMENT;
+    zero_status_t st = check_state(in, out, n, 4);
+    if (st != ZERO_OK)
+        return st;
+    if (ranges_overlap(grad, out->master, n * 4) || ranges_overlap(grad, out->m, n * 4) ||
+        ranges_overlap(grad, out->v, n * 4))
+        return ZERO_ERR_INVALID_ARG;
+    if (n == 0)
+        return ZERO_OK;
+    launch_adam(grad, in, out, n, make_scalars(h, 1, 1.0), static_cast<cudaStream_t>(stream));
+    return launch_status();
+}
+
+extern "C" zero_status_t zero_gather_params_shard(const float* master, uint64_t n, void* gathered,
+                                                  uint64_t slot_offset_elems, zero_dtype_t dtype,
+                                                  void* stream)
+{
+    if (!master || !gathered || (dtype != ZERO_F16 && dtype != ZERO_BF16))
+        return ZERO_ERR_INVALID_ARG;
+    if (!aligned(master, 4) || !aligned(gathered, 2))
+        return ZERO_ERR_ALIGNMENT;
+    if (mul_overflows(n, 4) || slot_offset_elems > (UINT64_MAX >> 2))
+        return ZERO_ERR_INVALID_ARG;
+    if (n == 0)
+        return ZERO_OK;
+    uint16_t* slot = static_cast<uint16_t*>(gathered) + slot_offset_elems;
+    if (ranges_overlap(slot, master, n * 4))   // conservative: the larger extent
+        return ZERO_ERR_INVALID_ARG;
+    launch_cast(master, n, slot, dtype, static_cast<cudaStream_t>(stream));
+    return launch_status();
+}
+
+extern "C" zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layout_t* L,
+                                         const zero_state_t* in, const zero_state_t* out,
+                                         void* gathered, uint64_t gathered_offset_elems,
+                                         uint64_t bucket_elems, double loss_scale,
+                                         const zero_adamw_t* h, uint32_t* d_nonfinite,
+                                         void* stream)
+{
+    zero_status_t st = check_step_common(g, L, in, out, gathered, bucket_elems, loss_scale, h,
+                                         d_nonfinite);
+    if (st != ZERO_OK)
+        return st;
+    const uint64_t n = L->length;
+    if (n == 0)
+        return ZERO_OK;
+    const StepScalars k = make_scalars(h, g->nd, loss_scale);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint16_t* rows = static_cast<const uint16_t*>(g->base) + g->offset;
+    uint16_t* gath = static_cast<uint16_t*>(gathered) + gathered_offset_elems;
+    for (uint64_t b0 = 0; b0 < n; b0 += bucket_elems) {
+        const uint64_t len = n - b0 < bucket_elems ? n - b0 : bucket_elems;
+        FusedArgs a{rows + b0, g->row_stride, g->nd, split_window(g->offset + b0, len),
+                    in->master + b0, in->m + b0, in->v + b0, out->master + b0, out->m + b0,
+                    out->v + b0, gath + b0, k, d_nonfinite};
+        const int width = store_width(gath + b0 + a.sp.head);
+        if (g->dtype == ZERO_F16)
+            launch_fused_dt<ZERO_F16>(a, width, s);
+        else
+            launch_fused_dt<ZERO_BF16>(a, width, s);
+        st = launch_status();
+        if (st != ZERO_OK)
+            return st;
+        if (len < bucket_elems)
+            break;
+    }
+    return ZERO_OK;
+}
+
+extern "C" zero_status_t zero_step_shard_unfused(const zero_grads_t* g, const zero_layout_t* L,
+                                                 const zero_state_t* in, const zero_state_t* out,
+                                                 void* gathered, uint64_t gathered_offset_elems,
+                                                 uint64_t bucket_elems, double loss_scale,
+                                                 const zero_adamw_t* h, float* cb,
+                                                 uint64_t cb_elems, uint32_t* d_nonfinite,
+                                                 void* stream)
+{
+    zero_status_t st = check_step_common(g, L, in, out, gathered, bucket_elems, loss_scale, h,
+                                         d_nonfinite);
+    if (st != ZERO_OK)
+        return st;
+    const uint64_t n = L->length;
+    const uint64_t need = (bucket_elems < n ? bucket_elems : n) + 4;
+    if (!cb || cb_elems < need)
+        return ZERO_ERR_INVALID_ARG;
+    if (!aligned(cb, 16))
+        return ZERO_ERR_ALIGNMENT;
+    if (n == 0)
+        return ZERO_OK;
+    const StepScalars k = make_scalars(h, g->nd, loss_scale);
+    const StepScalars k_adam_only = make_scalars(h, 1, 1.0);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint16_t* rows = static_cast<const uint16_t*>(g->base) + g->offset;
+    uint16_t* gath = static_cast<uint16_t*>(gathered) + gathered_offset_elems;
+    for (uint64_t b0 = 0; b0 < n; b0 += bucket_elems) {
+        const uint64_t len = n - b0 < bucket_elems ? n - b0 : bucket_elems;
+        // Shift the bucket inside cb so that cb and the state share a 16-byte
+        // phase and the optimizer pass runs on float4s.
+        float* cbb = cb + (b0 & 3);
+        ReduceArgs r{rows + b0, g->row_stride, g->nd, split_window(g->offset + b0, len), k.inv,
+                     cbb, d_nonfinite};
+        launch_reduce(r, g->dtype, s);
+        const zero_state_t bin{in->master + b0, in->m + b0, in->v + b0};
+        const zero_state_t bout{out->master + b0, out->m + b0, out->v + b0};
+        launch_adam(cbb, &bin, &bout, len, k_adam_only, s);
+        launch_cast(out->master + b0, len, gath + b0, g->dtype, s);
+        st = launch_status();
+        if (st != ZERO_OK)
+            return st;
+        if (len < bucket_elems)
+            break;
+    }
+    return ZERO_OK;
+}

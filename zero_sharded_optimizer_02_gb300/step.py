@@ -1,0 +1,169 @@
+"""Host side of the ZeRO-DP optimizer step: buffers, launch, skip and commit.
+
+``DataParallelStep`` holds the fp32 optimizer state of one or more ranks of a
+data-parallel group ("ZeRO: Memory Optimizations Toward Training Trillion
+Parameter Models", section "ZeRO-DP": each rank holds and updates only its
+1/Nd of the state) in device memory, launches the library's step for each of
+them and applies the global decision: if any rank's reduced gradient holds an
+inf or NaN, every rank keeps its previous state, gathered parameters and step
+count; otherwise every rank commits.  The state is double-buffered (``cur`` is
+read, ``next`` is written), so a skip costs no extra pass over the gradients
+and committing is a buffer swap.
+
+torch is used for device memory, streams and (optionally) the one-word OR of
+the skip flag over a process group; all optimizer arithmetic runs in the CUDA
+kernels behind the C ABI.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _abi
+
+_TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+class RankState:
+    """Double-buffered fp32 state (master, m, v) of one rank's shard."""
+
+    def __init__(self, layout: _abi.Layout, device):
+        self.layout = layout
+        # One [3, pitch] block per buffer; pitch is a multiple of 8 elements,
+        # so every row starts 32-byte aligned.
+        pitch = max(int(layout.row_pitch), 8)
+        self.bufs = [torch.zeros(3, pitch, dtype=torch.float32, device=device) for _ in range(2)]
+        self.states = [_abi.state(b[0], b[1], b[2]) for b in self.bufs]
+        self.cur = 0
+
+    def tensors(self, which: str = "cur"):
+        i = self.cur if which == "cur" else 1 - self.cur
+        n = int(self.layout.length)
+        b = self.bufs[i]
+        return b[0, :n], b[1, :n], b[2, :n]
+
+    def load(self, master, m, v) -> None:
+        for row, src in zip(self.bufs[self.cur], (master, m, v)):
+            row[:src.numel()].copy_(src)
+
+
+class DataParallelStep:
+    """The ZeRO-DP shard step for a set of ranks sharing one skip decision.
+
+    psi, nd      flat parameter count and data-parallel degree
+    ranks        the ranks held here (all of range(nd) for full emulation)
+    gathered     "full": one flat fp16/bf16 buffer of nd * S parameters that
+                 every rank writes its slot of; "slot": one S-element buffer
+                 per rank (the persistent parameters of a ZeRO-3 rank)
+    fused        zero_step_shard (default) or zero_step_shard_unfused
+    process_group  if given, the skip flag is OR-ed over it every step
+    """
+
+    def __init__(self, psi: int, nd: int, ranks, grad_dtype: str, hparams: dict,
+                 loss_scale: float, bucket: int, device="cuda", gathered: str = "full",
+                 fused: bool = True, process_group=None, row_align: int = 8, stream=None):
+        self.psi, self.nd, self.ranks = psi, nd, list(ranks)
+        self.grad_dtype = grad_dtype
+        self.hp = dict(hparams)
+        self.loss_scale = float(loss_scale)
+        self.bucket = int(bucket)
+        self.device = torch.device(device)
+        self.fused = fused
+        self.pg = process_group
+        self.layouts = {r: _abi.zero_partition_layout(psi, nd, r, row_align) for r in self.ranks}
+        self.state = {r: RankState(self.layouts[r], self.device) for r in self.ranks}
+        s = int(self.layouts[self.ranks[0]].shard_elems)
+        tdt = _TORCH_DTYPES[grad_dtype]
+        self.gathered_mode = gathered
+        if gathered == "full":
+            n = nd * s + 8
+            self.gathered = [torch.zeros(n, dtype=tdt, device=self.device) for _ in range(2)]
+        elif gathered == "slot":
+            self.gathered = [{r: torch.zeros(max(s, 1) + 8, dtype=tdt, device=self.device)
+                              for r in self.ranks} for _ in range(2)]
+        else:
+            raise ValueError(gathered)
+        self.gcur = 0
+        self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
+        self.flag = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.flag_host = torch.zeros(1, dtype=torch.int32, pin_memory=self.device.type == "cuda")
+        self.t = 0
+        self.skipped_steps = []
+        self.cb = None
+        self.cb_elems = 0
+        if not fused:
+            self.cb_elems = min(self.bucket, s) + 4
+            self.cb = torch.empty(self.cb_elems, dtype=torch.float32, device=self.device)
+        self.h = _abi.adamw(self.hp["lr"], self.hp["beta1"], self.hp["beta2"], self.hp["eps"],
+                            self.hp["weight_decay"], 1)
+
+    # -- buffers -------------------------------------------------------------
+
+    def gathered_view(self, rank=None, which: str = "cur") -> torch.Tensor:
+        i = self.gcur if which == "cur" else 1 - self.gcur
+        if self.gathered_mode == "full":
+            return self.gathered[i]
+        return self.gathered[i][rank]
+
+    def _gathered_target(self, r, i):
+        if self.gathered_mode == "full":
+            return self.gathered[i], int(self.layouts[r].begin)
+        return self.gathered[i][r], 0
+
+    # -- the step ------------------------------------------------------------
+
+    def launch(self, grads: dict) -> int:
+        """Launch the step of every held rank (cur -> next) on ``self.stream``.
+        ``grads[r]`` is the _abi.Grads descriptor of rank r's contributions.
+        Returns the number of kernel launches issued."""
+        self.h.step = self.t + 1
+        nxt = 1 - self.gcur
+        launches = 0
+        for r in self.ranks:
+            st = self.state[r]
+            L = self.layouts[r]
+            gbuf, goff = self._gathered_target(r, nxt)
+            s_in, s_out = st.states[st.cur], st.states[1 - st.cur]
+            if self.fused:
+                _abi.zero_step_shard(grads[r], L, s_in, s_out, gbuf, goff, self.bucket,
+                                     self.loss_scale, self.h, self.flag, self.stream)
+            else:
+                _abi.zero_step_shard_unfused(grads[r], L, s_in, s_out, gbuf, goff, self.bucket,
+                                             self.loss_scale, self.h, self.cb, self.cb_elems,
+                                             self.flag, self.stream)
+            n = int(L.length)
+            nb = -(-n // self.bucket) if n else 0
+            launches += nb * (1 if self.fused else 3)
+        return launches
+
+    def decide(self) -> bool:
+        """Read the nonfinite flag (OR-ed over the process group if any)."""
+        with torch.cuda.stream(self.stream):
+            self.flag_host.copy_(self.flag, non_blocking=True)
+        self.stream.synchronize()
+        bad = int(self.flag_host[0]) != 0
+        if self.pg is not None:
+            import torch.distributed as dist
+            word = torch.tensor([int(bad)], dtype=torch.int32)
+            if dist.get_backend(self.pg) == "nccl":
+                word = word.to(self.device)
+            dist.all_reduce(word, op=dist.ReduceOp.MAX, group=self.pg)
+            bad = int(word.item()) != 0
+        return bad
+
+    def commit(self, skipped: bool) -> None:
+        self.skipped_steps.append(skipped)
+        if skipped:
+            with torch.cuda.stream(self.stream):
+                self.flag.zero_()   # the flag is sticky; clear it only after a skip
+            return
+        for st in self.state.values():
+            st.cur = 1 - st.cur
+        self.gcur = 1 - self.gcur
+        self.t += 1
+
+    def step(self, grads: dict) -> bool:
+        """One full step: launch, global decision, commit.  Returns True if skipped."""
+        self.launch(grads)
+        skipped = self.decide()
+        self.commit(skipped)
+        return skipped
