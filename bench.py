@@ -48,6 +48,11 @@ def measured_peaks() -> dict:
         return {}
 
 
+def kernel_name() -> str:
+    flags = os.environ.get("ZERO_NVCC_FLAGS", "")
+    return "k_step_fused_ring" if "ZERO_FUSED_IMPL=0" not in flags else "k_step_fused"
+
+
 def kernel_source_hash() -> str:
     with open(KERNEL_SRC, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -142,7 +147,8 @@ def run_gpu(args) -> None:
 
     import synth
     from zero_sharded_optimizer_02_gb300 import build
-    from zero_sharded_optimizer_02_gb300.step import DataParallelStep
+    from zero_sharded_optimizer_02_gb300.step import (DataParallelStep, data_parallel_rank,
+                                                      max_over_ranks)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -158,13 +164,13 @@ def run_gpu(args) -> None:
         build.build()          # every rank loads the library (already built)
 
     w = synth.WORKLOADS[args.config]
-    dp_rank = args.rank + rank             # this process's data-parallel rank
-    assert dp_rank < w.nd, "more processes than data-parallel ranks"
+    dp_rank = data_parallel_rank(args.rank, rank, w.nd)
+    group = dist.group.WORLD if world > 1 else None
     stream = torch.cuda.Stream(dev)
     with torch.cuda.stream(stream):
         dps = DataParallelStep(w.psi, w.nd, [dp_rank], w.grad_dtype, w.hparams, w.loss_scale,
                                w.bucket, dev, gathered="slot", fused=True,
-                               process_group=dist.group.WORLD if world > 1 else None,
+                               process_group=group,
                                stream=stream)
         L = dps.layouts[dp_rank]
         n = int(L.length)
@@ -208,10 +214,22 @@ def run_gpu(args) -> None:
         dist.barrier()
     total_ms = t_start.elapsed_time(t_end)
     kernel_ms = [a.elapsed_time(b) for a, b in ev]
-    if world > 1:
-        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, group, dev)
+
+    # -- the fused kernel alone: back-to-back launches (no flag read between
+    #    them), timed with events on the launching stream; this removes the
+    #    host launch gap that the per-step events above include -----------------
+    nk = max(1, min(args.steps, 100))
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    k0.record(stream)
+    for _ in range(nk):
+        dps.launch(desc)
+    k1.record(stream)
+    torch.cuda.synchronize(dev)
+    back_to_back_ms = k0.elapsed_time(k1) / nk
+    with torch.cuda.stream(stream):
+        dps.flag.zero_()
     time.sleep(0.2 if sampler else 0.0)
     clocks = None
     if sampler:
@@ -241,10 +259,7 @@ def run_gpu(args) -> None:
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-        if world > 1:
-            tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
+        e2e_ms = max_over_ranks(e2e_ms, group, dev)
         e2e = {"value": world * n / (e2e_ms * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": host_grads.numel() * host_grads.element_size(),
                "d2h_bytes_per_step": n * host_params.element_size() + 4,
@@ -260,7 +275,8 @@ def run_gpu(args) -> None:
     peaks = measured_peaks()
     ms_per_step = total_ms / args.steps
     bytes_per_param = w.bytes_per_param
-    kern_avg_ms = statistics.fmean(kernel_ms)
+    kern_step_ms = statistics.fmean(kernel_ms)
+    kern_avg_ms = back_to_back_ms
     achieved = bytes_per_param * n / (kern_avg_ms * 1e-3) / 1e9
     peak = peaks.get("hbm_gbs")
     peak_src = "measured" if peak else "fallback"
@@ -290,10 +306,12 @@ def run_gpu(args) -> None:
                      "frac": achieved / peak, "peak_source": peak_src,
                      "frac_of_nominal_7900": achieved / NOMINAL_HBM_GBS,
                      "traffic": None if traffic_pp is None else traffic_pp * n,
-                     "kernel": "k_step_fused", "kernel_ms": kern_avg_ms,
+                     "kernel": kernel_name(), "kernel_ms": kern_avg_ms,
+                     "kernel_ms_in_step": kern_step_ms, "kernel_launches_timed": nk,
                      "algorithmic_bytes_per_launch": bytes_per_param * n},
         "e2e": e2e,
         "gpu_launches": launches,
+        "build_flags": os.environ.get("ZERO_NVCC_FLAGS", ""),
         "skipped_steps": skipped,
         "clocks": clocks,
         "wall_s_timed": wall1 - wall0,

@@ -21,9 +21,22 @@ LIB = os.path.join(HERE, "liboracle.so")
 F16, BF16 = 0, 1
 
 
+def _elf_matches_host(path: str) -> bool:
+    import platform
+    machine = {"x86_64": 62, "aarch64": 183, "arm64": 183}.get(platform.machine(), -1)
+    try:
+        with open(path, "rb") as f:
+            head = f.read(20)
+    except OSError:
+        return False
+    return len(head) == 20 and head[:4] == b"\x7fELF" and \
+        int.from_bytes(head[18:20], "little") == machine
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle (plain C, IEEE fp32 with no FMA contraction)."""
-    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SRC):
+    if (force or not os.path.exists(LIB) or not _elf_matches_host(LIB)
+            or os.path.getmtime(LIB) < os.path.getmtime(SRC)):
         tmp = LIB + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
                                "-fPIC", "-shared", SRC, "-o", tmp, "-lm"])

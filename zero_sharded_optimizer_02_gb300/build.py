@@ -7,6 +7,7 @@ library path at run time.
 from __future__ import annotations
 
 import os
+import platform
 import subprocess
 import sys
 
@@ -15,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "libzero.so")
-BUILD = os.path.join(PKG, "_build")
+BUILD = os.path.join(PKG, "_build", platform.machine())
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 SOURCES = {
@@ -33,15 +34,40 @@ def _nvcc() -> str:
     return "nvcc"
 
 
+_ELF_MACHINE = {"x86_64": 62, "aarch64": 183, "arm64": 183}
+
+
+def elf_matches_host(path: str) -> bool:
+    """True if the ELF file at path was built for this machine's architecture."""
+    try:
+        with open(path, "rb") as f:
+            head = f.read(20)
+    except OSError:
+        return False
+    if len(head) < 20 or head[:4] != b"\x7fELF":
+        return False
+    return int.from_bytes(head[18:20], "little") == _ELF_MACHINE.get(platform.machine(), -1)
+
+
 def _stale(target: str, deps: list[str]) -> bool:
-    if not os.path.exists(target):
+    if not os.path.exists(target) or not elf_matches_host(target):
         return True
     t = os.path.getmtime(target)
     return any(os.path.getmtime(d) > t for d in deps)
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile what is stale and link libzero.so.  Extra nvcc flags (e.g. -D
+    tuning macros of zero_kernels.cu) may be given in ZERO_NVCC_FLAGS; a
+    change of flags forces a rebuild."""
     os.makedirs(BUILD, exist_ok=True)
+    extra = os.environ.get("ZERO_NVCC_FLAGS", "").split()
+    stamp = os.path.join(BUILD, "nvcc_flags.txt")
+    old = open(stamp).read() if os.path.exists(stamp) else None
+    if old != " ".join(extra):
+        force = True
+        with open(stamp, "w") as f:
+            f.write(" ".join(extra))
     headers = [os.path.join(INCLUDE, "zero.h"), os.path.join(CSRC, "zero_internal.h")]
     objs, procs = [], []
     for src, cmd in SOURCES.items():
@@ -51,7 +77,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         if force or _stale(obj, [path, *headers, __file__]):
             cmd = list(cmd)
             if cmd[0] == "nvcc":
-                cmd[0] = _nvcc()
+                cmd = [_nvcc()] + cmd[1:] + extra
             log = open(obj + ".log", "w")
             procs.append((src, obj, log, subprocess.Popen(cmd + [path, "-o", obj], stdout=log,
                                                           stderr=subprocess.STDOUT)))

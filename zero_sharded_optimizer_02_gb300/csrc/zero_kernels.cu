@@ -41,6 +41,28 @@ constexpr int kRankUnroll = ZERO_RANK_UNROLL;
 // Elementwise kernels (AdamW from fp32, cast): full occupancy.
 constexpr int kCtasPerSmLight = 8;
 
+// Fused step variant: 0 = rows loaded into registers; 1 = rows staged through
+// a per-thread cp.async ring in shared memory (kRingDepth groups of
+// kRingRows rows of 16 bytes a thread), which keeps more bytes in flight per
+// SM than the register file allows.
+#ifndef ZERO_FUSED_IMPL
+#define ZERO_FUSED_IMPL 1
+#endif
+#ifndef ZERO_RING_ROWS
+#define ZERO_RING_ROWS 8
+#endif
+#ifndef ZERO_RING_DEPTH
+#define ZERO_RING_DEPTH 3
+#endif
+#ifndef ZERO_RING_THREADS
+#define ZERO_RING_THREADS 512
+#endif
+constexpr int kRingRows = ZERO_RING_ROWS;
+constexpr int kRingDepth = ZERO_RING_DEPTH;
+constexpr int kRingThreads = ZERO_RING_THREADS;
+constexpr size_t kRingBytes = (size_t)kRingDepth * kRingRows * kRingThreads * 16;
+static_assert(kRingBytes <= 227 * 1024, "ring exceeds shared memory");
+
 // ---------------------------------------------------------------------------
 // Memory access helpers
 // ---------------------------------------------------------------------------
@@ -61,6 +83,26 @@ __device__ __forceinline__ uint16_t ld_grad2(const uint16_t* p)
     uint16_t r;
     asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
     return r;
+}
+
+// 16-byte asynchronous copy global -> shared (L1 bypassed), and its group
+// commit / wait.  wait_group is a hardware wait on this thread's own copies.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem)
+{
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" ::"r"(sa), "l"(gmem)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Two 16-bit elements packed in a word (element 0 in the low half) to fp32;
@@ -232,53 +274,141 @@ struct FusedArgs {
     uint32_t* flag;
 };
 
-// K4: fused reduce + scale + AdamW + cast, one pass over the window.
+// Scalar element e of the window (head or tail): fold, AdamW, cast.
+template <int DT>
+__device__ __forceinline__ bool fused_scalar(const FusedArgs& a, uint64_t e)
+{
+    const float s = fold1<DT>(a.g + e, a.row_stride, a.nd);
+    float p = a.p_in[e], m = a.m_in[e], v = a.v_in[e];
+    adamw1(a.k, __fmul_rn(s, a.k.inv), p, m, v);
+    a.p_out[e] = p;
+    a.m_out[e] = m;
+    a.v_out[e] = v;
+    a.gath[e] = narrow1<DT>(p);
+    return nonfinite(s);
+}
+
+// Epilogue of 8 reduced sums at window element e (16-byte aligned state):
+// scale, AdamW, streaming state stores, cast into the gathered slot.  Runs in
+// two halves of 4 elements to bound live registers.  Returns "any nonfinite".
+template <int DT, int W>
+__device__ __forceinline__ bool fused_epilogue(const FusedArgs& a, uint64_t e, const float (&s)[8])
+{
+    bool bad = false;
+    uint32_t out16[4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const float4 pp = __ldcs(reinterpret_cast<const float4*>(a.p_in + e) + h);
+        const float4 mm = __ldcs(reinterpret_cast<const float4*>(a.m_in + e) + h);
+        const float4 vv = __ldcs(reinterpret_cast<const float4*>(a.v_in + e) + h);
+        float p[4] = {pp.x, pp.y, pp.z, pp.w};
+        float m[4] = {mm.x, mm.y, mm.z, mm.w};
+        float v[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            bad |= nonfinite(s[4 * h + i]);
+            adamw1(a.k, __fmul_rn(s[4 * h + i], a.k.inv), p[i], m[i], v[i]);
+        }
+        __stcs(reinterpret_cast<float4*>(a.p_out + e) + h, make_float4(p[0], p[1], p[2], p[3]));
+        __stcs(reinterpret_cast<float4*>(a.m_out + e) + h, make_float4(m[0], m[1], m[2], m[3]));
+        __stcs(reinterpret_cast<float4*>(a.v_out + e) + h, make_float4(v[0], v[1], v[2], v[3]));
+        out16[2 * h] = (uint32_t)narrow1<DT>(p[0]) | ((uint32_t)narrow1<DT>(p[1]) << 16);
+        out16[2 * h + 1] = (uint32_t)narrow1<DT>(p[2]) | ((uint32_t)narrow1<DT>(p[3]) << 16);
+    }
+    store8<W>(a.gath + e, out16);
+    return bad;
+}
+
+// K4, register variant: fused reduce + scale + AdamW + cast, one pass over
+// the window; each thread loads kRankUnroll rows of 16 bytes back to back.
 template <int DT, int W>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_step_fused(const FusedArgs a)
 {
     bool bad = false;
     const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
     const uint64_t nthr = (uint64_t)gridDim.x * kThreads;
-
-    if (tid < a.sp.nscalar()) {
-        const uint64_t e = a.sp.scalar_elem(tid);
-        const float s = fold1<DT>(a.g + e, a.row_stride, a.nd);
-        bad |= nonfinite(s);
-        float p = a.p_in[e], m = a.m_in[e], v = a.v_in[e];
-        adamw1(a.k, __fmul_rn(s, a.k.inv), p, m, v);
-        a.p_out[e] = p;
-        a.m_out[e] = m;
-        a.v_out[e] = v;
-        a.gath[e] = narrow1<DT>(p);
-    }
-
+    if (tid < a.sp.nscalar())
+        bad |= fused_scalar<DT>(a, a.sp.scalar_elem(tid));
     for (uint64_t q = tid; q < a.sp.nvec; q += nthr) {
         const uint64_t e = a.sp.head + 8 * q;
         float s[8];
         fold8<DT>(a.g + e, a.row_stride, a.nd, s);
-        uint32_t out16[4];
-        // Epilogue in two halves of 4 elements to bound live registers.
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const float4 pp = __ldcs(reinterpret_cast<const float4*>(a.p_in + e) + h);
-            const float4 mm = __ldcs(reinterpret_cast<const float4*>(a.m_in + e) + h);
-            const float4 vv = __ldcs(reinterpret_cast<const float4*>(a.v_in + e) + h);
-            float p[4] = {pp.x, pp.y, pp.z, pp.w};
-            float m[4] = {mm.x, mm.y, mm.z, mm.w};
-            float v[4] = {vv.x, vv.y, vv.z, vv.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                bad |= nonfinite(s[4 * h + i]);
-                adamw1(a.k, __fmul_rn(s[4 * h + i], a.k.inv), p[i], m[i], v[i]);
-            }
-            __stcs(reinterpret_cast<float4*>(a.p_out + e) + h, make_float4(p[0], p[1], p[2], p[3]));
-            __stcs(reinterpret_cast<float4*>(a.m_out + e) + h, make_float4(m[0], m[1], m[2], m[3]));
-            __stcs(reinterpret_cast<float4*>(a.v_out + e) + h, make_float4(v[0], v[1], v[2], v[3]));
-            out16[2 * h] = (uint32_t)narrow1<DT>(p[0]) | ((uint32_t)narrow1<DT>(p[1]) << 16);
-            out16[2 * h + 1] = (uint32_t)narrow1<DT>(p[2]) | ((uint32_t)narrow1<DT>(p[3]) << 16);
-        }
-        store8<W>(a.gath + e, out16);
+        bad |= fused_epilogue<DT, W>(a, e, s);
     }
+    flag_if_any(bad, a.flag);
+}
+
+// K4, ring variant.  Each thread walks its vectors (8 elements) as a stream
+// of row groups (kRingRows rows of 16 bytes); group copies are issued
+// kRingDepth - 1 groups ahead into the thread's private slots of a shared
+// ring, so the next vector's rows are already in flight during a vector's
+// epilogue.  Slots are laid out [depth][row][thread] so a warp's 16-byte
+// reads are contiguous.  Only the issuing thread reads its slots, so
+// cp.async.wait_group needs no block barrier.  Rows are still folded in
+// rank order.
+template <int DT, int W>
+__global__ void __launch_bounds__(kRingThreads, 1) k_step_fused_ring(const FusedArgs a)
+{
+    extern __shared__ uint4 ring[];
+    bool bad = false;
+    const int t = threadIdx.x;
+    const uint64_t tid = (uint64_t)blockIdx.x * kRingThreads + t;
+    const uint64_t nthr = (uint64_t)gridDim.x * kRingThreads;
+    if (tid < a.sp.nscalar())
+        bad |= fused_scalar<DT>(a, a.sp.scalar_elem(tid));
+
+    const uint32_t groups = (a.nd + kRingRows - 1) / kRingRows;   // groups per vector
+    const uint16_t* base = a.g + a.sp.head;
+    // issue cursor (vector qi, group gi) and consume cursor (qc, gc)
+    uint64_t qi = tid;
+    uint32_t gi = 0;
+    int slot_i = 0;
+    auto issue = [&]() {
+        if (qi < a.sp.nvec) {
+            const uint16_t* gp = base + 8 * qi;
+#pragma unroll
+            for (int u = 0; u < kRingRows; ++u) {
+                const uint32_t j = gi * kRingRows + u;
+                if (j < a.nd)
+                    cp_async16(&ring[(slot_i * kRingRows + u) * kRingThreads + t],
+                               gp + (uint64_t)j * a.row_stride);
+            }
+        }
+        cp_async_commit();
+        slot_i = slot_i + 1 == kRingDepth ? 0 : slot_i + 1;
+        if (++gi == groups) {
+            gi = 0;
+            qi += nthr;
+        }
+    };
+#pragma unroll
+    for (int d = 0; d < kRingDepth - 1; ++d)
+        issue();
+    int slot_c = 0;
+    uint32_t gc = 0;
+    float acc[8];
+    for (uint64_t qc = tid; qc < a.sp.nvec;) {
+        issue();
+        cp_async_wait<kRingDepth - 1>();     // the oldest group has landed
+#pragma unroll
+        for (int u = 0; u < kRingRows; ++u) {
+            const uint32_t j = gc * kRingRows + u;
+            if (j < a.nd) {
+                const uint4 w = ring[(slot_c * kRingRows + u) * kRingThreads + t];
+                if (j == 0)
+                    set8<DT>(acc, w);
+                else
+                    add8<DT>(acc, w);
+            }
+        }
+        slot_c = slot_c + 1 == kRingDepth ? 0 : slot_c + 1;
+        if (++gc == groups) {
+            gc = 0;
+            bad |= fused_epilogue<DT, W>(a, a.sp.head + 8 * qc, acc);
+            qc += nthr;
+        }
+    }
+    cp_async_wait<0>();
     flag_if_any(bad, a.flag);
 }
 
@@ -435,13 +565,11 @@ int store_width(const void* p)
     return 2;
 }
 
+int sm_count();
+
 unsigned grid_for(uint64_t work_items, int ctas_per_sm = kCtasPerSm)
 {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        sms <= 0)
-        sms = 1;
+    const int sms = sm_count();
     const uint64_t want = (work_items + kThreads - 1) / kThreads;
     const uint64_t cap = (uint64_t)sms * ctas_per_sm;
     const uint64_t g = want < cap ? want : cap;
@@ -522,15 +650,42 @@ zero_status_t check_state(const zero_state_t* in, const zero_state_t* out, uint6
     return ZERO_OK;
 }
 
+int sm_count()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+        sms = 1;
+    return sms;
+}
+
+template <int DT, int W>
+void launch_fused_w(const FusedArgs& a, cudaStream_t s)
+{
+    const uint64_t work = a.sp.nvec > a.sp.nscalar() ? a.sp.nvec : a.sp.nscalar();
+    if (ZERO_FUSED_IMPL == 1) {
+        // one resident CTA per SM; the ring needs the opt-in shared memory
+        // size (a per-device function attribute, so set on every launch)
+        cudaFuncSetAttribute(k_step_fused_ring<DT, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kRingBytes);
+        const uint64_t want = (work + kRingThreads - 1) / kRingThreads;
+        const uint64_t cap = (uint64_t)sm_count();
+        const unsigned grid = (unsigned)(want < cap ? (want ? want : 1) : cap);
+        k_step_fused_ring<DT, W><<<grid, kRingThreads, kRingBytes, s>>>(a);
+    } else {
+        k_step_fused<DT, W><<<grid_for(work), kThreads, 0, s>>>(a);
+    }
+}
+
 template <int DT>
 void launch_fused_dt(const FusedArgs& a, int width, cudaStream_t s)
 {
-    const unsigned grid = grid_for(a.sp.nvec > a.sp.nscalar() ? a.sp.nvec : a.sp.nscalar());
     switch (width) {
-    case 16: k_step_fused<DT, 16><<<grid, kThreads, 0, s>>>(a); break;
-    case 8: k_step_fused<DT, 8><<<grid, kThreads, 0, s>>>(a); break;
-    case 4: k_step_fused<DT, 4><<<grid, kThreads, 0, s>>>(a); break;
-    default: k_step_fused<DT, 2><<<grid, kThreads, 0, s>>>(a); break;
+    case 16: launch_fused_w<DT, 16>(a, s); break;
+    case 8: launch_fused_w<DT, 8>(a, s); break;
+    case 4: launch_fused_w<DT, 4>(a, s); break;
+    default: launch_fused_w<DT, 2>(a, s); break;
     }
 }
 

@@ -23,6 +23,44 @@ from . import _abi
 _TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16}
 
 
+def _collective_device(group, device):
+    import torch.distributed as dist
+    if dist.get_backend(group) == "nccl":
+        return device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    return torch.device("cpu")
+
+
+def global_skip(local_bad: bool, group=None, device=None) -> bool:
+    """The global skip decision: True if any rank of ``group`` saw a nonfinite
+    reduced gradient (a one-word MAX all-reduce; identity without a group)."""
+    if group is None:
+        return bool(local_bad)
+    import torch.distributed as dist
+    word = torch.tensor([int(bool(local_bad))], dtype=torch.int32,
+                        device=_collective_device(group, device))
+    dist.all_reduce(word, op=dist.ReduceOp.MAX, group=group)
+    return int(word.item()) != 0
+
+
+def max_over_ranks(x: float, group=None, device=None) -> float:
+    """The maximum of a per-rank float over ``group`` (identity without one)."""
+    if group is None:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=_collective_device(group, device))
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
+
+
+def data_parallel_rank(first_rank: int, process_rank: int, nd: int) -> int:
+    """The data-parallel rank a process runs: process k of a launch runs rank
+    first_rank + k of the emulated Nd-way group."""
+    r = first_rank + process_rank
+    if not 0 <= r < nd:
+        raise ValueError(f"process {process_rank} maps to rank {r}, outside 0..{nd - 1}")
+    return r
+
+
 class RankState:
     """Double-buffered fp32 state (master, m, v) of one rank's shard."""
 
@@ -141,14 +179,7 @@ class DataParallelStep:
             self.flag_host.copy_(self.flag, non_blocking=True)
         self.stream.synchronize()
         bad = int(self.flag_host[0]) != 0
-        if self.pg is not None:
-            import torch.distributed as dist
-            word = torch.tensor([int(bad)], dtype=torch.int32)
-            if dist.get_backend(self.pg) == "nccl":
-                word = word.to(self.device)
-            dist.all_reduce(word, op=dist.ReduceOp.MAX, group=self.pg)
-            bad = int(word.item()) != 0
-        return bad
+        return global_skip(bad, self.pg, self.device)
 
     def commit(self, skipped: bool) -> None:
         self.skipped_steps.append(skipped)
