@@ -90,6 +90,12 @@ def _bind(L: C.CDLL) -> C.CDLL:
     L.orc_step_sharded.restype = i32
     L.orc_step_unsharded_f64.argtypes = [u64, u32, i32, vp, u64, dbl, C.POINTER(Hparams),
                                          u64, vp, vp, vp, vp, vp, vp]
+    L.orc_comm_volume_elems.argtypes = [u64, u32]
+    L.orc_comm_volume_elems.restype = u64
+    L.orc_model_state_bytes_mp.argtypes = [u64, u32, u32, u32, u32]
+    L.orc_model_state_bytes_mp.restype = u64
+    L.orc_gather_range.argtypes = [vp, u64, u64, u32, u64, u64, u32, vp]
+    L.orc_gather_range.restype = i32
     L.orc_reduce_scaled.argtypes = [vp, i32, u32, u64, u64, u64, C.c_float, vp]
     L.orc_reduce_scaled.restype = i32
     L.orc_adamw_from_grad.argtypes = [u64, vp, C.POINTER(Hparams), u64, vp, vp, vp, vp, vp, vp]
@@ -165,6 +171,26 @@ def model_state_bytes(psi: int, nd: int, stage: int, k: int = 12) -> int:
 
 def model_state_bytes_formula(psi: float, nd: float, stage: int, k: float = 12.0) -> float:
     return float(lib().orc_model_state_bytes_formula(psi, nd, stage, k))
+
+
+def comm_volume_elems(psi: int, stage: int) -> int:
+    return int(lib().orc_comm_volume_elems(psi, stage))
+
+
+def model_state_bytes_mp(psi: int, nd: int, nm: int, stage: int, k: int = 12) -> int:
+    return int(lib().orc_model_state_bytes_mp(psi, nd, nm, stage, k))
+
+
+def gather_range(shards: np.ndarray, psi: int, nd: int, begin: int, length: int) -> np.ndarray:
+    """Flat range [begin, begin+length) of a partitioned buffer ``shards``
+    ([nd, pitch], uint16 or float32)."""
+    shards = np.ascontiguousarray(shards)
+    assert shards.ndim == 2 and shards.shape[0] == nd
+    out = np.empty(max(length, 1), shards.dtype)
+    if lib().orc_gather_range(_p(shards), shards.shape[1], psi, nd, begin, length,
+                              shards.itemsize, _p(out)) != 0:
+        raise ValueError("invalid gather range")
+    return out[:length]
 
 
 def scalars(h: dict, t: int, nd: int, loss_scale: float) -> Scalars:

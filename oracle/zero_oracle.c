@@ -178,6 +178,55 @@ double orc_model_state_bytes_formula(double psi, double nd, uint32_t stage, doub
     }
 }
 
+/* Per-step communication volume of a data-parallel process, in parameter
+ * elements, as the ZeRO summary states it (section "ZeRO-DP"): plain DP and
+ * Stage 1 2*Psi (an all-reduce), Stage 2 2*Psi (reduce-scatter Psi +
+ * all-gather Psi), Stage 3 3*Psi.  UINT64_MAX on an invalid stage or overflow. */
+uint64_t orc_comm_volume_elems(uint64_t psi, uint32_t stage)
+{
+    if (stage > 3)
+        return UINT64_MAX;
+    uint64_t mult = stage == 3 ? 3 : 2;
+    if (psi > UINT64_MAX / mult)
+        return UINT64_MAX;
+    return mult * psi;
+}
+
+/* Model-state bytes per GPU when ZeRO-DP (degree Nd) runs inside each of Nm
+ * model-parallel slices (section "ZeRO and MP"): the slice holds ceil(Psi/Nm)
+ * parameters and ZeRO partitions those over Nd. */
+uint64_t orc_model_state_bytes_mp(uint64_t psi, uint32_t nd, uint32_t nm, uint32_t stage,
+                                  uint32_t k)
+{
+    if (nm == 0)
+        return UINT64_MAX;
+    uint64_t slice = psi / nm + (psi % nm != 0);
+    return orc_model_state_bytes(slice, nd, stage, k);
+}
+
+/* Gather of the flat range [begin, begin + len) of a partitioned buffer:
+ * out[i] = element (begin + i) of the flat vector, read from the shard that
+ * owns it.  Shard r's elements sit at src[r * pitch + local] (elem_bytes
+ * each); S = ceil(psi / nd).  Used for the ZeRO-3 on-demand gather of a
+ * layer's parameters and for resharding.  Returns -1 on a bad range. */
+int orc_gather_range(const void* src, uint64_t pitch, uint64_t psi, uint32_t nd,
+                     uint64_t begin, uint64_t len, uint32_t elem_bytes, void* out)
+{
+    if (nd == 0 || begin > psi || len > psi - begin || (elem_bytes != 2 && elem_bytes != 4))
+        return -1;
+    uint64_t s = psi / nd + (psi % nd != 0);
+    if (s > pitch)
+        return -1;
+    for (uint64_t i = 0; i < len; ++i) {
+        uint64_t flat = begin + i;
+        uint64_t r = flat / s;
+        uint64_t local = flat % s;
+        const char* from = (const char*)src + (r * pitch + local) * elem_bytes;
+        memcpy((char*)out + i * elem_bytes, from, elem_bytes);
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* The step.                                                                 */
 /* ------------------------------------------------------------------------ */

@@ -321,6 +321,36 @@ def check_primitives_compose(orc):
         assert np.array_equal(gw.view(np.uint32), g[100:150].view(np.uint32))
 
 
+def check_comm_and_mp_accounting(orc):
+    """Communication volumes 2/2/2/3 Psi and the ZeRO+MP example (1T params,
+    16-way MP x 64-way DP fits a 32 GB GPU), both printed on the pages."""
+    for stage, mult in ((0, 2), (1, 2), (2, 2), (3, 3)):
+        assert orc.comm_volume_elems(10 ** 9, stage) == mult * 10 ** 9
+    assert orc.comm_volume_elems(10, 4) == 2 ** 64 - 1
+    per_gpu = orc.model_state_bytes_mp(10 ** 12, 64, 16, 3, 12)
+    assert per_gpu == 16 * 10 ** 12 // 1024 and per_gpu < 32 * 10 ** 9
+    # Nm = 1 is plain ZeRO-DP; the MP slice divides memory once more
+    assert orc.model_state_bytes_mp(7_500_000_000, 64, 1, 2) == \
+        orc.model_state_bytes(7_500_000_000, 64, 2)
+
+
+def check_gather_range(orc):
+    """The flat range of a partitioned buffer equals the same range of the
+    concatenated shards (numpy concatenate), for every range on tiny cases."""
+    rng = np.random.default_rng(29)
+    for psi, nd in ((0, 3), (1, 1), (17, 4), (33, 5), (64, 8)):
+        s = -(-psi // nd)
+        pitch = -(-max(s, 1) // 8) * 8
+        for dt in (np.uint16, np.float32):
+            shards = rng.integers(0, 60000, size=(nd, pitch)).astype(dt)
+            flat = np.concatenate([shards[r, :max(0, min(s, psi - r * s))] for r in range(nd)])
+            for b in range(psi + 1):
+                for ln in range(psi - b + 1):
+                    got = orc.gather_range(shards, psi, nd, b, ln)
+                    assert np.array_equal(got, flat[b:b + ln]), (psi, nd, b, ln)
+
+
 ALL = [check_codec, check_layout, check_accounting, check_fold, check_adamw_vs_torch,
        check_closed_forms, check_shard_invariant, check_bucket_invariance, check_skip,
-       check_f64_shadow, check_primitives_compose]
+       check_f64_shadow, check_primitives_compose, check_comm_and_mp_accounting,
+       check_gather_range]

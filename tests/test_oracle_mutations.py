@@ -45,6 +45,10 @@ MUTANTS = {
     "bucket_drops_scaling": ("cb[i] = s * k.inv;", "cb[i] = s;"),
     "shard_wrong_state_offset": ("adamw_elem(&k, cb[i], p[e], m[e], v[e]",
                                  "adamw_elem(&k, cb[i], p[i], m[i], v[i]"),
+    "stage3_comm_like_stage2": ("uint64_t mult = stage == 3 ? 3 : 2;",
+                                "uint64_t mult = 2;"),
+    "mp_slice_floor": ("uint64_t slice = psi / nm + (psi % nm != 0);", "uint64_t slice = psi;"),
+    "gather_wrong_owner": ("uint64_t r = flat / s;", "uint64_t r = flat / pitch;"),
     "skip_ignored": ("        if (!isfinite(orc_fold(grads, dtype, nd, row_stride, i)))\n"
                      "            return 1;", "        (void)0;"),
 }
