@@ -188,6 +188,41 @@ zero_status_t zero_step_shard_unfused(const zero_grads_t* g, const zero_layout_t
                                       const zero_adamw_t* h, float* cb, uint64_t cb_elems,
                                       uint32_t* d_nonfinite, void* stream);
 
+/* Size of the library's own fusion buffer used by zero_step_shard_unfused_static:
+ * 4,194,304 fp32 values (16 MiB) of device memory in every GPU that loads the
+ * library, held until the process exits.  A call needs
+ * min(bucket_elems, L->length) + 4 of them, so buckets of up to
+ * ZERO_STATIC_CB_MAX_BUCKET elements fit. */
+#define ZERO_STATIC_CB_ELEMS 4194304ull
+#define ZERO_STATIC_CB_MAX_BUCKET (ZERO_STATIC_CB_ELEMS - 4ull)
+
+/* Allocation-free form of zero_step_shard_unfused (the paper has no
+ * counterpart: this exists for callers that cannot call cudaMalloc, such as
+ * a host framework whose memory pool owns the whole device and forbids
+ * outside allocations, or code that must not take the device-wide
+ * synchronisation that cudaMalloc/cudaFree can imply).  Same arguments and
+ * results as zero_step_shard_unfused minus the workspace: the fusion buffer
+ * is the library's own file-scope device array of ZERO_STATIC_CB_ELEMS
+ * floats.  The caller still provides every input and output.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device looks up that device's address of the array
+ *     (cudaGetSymbolAddress, with the device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - ZERO_ERR_INVALID_ARG, with nothing launched, if
+ *     min(bucket_elems, L->length) > ZERO_STATIC_CB_MAX_BUCKET; the other
+ *     validation is that of zero_step_shard_unfused.
+ *   - Every call on a device shares the one array and it keeps the last
+ *     call's contents (nothing in it needs to start at zero: each bucket is
+ *     written before it is read).  Calls whose kernels overlap on the GPU --
+ *     on different streams or from different threads without ordering --
+ *     race on the array and give wrong results; order them on one stream. */
+zero_status_t zero_step_shard_unfused_static(const zero_grads_t* g, const zero_layout_t* L,
+                                             const zero_state_t* in, const zero_state_t* out,
+                                             void* gathered, uint64_t gathered_offset_elems,
+                                             uint64_t bucket_elems, double loss_scale,
+                                             const zero_adamw_t* h, uint32_t* d_nonfinite,
+                                             void* stream);
+
 /* Pre-pass for in-place stepping: *d_nonfinite |= 1 if any reduced sum
  * s_i (as in zero_reduce_scatter_bucket) over shard elements [begin, begin+n)
  * is nonfinite.  Reads only the gradients (2 * nd bytes per element). */

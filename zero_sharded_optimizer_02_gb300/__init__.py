@@ -10,4 +10,5 @@ from ._abi import (  # noqa: F401
     ZERO_ERR_UNSUPPORTED, ZERO_F16, ZERO_OK, AdamW, Grads, Layout, State, ZeroError, adamw,
     exported_names, grads, lib, state, zero_adam_step_shard, zero_check_nonfinite,
     zero_gather_params_shard, zero_model_state_bytes, zero_partition_layout,
-    zero_reduce_scatter_bucket, zero_status_string, zero_step_shard, zero_step_shard_unfused)
+    zero_reduce_scatter_bucket, zero_status_string, zero_step_shard, zero_step_shard_unfused,
+    zero_step_shard_unfused_static, ZERO_STATIC_CB_ELEMS, ZERO_STATIC_CB_MAX_BUCKET)

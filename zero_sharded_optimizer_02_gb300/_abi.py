@@ -64,7 +64,14 @@ _SIGNATURES = {
                                  C.POINTER(State), vp, u64, u64, dbl, C.POINTER(AdamW), vp, u64,
                                  vp, vp], i32),
     "zero_check_nonfinite": ([C.POINTER(Grads), u64, u64, vp, vp], i32),
+    "zero_step_shard_unfused_static": ([C.POINTER(Grads), C.POINTER(Layout), C.POINTER(State),
+                                        C.POINTER(State), vp, u64, u64, dbl, C.POINTER(AdamW),
+                                        vp, vp], i32),
 }
+
+# Capacity of the library's own fusion buffer (include/zero.h).
+ZERO_STATIC_CB_ELEMS = 4194304
+ZERO_STATIC_CB_MAX_BUCKET = ZERO_STATIC_CB_ELEMS - 4
 
 
 def lib() -> C.CDLL:
@@ -184,3 +191,25 @@ def zero_step_shard_unfused(g: Grads, L: Layout, s_in: State, s_out: State, gath
 def zero_check_nonfinite(g: Grads, begin: int, n: int, d_nonfinite, stream=None) -> None:
     _check(lib().zero_check_nonfinite(C.byref(g), begin, n, _ptr(d_nonfinite), _stream(stream)),
            "zero_check_nonfinite")
+
+
+def zero_step_shard_unfused_static(g: Grads, L: Layout, s_in: State, s_out: State, gathered,
+                                   gathered_offset_elems: int, bucket_elems: int,
+                                   loss_scale: float, h: AdamW, d_nonfinite,
+                                   stream=None) -> None:
+    """zero_step_shard_unfused without a workspace argument: for callers that
+    cannot allocate device memory (their framework's pool owns the device, or
+    they must avoid the synchronisation cudaMalloc/cudaFree can cause).  The
+    fusion buffer is the library's own 16 MiB device array, shared by every
+    call on a device, so calls must not overlap on the GPU; buckets are limited
+    to ZERO_STATIC_CB_MAX_BUCKET elements."""
+    used = min(bucket_elems, int(L.length))
+    if used > ZERO_STATIC_CB_MAX_BUCKET:
+        raise ZeroError(ZERO_ERR_INVALID_ARG,
+                        f"zero_step_shard_unfused_static: bucket of {used} elements exceeds the "
+                        f"static fusion buffer ({ZERO_STATIC_CB_MAX_BUCKET} elements)")
+    _check(lib().zero_step_shard_unfused_static(C.byref(g), C.byref(L), C.byref(s_in),
+                                                C.byref(s_out), _ptr(gathered),
+                                                gathered_offset_elems, bucket_elems, loss_scale,
+                                                C.byref(h), _ptr(d_nonfinite), _stream(stream)),
+           "zero_step_shard_unfused_static")

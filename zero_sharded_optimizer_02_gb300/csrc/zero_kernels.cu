@@ -20,6 +20,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "zero.h"
 #include "zero_internal.h"
 
@@ -937,4 +939,70 @@ extern "C" zero_status_t zero_step_shard_unfused(const zero_grads_t* g, const ze
             break;
     }
     return ZERO_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free unfused step: the fusion buffer lives in this library's own
+// device memory instead of a caller-provided workspace.
+// ---------------------------------------------------------------------------
+
+namespace zero {
+namespace {
+
+// The fusion buffer: ZERO_STATIC_CB_ELEMS floats (16 MiB) on every device that
+// loads the library.  In host code this name is only a stand-in for the
+// symbol; kernels get the device address from cudaGetSymbolAddress.
+__device__ __align__(256) float g_static_cb[ZERO_STATIC_CB_ELEMS];
+
+constexpr int kMaxDevices = 128;
+std::atomic<float*> g_static_cb_addr[kMaxDevices];   // per device, null until looked up
+
+// Device address of g_static_cb on the current device, looked up once per
+// device (with that device current) and cached.
+zero_status_t static_cb_address(float** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return ZERO_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices)
+        return ZERO_ERR_UNSUPPORTED;
+    float* p = g_static_cb_addr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        void* a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_static_cb) != cudaSuccess || a == nullptr)
+            return ZERO_ERR_CUDA;
+        p = static_cast<float*>(a);
+        g_static_cb_addr[dev].store(p, std::memory_order_release);
+    }
+    *out = p;
+    return ZERO_OK;
+}
+
+}  // namespace
+}  // namespace zero
+
+extern "C" zero_status_t zero_step_shard_unfused_static(const zero_grads_t* g,
+                                                        const zero_layout_t* L,
+                                                        const zero_state_t* in,
+                                                        const zero_state_t* out, void* gathered,
+                                                        uint64_t gathered_offset_elems,
+                                                        uint64_t bucket_elems, double loss_scale,
+                                                        const zero_adamw_t* h,
+                                                        uint32_t* d_nonfinite, void* stream)
+{
+    if (!L || bucket_elems == 0)
+        return ZERO_ERR_INVALID_ARG;
+    const uint64_t used = bucket_elems < L->length ? bucket_elems : L->length;
+    if (used > ZERO_STATIC_CB_MAX_BUCKET)
+        return ZERO_ERR_INVALID_ARG;   // the bucket does not fit the static fusion buffer
+    zero_status_t st = check_step_common(g, L, in, out, gathered, bucket_elems, loss_scale, h,
+                                         d_nonfinite);
+    if (st != ZERO_OK)
+        return st;
+    float* cb = nullptr;
+    st = static_cb_address(&cb);
+    if (st != ZERO_OK)
+        return st;
+    return zero_step_shard_unfused(g, L, in, out, gathered, gathered_offset_elems, bucket_elems,
+                                   loss_scale, h, cb, ZERO_STATIC_CB_ELEMS, d_nonfinite, stream);
 }
