@@ -35,7 +35,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "ZeRO shard step: params updated/s and HBM GB/s vs GB300 peak (1 GPU)"
 UNIT = "params/s"
-KERNEL_SRC = os.path.join(ROOT, "zero_sharded_optimizer_02_gb300", "csrc", "zero_kernels.cu")
+KERNEL_SRCS = [os.path.join(ROOT, "zero_sharded_optimizer_02_gb300", "csrc", f)
+               for f in ("zero_kernels.cu", "zero_device.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k_step_fused_traffic.txt")
 NOMINAL_HBM_GBS = 7900.0
 
@@ -54,8 +55,12 @@ def kernel_name() -> str:
 
 
 def kernel_source_hash() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of the sources the fused kernel is compiled from."""
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload: str):
@@ -72,7 +77,8 @@ def recorded_traffic(workload: str):
         return None
     if kv.get("kernel_source_sha256_16") != kernel_source_hash():
         return None
-    if kv.get("workload") != workload:
+    if kv.get("workload") != workload or kv.get("build_flags", "") != os.environ.get(
+            "ZERO_NVCC_FLAGS", ""):
         return None
     return float(kv["dram_bytes_per_param"])
 
@@ -236,34 +242,54 @@ def run_gpu(args) -> None:
         sampler.stop()
         clocks = sampler.summary(wall0, wall1)
 
-    # -- end to end through host buffers (pinned H2D of the step's gradients,
-    #    the step, D2H of the new parameters and the flag) ----------------------
+    # -- end to end through host buffers.  Every step: the step's gradients
+    #    enter from pinned host memory, the step runs, the new parameters and
+    #    the flag come back.  The gradients are fed in transfer buckets by
+    #    zero_feed_buckets on a copy stream while the bucket-ready kernel
+    #    (zero_step_shard_streamed) runs the optimizer on the buckets that have
+    #    landed; results do not depend on the bucket size.  The plain
+    #    sequential form (copy everything, then step) is timed beside it. -----
     e2e = None
     if args.e2e_steps > 0:
         host_grads = torch.empty(grads.shape, dtype=grads.dtype, pin_memory=True)
         host_grads.copy_(grads)
         host_params = torch.empty(n, dtype=grads.dtype, pin_memory=True)
-        for it in range(args.e2e_steps + 1):      # first iteration untimed
-            if it == 1:
-                if world > 1:
-                    dist.barrier()
-                torch.cuda.synchronize(dev)
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
+        copy_stream = torch.cuda.Stream(dev)
+        stream_bucket = max(8, -(-(-(-n // args.e2e_buckets)) // 8) * 8)
+
+        def timed(fn):
+            for it in range(args.e2e_steps + 1):      # first iteration untimed
+                if it == 1:
+                    if world > 1:
+                        dist.barrier()
+                    torch.cuda.synchronize(dev)
+                    t0 = time.perf_counter()
+                fn()
+                with torch.cuda.stream(stream):
+                    host_params.copy_(dps.gathered_view(dp_rank)[:n], non_blocking=True)
+                stream.synchronize()
+            return (time.perf_counter() - t0) * 1e3 / args.e2e_steps
+
+        def host_fed():
+            dps.launch_host_fed(dp_rank, host_grads, desc[dp_rank], stream_bucket, copy_stream)
+            dps.commit(dps.decide())
+
+        def sequential():
             with torch.cuda.stream(stream):
                 grads.copy_(host_grads, non_blocking=True)
-            s = dps.step(desc)
-            with torch.cuda.stream(stream):
-                host_params.copy_(dps.gathered_view(dp_rank)[:n], non_blocking=True)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-        e2e_ms = max_over_ranks(e2e_ms, group, dev)
-        e2e = {"value": world * n / (e2e_ms * 1e-3), "unit": UNIT,
+            dps.step(desc)
+
+        fed_ms = max_over_ranks(timed(host_fed), group, dev)
+        assert dps.host_fed_status() == 0, "a bucket never arrived"
+        seq_ms = max_over_ranks(timed(sequential), group, dev)
+        e2e = {"value": world * n / (fed_ms * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": host_grads.numel() * host_grads.element_size(),
                "d2h_bytes_per_step": n * host_params.element_size() + 4,
-               "ms_per_step": e2e_ms, "steps": args.e2e_steps}
+               "ms_per_step": fed_ms, "steps": args.e2e_steps,
+               "path": f"zero_feed_buckets + zero_step_shard_streamed, "
+                       f"{-(-n // stream_bucket)} transfer buckets",
+               "sequential_ms_per_step": seq_ms,
+               "sequential_value": world * n / (seq_ms * 1e-3)}
         del host_grads, host_params
 
     if rank != 0:
@@ -416,6 +442,8 @@ def main():
     ap.add_argument("--config", default="c4", choices=["c1", "c2", "c3", "c4"])
     ap.add_argument("--rank", type=int, default=0, help="first data-parallel rank to run")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-buckets", type=int, default=16,
+                    help="transfer buckets of the host-fed e2e step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-sample", type=int, default=1 << 16,

@@ -50,7 +50,8 @@ typedef enum zero_status {
     ZERO_ERR_ALIGNMENT = 2,    /* a pointer or stride breaks the documented alignment */
     ZERO_ERR_CUDA = 3,         /* the CUDA runtime reported an error */
     ZERO_ERR_TIMEOUT = 4,      /* a bounded wait expired (reserved) */
-    ZERO_ERR_UNSUPPORTED = 5   /* valid request this build does not implement */
+    ZERO_ERR_UNSUPPORTED = 5,  /* valid request this build does not implement */
+    ZERO_ERR_IO = 6            /* a checkpoint file is missing, unreadable, torn or corrupt */
 } zero_status_t;
 
 typedef enum zero_dtype {
@@ -228,6 +229,127 @@ zero_status_t zero_step_shard_unfused_static(const zero_grads_t* g, const zero_l
  * is nonfinite.  Reads only the gradients (2 * nd bytes per element). */
 zero_status_t zero_check_nonfinite(const zero_grads_t* g, uint64_t begin, uint64_t n,
                                    uint32_t* d_nonfinite, void* stream);
+
+/* ---- Bucket-ready stepping ------------------------------------------------- */
+
+/* The fused step started bucket by bucket as gradients arrive ("ZeRO-DP",
+ * Stage 2: gradients are reduce-scattered in buckets during the backward
+ * pass).  One persistent launch walks the shard's buckets in order; before
+ * bucket b (elements [b*bucket_elems, ...) of the shard) each CTA waits until
+ * d_ready[b] >= epoch (wrap-around comparison).  The producer of bucket b
+ * writes d_ready[b] after the bucket's contributions are in place -- e.g. a
+ * cudaMemcpyAsync of the word on the copy stream that copied the data.  The
+ * ready words must be written by a copy engine or the host, never by a kernel
+ * that would have to run concurrently with this one.
+ * Each wait is bounded by timeout_ns of GPU time (%globaltimer) and an
+ * iteration cap; on expiry the kernel stores ZERO_ERR_TIMEOUT into *d_status
+ * (if it is still 0), leaves that bucket and the later ones unwritten, and
+ * returns: the caller reads *d_status after the stream work completes.
+ * timeout_ns must be in [1, ZERO_MAX_WAIT_NS] (ZERO_ERR_INVALID_ARG otherwise).
+ * Other arguments, alignment and results as zero_step_shard (bitwise equal). */
+#define ZERO_MAX_WAIT_NS 60000000000ull
+zero_status_t zero_step_shard_streamed(const zero_grads_t* g, const zero_layout_t* L,
+                                       const zero_state_t* in, const zero_state_t* out,
+                                       void* gathered, uint64_t gathered_offset_elems,
+                                       uint64_t bucket_elems, double loss_scale,
+                                       const zero_adamw_t* h, const uint32_t* d_ready,
+                                       uint32_t epoch, uint64_t timeout_ns,
+                                       uint32_t* d_nonfinite, uint32_t* d_status, void* stream);
+
+/* Producer for zero_step_shard_streamed when the gradients come from host
+ * memory: for each bucket b of the shard (elements [b*bucket_elems, ...) of
+ * the first n), enqueues on copy_stream one 2D copy of the bucket's slice of
+ * all nd contributor rows -- host element i of contributor j at
+ * host[j * host_row_stride + i] to g's device rows -- and then a 4-byte copy
+ * of *h_epoch into d_ready[b], so the ready word lands after the data.
+ * host and h_epoch: pinned host memory that must stay valid and unchanged
+ * until the copies complete; copy_stream must not be ordered behind the
+ * stream running the consumer (use two non-blocking streams).  Only enqueues
+ * copies (no kernel, no allocation).  ZERO_ERR_INVALID_ARG if a row is
+ * shorter than n (host_row_stride < n, g->row_stride < g->offset + n). */
+zero_status_t zero_feed_buckets(const void* host, uint64_t host_row_stride,
+                                const zero_grads_t* g, uint64_t n, uint64_t bucket_elems,
+                                uint32_t* d_ready, const uint32_t* h_epoch, void* copy_stream);
+
+/* ---- ZeRO-3 parameter gather and resharding ------------------------------- */
+
+/* On-demand gather of a flat range ("ZeRO-DP", Stage 3: parameters are
+ * partitioned; a layer's are collected from their owners before use and
+ * released after): out[i] = element begin + i of the flat psi-element vector,
+ * for i in [0, len).  The vector is partitioned as zero_partition_layout
+ * gives (S = ceil(psi / nd)); shard r's elements sit at
+ * shards[r * pitch + local], local < S, pitch >= S.  elem_bytes is 2 (fp16 or
+ * bf16 parameters) or 4 (fp32 state, e.g. to reshard to another nd).
+ * shards and out: device, aligned to elem_bytes; out must not overlap the
+ * shards; only the range's own elements are read.  One launch per shard
+ * segment of the range (at most ceil(len / S) + 1).  ZERO_ERR_INVALID_ARG on a
+ * range outside [0, psi), pitch < S, NULL pointers or overlap. */
+zero_status_t zero_gather_range(const void* shards, uint64_t pitch, uint64_t psi, uint32_t nd,
+                                uint64_t begin, uint64_t len, uint32_t elem_bytes, void* out,
+                                void* stream);
+
+/* ---- Sharded checkpoints ---------------------------------------------------- */
+
+/* Header of one rank's checkpoint file ("ZeRO" (process-cxr ai-library),
+ * checkpointing and recovery: each rank saves only the state it owns; the
+ * metadata must be stored reliably and resuming on another world size must be
+ * possible).  The file is this header followed by the rank's fp32 master
+ * weights, m and v, `length` elements each, in that order. */
+typedef struct zero_ckpt_header {
+    char magic[8];              /* "ZEROCKPT" */
+    uint32_t version;           /* 1 */
+    uint32_t header_bytes;      /* sizeof(zero_ckpt_header_t) */
+    uint64_t psi;               /* flat parameters of the model */
+    uint32_t nd;                /* data-parallel degree when saved */
+    uint32_t rank;              /* the rank that saved this file */
+    uint64_t shard_elems;       /* S = ceil(psi / nd) */
+    uint64_t begin;             /* rank * S */
+    uint64_t length;            /* elements of each array in the payload */
+    uint64_t step;              /* committed optimizer steps t */
+    double lr, beta1, beta2, eps, weight_decay;   /* AdamW hyperparameters */
+    uint64_t payload_checksum;  /* FNV-1a (64-bit) over the payload's 32-bit words */
+} zero_ckpt_header_t;
+
+/* Writes rank L->rank's state (host fp32 arrays of L->length elements) and
+ * h's hyperparameters, with h->step = the committed step count t, to `path`
+ * (written to path.tmp, then renamed, so a crash leaves no torn file).
+ * ZERO_ERR_INVALID_ARG on NULL arguments or a layout that
+ * zero_partition_layout would not produce; ZERO_ERR_IO on a file error. */
+zero_status_t zero_checkpoint_save(const char* path, const zero_layout_t* L,
+                                   const zero_adamw_t* h, const float* master, const float* m,
+                                   const float* v);
+
+/* Reads and validates one file's header (magic, version, partition). */
+zero_status_t zero_checkpoint_read_header(const char* path, zero_ckpt_header_t* out);
+
+/* Loads rank L->rank of an L->nd-way partition from the n_paths files of a
+ * checkpoint saved with n_paths ranks (paths[r] = old rank r's file),
+ * resharding when L->nd != n_paths: the new rank's flat range is filled from
+ * the overlapping ranges of the old files, so the result is bit-identical to
+ * the saved state.  Every file read is checked against its payload checksum.
+ * master, m, v: host arrays of L->length floats.  h_out (may be NULL)
+ * receives the saved hyperparameters and step.  ZERO_ERR_INVALID_ARG if the
+ * files disagree on psi or nd or are not ranks 0..n_paths-1 in order;
+ * ZERO_ERR_IO on a missing, torn or corrupt file or differing steps. */
+zero_status_t zero_checkpoint_load(const char* const* paths, uint32_t n_paths,
+                                   const zero_layout_t* L, float* master, float* m, float* v,
+                                   zero_adamw_t* h_out);
+
+/* ---- Accounting variants ------------------------------------------------- */
+
+/* Per-step communication volume of one data-parallel process, in parameter
+ * elements, as the ZeRO summary gives it (section "ZeRO-DP"): stage 0 (plain
+ * data parallel, an all-reduce) and stage 1 move 2*psi, stage 2 moves 2*psi
+ * (reduce-scatter psi + all-gather psi), stage 3 moves 3*psi (1.5x).  Host
+ * only.  UINT64_MAX if stage > 3 or the result overflows. */
+uint64_t zero_comm_volume_elems(uint64_t psi, uint32_t stage);
+
+/* Per-GPU model-state bytes when ZeRO-DP of degree nd runs inside each of nm
+ * model-parallel slices (section "ZeRO and MP": memory falls by up to
+ * Nd x Nm): zero_model_state_bytes(ceil(psi / nm), nd, stage, k).  Host only.
+ * UINT64_MAX if nm == 0 or as zero_model_state_bytes. */
+uint64_t zero_model_state_bytes_mp(uint64_t psi, uint32_t nd, uint32_t nm, uint32_t stage,
+                                   uint32_t k);
 
 #ifdef __cplusplus
 }

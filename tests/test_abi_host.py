@@ -72,6 +72,28 @@ def test_accounting_matches_oracle_and_table(z, orc):
     assert z.zero_model_state_bytes(1, 1, 4, 12) == 2 ** 64 - 1
 
 
+def test_comm_volume_and_mp_accounting(z, orc):
+    import os
+    gold = os.path.join(ROOT, "tests", "golden")
+    rows = [ln.split() for ln in open(os.path.join(gold, "stage_reductions.txt"))
+            if ln.strip() and not ln.startswith("#")]
+    for stage, _, comm in rows:
+        assert z.zero_comm_volume_elems(10 ** 9, int(stage)) == int(comm) * 10 ** 9
+    assert z.zero_comm_volume_elems(10 ** 9, 0) == 2 * 10 ** 9
+    assert z.zero_comm_volume_elems(1, 4) == 2 ** 64 - 1
+    kv = {r[0]: r[1] for r in (ln.split() for ln in open(os.path.join(
+        gold, "model_state_examples.txt")) if ln.strip() and not ln.startswith("#"))}
+    per_gpu = z.zero_model_state_bytes_mp(int(kv["mp_psi"]), int(kv["mp_nd"]), int(kv["mp_nm"]),
+                                          3, int(kv["k"]))
+    assert per_gpu < int(kv["mp_gpu_gb"]) * 10 ** 9
+    for psi in (1, 999, 10 ** 12, 7_500_000_000):
+        for nd, nm in ((64, 16), (1, 1), (7, 3)):
+            for st in range(4):
+                assert z.zero_model_state_bytes_mp(psi, nd, nm, st, 12) == \
+                    orc.model_state_bytes_mp(psi, nd, nm, st, 12)
+    assert z.zero_model_state_bytes_mp(10, 1, 0, 0, 12) == 2 ** 64 - 1
+
+
 def test_status_strings(z):
     for code in range(6):
         assert z.zero_status_string(code).startswith("ZERO_")

@@ -1,0 +1,94 @@
+"""GPU parity of zero_gather_range (ZeRO-3 on-demand parameter gather and
+fp32 resharding) against the oracle, bit for bit.
+
+"ZeRO: Memory Optimizations Toward Training Trillion Parameter Models",
+section "ZeRO-DP", Stage 3: each rank keeps only its shard of the parameters;
+a layer's parameters are collected from the owners before use.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import zero_sharded_optimizer_02_gb300 as z
+from gpu_util import DEV, full_rows, make_group, oracle_trajectory, u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from zero_sharded_optimizer_02_gb300 import build
+    build.build()
+    oracle.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def _ranges(rng, psi, s, count):
+    out = [(0, psi), (0, 0), (psi, 0), (0, 1), (psi - 1, 1)] if psi else [(0, 0)]
+    for r in range(0, psi, max(s, 1)):
+        out += [(r, min(s, psi - r)), (max(0, r - 3), min(psi - max(0, r - 3), 11))]
+    for _ in range(count):
+        b = int(rng.integers(0, psi + 1))
+        out.append((b, int(rng.integers(0, psi - b + 1))))
+    return out
+
+
+@pytest.mark.parametrize("psi,nd,pad", [(1000, 3, 0), (100_003, 7, 5), (64, 64, 0),
+                                        (2_000_001, 16, 13), (5, 8, 3), (300_000, 1, 0)])
+@pytest.mark.parametrize("dtype", [np.uint16, np.float32])
+def test_gather_range_matches_oracle(psi, nd, pad, dtype):
+    rng = np.random.default_rng(psi + nd)
+    s = -(-psi // nd)
+    pitch = s + pad
+    host = rng.integers(0, 1 << 16, size=(nd, pitch)).astype(dtype)
+    if dtype == np.float32:
+        host = rng.standard_normal((nd, pitch)).astype(np.float32)
+    tdt = torch.int16 if dtype == np.uint16 else torch.float32
+    dev = torch.from_numpy(host.view(np.int16) if dtype == np.uint16 else host).to(DEV)
+    eb = host.itemsize
+    for b, ln in _ranges(rng, psi, s, 12):
+        for shift in (0, 1, 3):             # destination phases
+            out = torch.full((ln + shift + 16,), 7, dtype=tdt, device=DEV)
+            z.zero_gather_range(dev, pitch, psi, nd, b, ln, eb, out[shift:])
+            torch.cuda.synchronize()
+            got = out[shift:shift + ln].cpu().numpy()
+            ref = oracle.gather_range(host, psi, nd, b, ln)
+            assert np.array_equal(got.view(dtype), ref), (b, ln, shift)
+            rest = torch.cat([out[:shift], out[shift + ln:]])
+            assert bool((rest == 7).all()), "write outside the destination range"
+
+
+def test_gather_rejects_bad_ranges():
+    buf = torch.zeros(4, 16, dtype=torch.int16, device=DEV)
+    out = torch.zeros(64, dtype=torch.int16, device=DEV)
+    for args in ((buf, 16, 60, 4, 50, 11, 2, out), (buf, 14, 60, 4, 0, 1, 2, out),
+                 (buf, 16, 60, 0, 0, 1, 2, out), (buf, 16, 60, 4, 0, 1, 3, out),
+                 (buf, 16, 60, 4, 0, 8, 2, buf[1])):
+        with pytest.raises(z.ZeroError) as e:
+            z.zero_gather_range(*args)
+        assert e.value.status == z.ZERO_ERR_INVALID_ARG
+
+
+def test_zero3_layer_gather_after_step():
+    """ZeRO-3 flow: every rank steps its shard into its own parameter row,
+    then each "layer" (a flat range) is gathered from the rows and equals the
+    oracle's unsharded parameters over that range."""
+    w = dataclasses.replace(synth.WORKLOADS["c1"], psi=1_000_003, nd=16, plant=None)
+    dps = make_group(w, gathered="pitched", bucket=50_000)
+    buf, desc = full_rows(w, dps, 0)
+    assert not dps.step(desc)
+    _, hist = oracle_trajectory(w, np.arange(w.psi), 1)
+    params_ref = hist[0][3]
+    rows = dps.gathered_view()
+    pitch = rows.shape[1]
+    bounds = np.sort(np.random.default_rng(3).choice(np.arange(1, w.psi), 6, replace=False))
+    layers = list(zip(np.r_[0, bounds], np.r_[bounds, w.psi]))
+    for a, b in layers:
+        out = torch.empty(int(b - a), dtype=rows.dtype, device=DEV)
+        z.zero_gather_range(rows, pitch, w.psi, w.nd, int(a), int(b - a), 2, out)
+        torch.cuda.synchronize()
+        assert np.array_equal(u16(out), params_ref[a:b]), (a, b)

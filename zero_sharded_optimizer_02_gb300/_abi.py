@@ -16,7 +16,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libzero.so")
 
 ZERO_OK, ZERO_ERR_INVALID_ARG, ZERO_ERR_ALIGNMENT, ZERO_ERR_CUDA = 0, 1, 2, 3
-ZERO_ERR_TIMEOUT, ZERO_ERR_UNSUPPORTED = 4, 5
+ZERO_ERR_TIMEOUT, ZERO_ERR_UNSUPPORTED, ZERO_ERR_IO = 4, 5, 6
 ZERO_F16, ZERO_BF16 = 0, 1
 DTYPES = {"f16": ZERO_F16, "bf16": ZERO_BF16}
 UINT64_MAX = (1 << 64) - 1
@@ -43,6 +43,13 @@ class State(C.Structure):
     _fields_ = [("master", vp), ("m", vp), ("v", vp)]
 
 
+class CkptHeader(C.Structure):
+    _fields_ = [("magic", C.c_char * 8), ("version", u32), ("header_bytes", u32), ("psi", u64),
+                ("nd", u32), ("rank", u32), ("shard_elems", u64), ("begin", u64),
+                ("length", u64), ("step", u64), ("lr", dbl), ("beta1", dbl), ("beta2", dbl),
+                ("eps", dbl), ("weight_decay", dbl), ("payload_checksum", u64)]
+
+
 class AdamW(C.Structure):
     _fields_ = [("lr", dbl), ("beta1", dbl), ("beta2", dbl), ("eps", dbl),
                 ("weight_decay", dbl), ("step", u64)]
@@ -64,6 +71,17 @@ _SIGNATURES = {
                                  C.POINTER(State), vp, u64, u64, dbl, C.POINTER(AdamW), vp, u64,
                                  vp, vp], i32),
     "zero_check_nonfinite": ([C.POINTER(Grads), u64, u64, vp, vp], i32),
+    "zero_step_shard_streamed": ([C.POINTER(Grads), C.POINTER(Layout), C.POINTER(State),
+                                  C.POINTER(State), vp, u64, u64, dbl, C.POINTER(AdamW), vp, u32,
+                                  u64, vp, vp, vp], i32),
+    "zero_feed_buckets": ([vp, u64, C.POINTER(Grads), u64, u64, vp, vp, vp], i32),
+    "zero_gather_range": ([vp, u64, u64, u32, u64, u64, u32, vp, vp], i32),
+    "zero_checkpoint_save": ([C.c_char_p, C.POINTER(Layout), C.POINTER(AdamW), vp, vp, vp], i32),
+    "zero_checkpoint_read_header": ([C.c_char_p, C.POINTER(CkptHeader)], i32),
+    "zero_checkpoint_load": ([C.POINTER(C.c_char_p), u32, C.POINTER(Layout), vp, vp, vp,
+                              C.POINTER(AdamW)], i32),
+    "zero_comm_volume_elems": ([u64, u32], u64),
+    "zero_model_state_bytes_mp": ([u64, u32, u32, u32, u32], u64),
     "zero_step_shard_unfused_static": ([C.POINTER(Grads), C.POINTER(Layout), C.POINTER(State),
                                         C.POINTER(State), vp, u64, u64, dbl, C.POINTER(AdamW),
                                         vp, vp], i32),
@@ -147,6 +165,74 @@ def zero_partition_layout(psi: int, nd: int, rank: int, row_align_elems: int = 8
 
 def zero_model_state_bytes(psi: int, nd: int, stage: int, k: int = 12) -> int:
     return int(lib().zero_model_state_bytes(psi, nd, stage, k))
+
+
+def zero_step_shard_streamed(g: Grads, L: Layout, s_in: State, s_out: State, gathered,
+                             gathered_offset_elems: int, bucket_elems: int, loss_scale: float,
+                             h: AdamW, d_ready, epoch: int, timeout_ns: int, d_nonfinite,
+                             d_status, stream=None) -> None:
+    _check(lib().zero_step_shard_streamed(C.byref(g), C.byref(L), C.byref(s_in), C.byref(s_out),
+                                          _ptr(gathered), gathered_offset_elems, bucket_elems,
+                                          loss_scale, C.byref(h), _ptr(d_ready), epoch,
+                                          timeout_ns, _ptr(d_nonfinite), _ptr(d_status),
+                                          _stream(stream)), "zero_step_shard_streamed")
+
+
+def zero_feed_buckets(host, host_row_stride: int, g: Grads, n: int, bucket_elems: int, d_ready,
+                      h_epoch, copy_stream=None) -> None:
+    _check(lib().zero_feed_buckets(_ptr(host), host_row_stride, C.byref(g), n, bucket_elems,
+                                   _ptr(d_ready), _ptr(h_epoch), _stream(copy_stream)),
+           "zero_feed_buckets")
+
+
+def zero_gather_range(shards, pitch: int, psi: int, nd: int, begin: int, length: int,
+                      elem_bytes: int, out, stream=None) -> None:
+    _check(lib().zero_gather_range(_ptr(shards), pitch, psi, nd, begin, length, elem_bytes,
+                                   _ptr(out), _stream(stream)), "zero_gather_range")
+
+
+def zero_checkpoint_save(path: str, L: Layout, h: AdamW, master, m, v) -> None:
+    """Host arrays (numpy float32, contiguous) of L.length elements."""
+    _check(lib().zero_checkpoint_save(os.fsencode(path), C.byref(L), C.byref(h),
+                                      _host_ptr(master), _host_ptr(m), _host_ptr(v)),
+           "zero_checkpoint_save")
+
+
+def zero_checkpoint_read_header(path: str) -> CkptHeader:
+    out = CkptHeader()
+    _check(lib().zero_checkpoint_read_header(os.fsencode(path), C.byref(out)),
+           "zero_checkpoint_read_header")
+    return out
+
+
+def zero_checkpoint_load(paths, L: Layout, master, m, v) -> AdamW:
+    """Fills host arrays master/m/v (L.length floats) of rank L.rank from the
+    old ranks' files ``paths``; returns the saved hyperparameters and step."""
+    arr = (C.c_char_p * len(paths))(*[os.fsencode(p) for p in paths])
+    h = AdamW()
+    _check(lib().zero_checkpoint_load(arr, len(paths), C.byref(L), _host_ptr(master),
+                                      _host_ptr(m), _host_ptr(v), C.byref(h)),
+           "zero_checkpoint_load")
+    return h
+
+
+def _host_ptr(a):
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    if hasattr(a, "ctypes"):
+        assert a.flags["C_CONTIGUOUS"] and a.dtype.itemsize == 4
+        return a.ctypes.data
+    return a.data_ptr()
+
+
+def zero_comm_volume_elems(psi: int, stage: int) -> int:
+    return int(lib().zero_comm_volume_elems(psi, stage))
+
+
+def zero_model_state_bytes_mp(psi: int, nd: int, nm: int, stage: int, k: int = 12) -> int:
+    return int(lib().zero_model_state_bytes_mp(psi, nd, nm, stage, k))
 
 
 def zero_reduce_scatter_bucket(g: Grads, bucket_begin: int, bucket_len: int, inv_scale: float,

@@ -22,8 +22,14 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = {
     "zero_kernels.cu": ["nvcc", "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC",
                         "-Xptxas", "-v", "-I", INCLUDE, "-c"],
+    "zero_streamed.cu": ["nvcc", "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler",
+                         "-fPIC", "-Xptxas", "-v", "-I", INCLUDE, "-c"],
+    "zero_gather.cu": ["nvcc", "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC",
+                       "-Xptxas", "-v", "-I", INCLUDE, "-c"],
     "zero_host.cpp": ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-Wextra", "-I", INCLUDE,
                       "-c"],
+    "zero_checkpoint.cpp": ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-Wextra", "-I",
+                            INCLUDE, "-c"],
 }
 
 
@@ -68,7 +74,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
         force = True
         with open(stamp, "w") as f:
             f.write(" ".join(extra))
-    headers = [os.path.join(INCLUDE, "zero.h"), os.path.join(CSRC, "zero_internal.h")]
+    headers = [os.path.join(INCLUDE, "zero.h"), os.path.join(CSRC, "zero_internal.h"),
+               os.path.join(CSRC, "zero_device.cuh")]
     objs, procs = [], []
     for src, cmd in SOURCES.items():
         path = os.path.join(CSRC, src)

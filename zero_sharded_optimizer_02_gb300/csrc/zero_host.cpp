@@ -21,6 +21,7 @@ extern "C" const char* zero_status_string(zero_status_t status)
     case ZERO_ERR_CUDA: return "ZERO_ERR_CUDA: CUDA runtime error";
     case ZERO_ERR_TIMEOUT: return "ZERO_ERR_TIMEOUT: bounded wait expired";
     case ZERO_ERR_UNSUPPORTED: return "ZERO_ERR_UNSUPPORTED: not supported";
+    case ZERO_ERR_IO: return "ZERO_ERR_IO: checkpoint file missing, unreadable or corrupt";
     }
     return "ZERO_ERR_UNKNOWN";
 }
@@ -64,6 +65,24 @@ extern "C" uint64_t zero_model_state_bytes(uint64_t psi, uint32_t nd, uint32_t s
     case 2: return 2 * psi + (2 + (uint64_t)k) * held;       // + gradients partitioned
     default: return bytes_per_param * held;                  // + parameters partitioned
     }
+}
+
+extern "C" uint64_t zero_comm_volume_elems(uint64_t psi, uint32_t stage)
+{
+    if (stage > 3)
+        return UINT64_MAX;
+    const uint64_t times = stage == 3 ? 3 : 2;   // all-reduce (or RS + AG) 2, + param gathers 3
+    if (psi > UINT64_MAX / times)
+        return UINT64_MAX;
+    return times * psi;
+}
+
+extern "C" uint64_t zero_model_state_bytes_mp(uint64_t psi, uint32_t nd, uint32_t nm,
+                                              uint32_t stage, uint32_t k)
+{
+    if (nm == 0)
+        return UINT64_MAX;
+    return zero_model_state_bytes(ceil_div(psi, nm), nd, stage, k);   // one MP slice
 }
 
 namespace zero {

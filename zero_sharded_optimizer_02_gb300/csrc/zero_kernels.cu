@@ -15,15 +15,12 @@
 // intrinsic (__fadd_rn/__fmul_rn/__fdiv_rn/__fsqrt_rn), so no multiply-add is
 // contracted, and the reduction is a per-element sequential fold over ranks
 // 0..Nd-1.  Warp votes are used only for the nonfinite flag.
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include <atomic>
 
-#include "zero.h"
-#include "zero_internal.h"
+#include "zero_device.cuh"
 
 namespace zero {
 namespace {
@@ -32,14 +29,10 @@ constexpr int kThreads = 256;       // threads per CTA
 #ifndef ZERO_CTAS_PER_SM
 #define ZERO_CTAS_PER_SM 2
 #endif
-#ifndef ZERO_RANK_UNROLL
-#define ZERO_RANK_UNROLL 8
-#endif
 // Reduction kernels: resident CTAs per SM (2 x 256 threads leaves ~114
 // registers a thread, enough for 8 rows of 16-byte loads in flight with no
 // spills) and rank rows loaded back to back per thread.
 constexpr int kCtasPerSm = ZERO_CTAS_PER_SM;
-constexpr int kRankUnroll = ZERO_RANK_UNROLL;
 // Elementwise kernels (AdamW from fp32, cast): full occupancy.
 constexpr int kCtasPerSmLight = 8;
 
@@ -54,7 +47,7 @@ constexpr int kCtasPerSmLight = 8;
 #define ZERO_RING_ROWS 8
 #endif
 #ifndef ZERO_RING_DEPTH
-#define ZERO_RING_DEPTH 3
+#define ZERO_RING_DEPTH 2
 #endif
 #ifndef ZERO_RING_THREADS
 #define ZERO_RING_THREADS 512
@@ -65,265 +58,9 @@ constexpr int kRingThreads = ZERO_RING_THREADS;
 constexpr size_t kRingBytes = (size_t)kRingDepth * kRingRows * kRingThreads * 16;
 static_assert(kRingBytes <= 227 * 1024, "ring exceeds shared memory");
 
-// ---------------------------------------------------------------------------
-// Memory access helpers
-// ---------------------------------------------------------------------------
-
-// 16-byte read of gradient data that is used once: bypass L1, hint the L2
-// to fetch the whole 256-byte sector group.
-__device__ __forceinline__ uint4 ld_grad16(const uint16_t* p)
-{
-    uint4 r;
-    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(p));
-    return r;
-}
-
-__device__ __forceinline__ uint16_t ld_grad2(const uint16_t* p)
-{
-    uint16_t r;
-    asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
-    return r;
-}
-
-// 16-byte asynchronous copy global -> shared (L1 bypassed), and its group
-// commit / wait.  wait_group is a hardware wait on this thread's own copies.
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem)
-{
-    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" ::"r"(sa), "l"(gmem)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit()
-{
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
-template <int N>
-__device__ __forceinline__ void cp_async_wait()
-{
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Two 16-bit elements packed in a word (element 0 in the low half) to fp32;
-// both conversions are exact.
-template <int DT>
-__device__ __forceinline__ float2 widen2(uint32_t w)
-{
-    if (DT == ZERO_F16) {
-        __half2 h;
-        static_assert(sizeof(h) == sizeof(w), "half2 is one word");
-        memcpy(&h, &w, sizeof(w));
-        return __half22float2(h);
-    } else {
-        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-    }
-}
-
-template <int DT>
-__device__ __forceinline__ float widen1(uint16_t b)
-{
-    if (DT == ZERO_F16)
-        return __half2float(__ushort_as_half(b));
-    return __uint_as_float((uint32_t)b << 16);
-}
-
-// Round-to-nearest-even fp32 -> fp16/bf16 bits.
-template <int DT>
-__device__ __forceinline__ uint16_t narrow1(float x)
-{
-    if (DT == ZERO_F16)
-        return __half_as_ushort(__float2half_rn(x));
-    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
-}
-
-__device__ __forceinline__ bool nonfinite(float x)
-{
-    return (__float_as_uint(x) & 0x7F800000u) == 0x7F800000u;   // exponent all ones
-}
-
-template <int DT>
-__device__ __forceinline__ void set8(float (&a)[8], uint4 w)
-{
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = widen2<DT>(ws[i]);
-        a[2 * i] = f.x;
-        a[2 * i + 1] = f.y;
-    }
-}
-
-template <int DT>
-__device__ __forceinline__ void add8(float (&a)[8], uint4 w)
-{
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = widen2<DT>(ws[i]);
-        a[2 * i] = __fadd_rn(a[2 * i], f.x);
-        a[2 * i + 1] = __fadd_rn(a[2 * i + 1], f.y);
-    }
-}
-
-// Rank-ordered fold of 8 consecutive elements: acc = ((c_0 + c_1) + ...) +
-// c_{nd-1}.  Rows are loaded kRankUnroll at a time so that many 16-byte
-// reads are in flight per thread; the adds still run in rank order.
-template <int DT>
-__device__ __forceinline__ void fold8(const uint16_t* gp, uint64_t row_stride, uint32_t nd,
-                                      float (&acc)[8])
-{
-    set8<DT>(acc, ld_grad16(gp));
-    for (uint32_t j0 = 1; j0 < nd; j0 += kRankUnroll) {
-        uint4 w[kRankUnroll];
-#pragma unroll
-        for (int u = 0; u < kRankUnroll; ++u)
-            if (j0 + u < nd)
-                w[u] = ld_grad16(gp + (uint64_t)(j0 + u) * row_stride);
-#pragma unroll
-        for (int u = 0; u < kRankUnroll; ++u)
-            if (j0 + u < nd)
-                add8<DT>(acc, w[u]);
-    }
-}
-
-template <int DT>
-__device__ __forceinline__ float fold1(const uint16_t* gp, uint64_t row_stride, uint32_t nd)
-{
-    float s = widen1<DT>(ld_grad2(gp));
-    for (uint32_t j = 1; j < nd; ++j)
-        s = __fadd_rn(s, widen1<DT>(ld_grad2(gp + (uint64_t)j * row_stride)));
-    return s;
-}
-
-// AdamW on one element (decoupled weight decay, bias correction, eps outside
-// the square root), every operation correctly rounded.
-__device__ __forceinline__ void adamw1(const StepScalars& k, float g, float& p, float& m,
-                                       float& v)
-{
-    const float m1 = __fadd_rn(__fmul_rn(k.b1, m), __fmul_rn(k.c1, g));
-    const float v1 = __fadd_rn(__fmul_rn(k.b2, v), __fmul_rn(k.c2, __fmul_rn(g, g)));
-    const float m_hat = __fdiv_rn(m1, k.bc1);
-    const float v_hat = __fdiv_rn(v1, k.bc2);
-    const float u = __fdiv_rn(m_hat, __fadd_rn(__fsqrt_rn(v_hat), k.eps));
-    p = __fsub_rn(__fmul_rn(p, k.wdf), __fmul_rn(k.lr, u));
-    m = m1;
-    v = v1;
-}
-
-// Store 8 consecutive 16-bit values (packed in 4 words) at q, using the
-// widest stores the address phase allows (W = 16, 8, 4 or 2 bytes).
-template <int W>
-__device__ __forceinline__ void store8(uint16_t* q, const uint32_t (&w)[4])
-{
-    if (W == 16) {
-        __stcs(reinterpret_cast<uint4*>(q), make_uint4(w[0], w[1], w[2], w[3]));
-    } else if (W == 8) {
-        __stcs(reinterpret_cast<uint2*>(q), make_uint2(w[0], w[1]));
-        __stcs(reinterpret_cast<uint2*>(q + 4), make_uint2(w[2], w[3]));
-    } else if (W == 4) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            __stcs(reinterpret_cast<unsigned int*>(q + 2 * i), w[i]);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            __stcs(reinterpret_cast<unsigned short*>(q + 2 * i), (unsigned short)(w[i] & 0xFFFF));
-            __stcs(reinterpret_cast<unsigned short*>(q + 2 * i + 1), (unsigned short)(w[i] >> 16));
-        }
-    }
-}
-
-__device__ __forceinline__ void flag_if_any(bool bad, uint32_t* flag)
-{
-    if (__any_sync(0xFFFFFFFFu, bad) && (threadIdx.x & 31) == 0)
-        atomicOr(flag, 1u);
-}
-
-// ---------------------------------------------------------------------------
-// Kernels
-// ---------------------------------------------------------------------------
-
-// Element split of a window [0, len): `head` scalar elements up to the first
-// 16-byte aligned gradient element, `nvec` 8-element vectors, then a scalar
-// tail.  Scalar elements are handled by the first threads of the grid.
-struct Split {
-    uint64_t len;
-    uint64_t head;
-    uint64_t nvec;
-    __host__ __device__ __forceinline__ uint64_t nscalar() const { return len - 8 * nvec; }
-    __host__ __device__ __forceinline__ uint64_t scalar_elem(uint64_t t) const
-    {
-        return t < head ? t : head + 8 * nvec + (t - head);
-    }
-};
-
-struct FusedArgs {
-    const uint16_t* g;     // element 0 of the window in row 0
-    uint64_t row_stride;   // elements
-    uint32_t nd;
-    Split sp;
-    const float* p_in;
-    const float* m_in;
-    const float* v_in;
-    float* p_out;
-    float* m_out;
-    float* v_out;
-    uint16_t* gath;        // gathered element of window element 0
-    StepScalars k;
-    uint32_t* flag;
-};
-
-// Scalar element e of the window (head or tail): fold, AdamW, cast.
-template <int DT>
-__device__ __forceinline__ bool fused_scalar(const FusedArgs& a, uint64_t e)
-{
-    const float s = fold1<DT>(a.g + e, a.row_stride, a.nd);
-    float p = a.p_in[e], m = a.m_in[e], v = a.v_in[e];
-    adamw1(a.k, __fmul_rn(s, a.k.inv), p, m, v);
-    a.p_out[e] = p;
-    a.m_out[e] = m;
-    a.v_out[e] = v;
-    a.gath[e] = narrow1<DT>(p);
-    return nonfinite(s);
-}
-
-// Epilogue of 8 reduced sums at window element e (16-byte aligned state):
-// scale, AdamW, streaming state stores, cast into the gathered slot.  Runs in
-// two halves of 4 elements to bound live registers.  Returns "any nonfinite".
-template <int DT, int W>
-__device__ __forceinline__ bool fused_epilogue(const FusedArgs& a, uint64_t e, const float (&s)[8])
-{
-    bool bad = false;
-    uint32_t out16[4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const float4 pp = __ldcs(reinterpret_cast<const float4*>(a.p_in + e) + h);
-        const float4 mm = __ldcs(reinterpret_cast<const float4*>(a.m_in + e) + h);
-        const float4 vv = __ldcs(reinterpret_cast<const float4*>(a.v_in + e) + h);
-        float p[4] = {pp.x, pp.y, pp.z, pp.w};
-        float m[4] = {mm.x, mm.y, mm.z, mm.w};
-        float v[4] = {vv.x, vv.y, vv.z, vv.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            bad |= nonfinite(s[4 * h + i]);
-            adamw1(a.k, __fmul_rn(s[4 * h + i], a.k.inv), p[i], m[i], v[i]);
-        }
-        __stcs(reinterpret_cast<float4*>(a.p_out + e) + h, make_float4(p[0], p[1], p[2], p[3]));
-        __stcs(reinterpret_cast<float4*>(a.m_out + e) + h, make_float4(m[0], m[1], m[2], m[3]));
-        __stcs(reinterpret_cast<float4*>(a.v_out + e) + h, make_float4(v[0], v[1], v[2], v[3]));
-        out16[2 * h] = (uint32_t)narrow1<DT>(p[0]) | ((uint32_t)narrow1<DT>(p[1]) << 16);
-        out16[2 * h + 1] = (uint32_t)narrow1<DT>(p[2]) | ((uint32_t)narrow1<DT>(p[3]) << 16);
-    }
-    store8<W>(a.gath + e, out16);
-    return bad;
-}
-
 // K4, register variant: fused reduce + scale + AdamW + cast, one pass over
 // the window; each thread loads kRankUnroll rows of 16 bytes back to back.
-template <int DT, int W>
+template <int DT, int W, bool V8>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_step_fused(const FusedArgs a)
 {
     bool bad = false;
@@ -335,7 +72,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_step_fused(const Fused
         const uint64_t e = a.sp.head + 8 * q;
         float s[8];
         fold8<DT>(a.g + e, a.row_stride, a.nd, s);
-        bad |= fused_epilogue<DT, W>(a, e, s);
+        bad |= fused_epilogue<DT, W, V8>(a, e, s);
     }
     flag_if_any(bad, a.flag);
 }
@@ -348,7 +85,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_step_fused(const Fused
 // reads are contiguous.  Only the issuing thread reads its slots, so
 // cp.async.wait_group needs no block barrier.  Rows are still folded in
 // rank order.
-template <int DT, int W>
+template <int DT, int W, bool V8>
 __global__ void __launch_bounds__(kRingThreads, 1) k_step_fused_ring(const FusedArgs a)
 {
     extern __shared__ uint4 ring[];
@@ -406,7 +143,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_step_fused_ring(const Fused
         slot_c = slot_c + 1 == kRingDepth ? 0 : slot_c + 1;
         if (++gc == groups) {
             gc = 0;
-            bad |= fused_epilogue<DT, W>(a, a.sp.head + 8 * qc, acc);
+            bad |= fused_epilogue<DT, W, V8>(a, a.sp.head + 8 * qc, acc);
             qc += nthr;
         }
     }
@@ -662,33 +399,42 @@ int sm_count()
     return sms;
 }
 
-template <int DT, int W>
+template <int DT, int W, bool V8>
 void launch_fused_w(const FusedArgs& a, cudaStream_t s)
 {
     const uint64_t work = a.sp.nvec > a.sp.nscalar() ? a.sp.nvec : a.sp.nscalar();
     if (ZERO_FUSED_IMPL == 1) {
         // one resident CTA per SM; the ring needs the opt-in shared memory
         // size (a per-device function attribute, so set on every launch)
-        cudaFuncSetAttribute(k_step_fused_ring<DT, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kRingBytes);
+        cudaFuncSetAttribute(k_step_fused_ring<DT, W, V8>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingBytes);
         const uint64_t want = (work + kRingThreads - 1) / kRingThreads;
         const uint64_t cap = (uint64_t)sm_count();
         const unsigned grid = (unsigned)(want < cap ? (want ? want : 1) : cap);
-        k_step_fused_ring<DT, W><<<grid, kRingThreads, kRingBytes, s>>>(a);
+        k_step_fused_ring<DT, W, V8><<<grid, kRingThreads, kRingBytes, s>>>(a);
     } else {
-        k_step_fused<DT, W><<<grid_for(work), kThreads, 0, s>>>(a);
+        k_step_fused<DT, W, V8><<<grid_for(work), kThreads, 0, s>>>(a);
+    }
+}
+
+template <int DT, bool V8>
+void launch_fused_v(const FusedArgs& a, int width, cudaStream_t s)
+{
+    switch (width) {
+    case 16: launch_fused_w<DT, 16, V8>(a, s); break;
+    case 8: launch_fused_w<DT, 8, V8>(a, s); break;
+    case 4: launch_fused_w<DT, 4, V8>(a, s); break;
+    default: launch_fused_w<DT, 2, V8>(a, s); break;
     }
 }
 
 template <int DT>
-void launch_fused_dt(const FusedArgs& a, int width, cudaStream_t s)
+void launch_fused_dt(const FusedArgs& a, int width, bool v8, cudaStream_t s)
 {
-    switch (width) {
-    case 16: launch_fused_w<DT, 16>(a, s); break;
-    case 8: launch_fused_w<DT, 8>(a, s); break;
-    case 4: launch_fused_w<DT, 4>(a, s); break;
-    default: launch_fused_w<DT, 2>(a, s); break;
-    }
+    if (v8)
+        launch_fused_v<DT, true>(a, width, s);
+    else
+        launch_fused_v<DT, false>(a, width, s);
 }
 
 void launch_reduce(const ReduceArgs& a, int dtype, cudaStream_t s)
@@ -882,10 +628,12 @@ extern "C" zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layou
                     in->master + b0, in->m + b0, in->v + b0, out->master + b0, out->m + b0,
                     out->v + b0, gath + b0, k, d_nonfinite};
         const int width = store_width(gath + b0 + a.sp.head);
+        const float* const sp[6] = {in->master, in->m, in->v, out->master, out->m, out->v};
+        const bool v8 = state_v8_ok(sp);
         if (g->dtype == ZERO_F16)
-            launch_fused_dt<ZERO_F16>(a, width, s);
+            launch_fused_dt<ZERO_F16>(a, width, v8, s);
         else
-            launch_fused_dt<ZERO_BF16>(a, width, s);
+            launch_fused_dt<ZERO_BF16>(a, width, v8, s);
         st = launch_status();
         if (st != ZERO_OK)
             return st;

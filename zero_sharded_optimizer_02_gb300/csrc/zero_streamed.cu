@@ -1,0 +1,302 @@
+// Bucket-ready shard step: the optimizer starts on a bucket as soon as its
+// reduced gradients have landed (sm_103a).
+//
+// "ZeRO: Memory Optimizations Toward Training Trillion Parameter Models",
+// section "ZeRO-DP", Stage 2: gradients are reduce-scattered bucket by bucket
+// during the backward pass.  Here the producer of a bucket -- in one GPU's
+// emulation, a copy stream landing the bucket's Nd contribution slices --
+// writes the bucket's ready word after its data; one persistent kernel walks
+// the shard's buckets in order and, before each, waits for that word.
+//
+// Every wait is bounded: thread 0 of each CTA polls the word with an acquire
+// load, sleeping between polls, for at most timeout_ns of %globaltimer time
+// and a matching iteration cap.  On expiry it records ZERO_ERR_TIMEOUT in the
+// status word and the CTA returns without touching that bucket or later ones;
+// the context stays usable.  The kernel never waits on another kernel: only on
+// a word written by a copy engine or the host.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zero_device.cuh"
+
+namespace zero {
+namespace {
+
+constexpr int kStreamThreads = 256;
+constexpr int kStreamCtasPerSm = 2;
+
+// Gradient loads of this kernel read data that arrives while it runs, so they
+// go through L2 (.cg) instead of the non-coherent path.
+__device__ __forceinline__ uint4 ld_grad16_cg(const uint16_t* p)
+{
+    return __ldcg(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ uint16_t ld_grad2_cg(const uint16_t* p)
+{
+    return __ldcg(reinterpret_cast<const unsigned short*>(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bounded wait for *word >= epoch (by wrap-around comparison).
+__device__ bool wait_ready(const uint32_t* word, uint32_t epoch, uint64_t timeout_ns)
+{
+    const uint64_t t0 = global_ns();
+    const uint64_t max_polls = timeout_ns / 64 + 16;   // each poll sleeps >= ~64 ns
+    for (uint64_t i = 0; i < max_polls; ++i) {
+        if ((int32_t)(ld_acquire(word) - epoch) >= 0)
+            return true;
+        if (global_ns() - t0 > timeout_ns)
+            return false;
+        __nanosleep(64);
+    }
+    return (int32_t)(ld_acquire(word) - epoch) >= 0;
+}
+
+template <int DT>
+__device__ __forceinline__ void fold8_cg(const uint16_t* gp, uint64_t row_stride, uint32_t nd,
+                                         float (&acc)[8])
+{
+    set8<DT>(acc, ld_grad16_cg(gp));
+    for (uint32_t j0 = 1; j0 < nd; j0 += kRankUnroll) {
+        uint4 w[kRankUnroll];
+#pragma unroll
+        for (int u = 0; u < kRankUnroll; ++u)
+            if (j0 + u < nd)
+                w[u] = ld_grad16_cg(gp + (uint64_t)(j0 + u) * row_stride);
+#pragma unroll
+        for (int u = 0; u < kRankUnroll; ++u)
+            if (j0 + u < nd)
+                add8<DT>(acc, w[u]);
+    }
+}
+
+struct StreamArgs {
+    FusedArgs a;           // the whole shard: pointers at shard element 0
+    uint64_t n;            // shard length
+    uint64_t bucket;       // bucket size (elements)
+    uint64_t phase;        // gradient element phase of shard element 0 (offset % 8)
+    const uint32_t* ready; // ready word of each bucket
+    uint32_t epoch;
+    uint64_t timeout_ns;
+    uint32_t* status;      // ZERO_ERR_TIMEOUT is recorded here on expiry
+};
+
+template <int DT, int W, bool V8>
+__global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) k_step_streamed(const StreamArgs s)
+{
+    __shared__ int s_ok;
+    bool bad = false;
+    const uint64_t tid = (uint64_t)blockIdx.x * kStreamThreads + threadIdx.x;
+    const uint64_t nthr = (uint64_t)gridDim.x * kStreamThreads;
+    const uint64_t nb = (s.n + s.bucket - 1) / s.bucket;
+    for (uint64_t b = 0; b < nb; ++b) {
+        if (threadIdx.x == 0)
+            s_ok = wait_ready(s.ready + b, s.epoch, s.timeout_ns) ? 1 : 0;
+        __syncthreads();
+        const bool ok = s_ok != 0;
+        __syncthreads();            // s_ok is rewritten in the next round
+        if (!ok) {
+            if (threadIdx.x == 0)
+                atomicCAS(s.status, 0u, (uint32_t)ZERO_ERR_TIMEOUT);
+            break;
+        }
+        const uint64_t b0 = b * s.bucket;
+        const uint64_t len = s.n - b0 < s.bucket ? s.n - b0 : s.bucket;
+        Split sp;
+        sp.len = len;
+        const uint64_t head = (8 - ((s.phase + b0) & 7)) & 7;
+        sp.head = head < len ? head : len;
+        sp.nvec = (len - sp.head) / 8;
+        FusedArgs a = s.a;
+        a.g += b0;
+        a.p_in += b0;
+        a.m_in += b0;
+        a.v_in += b0;
+        a.p_out += b0;
+        a.m_out += b0;
+        a.v_out += b0;
+        a.gath += b0;
+        a.sp = sp;
+        if (tid < sp.nscalar()) {
+            const uint64_t e = sp.scalar_elem(tid);
+            float g = widen1<DT>(ld_grad2_cg(a.g + e));
+            for (uint32_t j = 1; j < a.nd; ++j)
+                g = __fadd_rn(g, widen1<DT>(ld_grad2_cg(a.g + e + (uint64_t)j * a.row_stride)));
+            bad |= nonfinite(g);
+            float p = a.p_in[e], m = a.m_in[e], v = a.v_in[e];
+            adamw1(a.k, __fmul_rn(g, a.k.inv), p, m, v);
+            a.p_out[e] = p;
+            a.m_out[e] = m;
+            a.v_out[e] = v;
+            a.gath[e] = narrow1<DT>(p);
+        }
+        for (uint64_t q = tid; q < sp.nvec; q += nthr) {
+            const uint64_t e = sp.head + 8 * q;
+            float acc[8];
+            fold8_cg<DT>(a.g + e, a.row_stride, a.nd, acc);
+            bad |= fused_epilogue<DT, W, V8>(a, e, acc);
+        }
+    }
+    flag_if_any(bad, s.a.flag);
+}
+
+int sms_streamed()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+        sms = 1;
+    return sms;
+}
+
+bool is_aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+bool overlap(const void* a, const void* b, uint64_t bytes)
+{
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + bytes && y < x + bytes;
+}
+
+}  // namespace
+}  // namespace zero
+
+using namespace zero;
+
+extern "C" zero_status_t zero_step_shard_streamed(
+    const zero_grads_t* g, const zero_layout_t* L, const zero_state_t* in,
+    const zero_state_t* out, void* gathered, uint64_t gathered_offset_elems,
+    uint64_t bucket_elems, double loss_scale, const zero_adamw_t* h, const uint32_t* d_ready,
+    uint32_t epoch, uint64_t timeout_ns, uint32_t* d_nonfinite, uint32_t* d_status,
+    void* stream)
+{
+    if (!g || !L || !in || !out || !gathered || !h || !d_ready || !d_nonfinite || !d_status ||
+        bucket_elems == 0 || !(loss_scale > 0.0 && loss_scale <= 1.0e300) || !adamw_valid(h))
+        return ZERO_ERR_INVALID_ARG;
+    if (timeout_ns == 0 || timeout_ns > ZERO_MAX_WAIT_NS)
+        return ZERO_ERR_INVALID_ARG;   // every device wait must stay bounded
+    if (!g->base || g->nd == 0 || g->nd != L->nd || (g->dtype != ZERO_F16 && g->dtype != ZERO_BF16) ||
+        L->length > L->shard_elems)
+        return ZERO_ERR_INVALID_ARG;
+    if (!is_aligned(g->base, 16) || (g->row_stride & 7) || (g->offset & 7) ||
+        !is_aligned(gathered, 2) || !is_aligned(d_ready, 4) || !is_aligned(d_nonfinite, 4) ||
+        !is_aligned(d_status, 4))
+        return ZERO_ERR_ALIGNMENT;
+    const float* ins[3] = {in->master, in->m, in->v};
+    float* outs[3] = {out->master, out->m, out->v};
+    const uint64_t n = L->length;
+    const uint64_t lim = 1ull << 61;   // element indices stay far from overflow
+    if (n > lim || g->offset > lim - n ||
+        (g->nd > 1 && g->row_stride > (lim - g->offset - n) / (g->nd - 1)))
+        return ZERO_ERR_INVALID_ARG;
+    for (int i = 0; i < 3; ++i) {
+        if (!ins[i] || !outs[i])
+            return ZERO_ERR_INVALID_ARG;
+        if (!is_aligned(ins[i], 16) || !is_aligned(outs[i], 16))
+            return ZERO_ERR_ALIGNMENT;
+        for (int j = 0; j < 3; ++j)
+            if (!(i == j && outs[i] == ins[j]) && overlap(outs[i], ins[j], n * 4))
+                return ZERO_ERR_INVALID_ARG;
+    }
+    if (n == 0)
+        return ZERO_OK;
+    StreamArgs s;
+    s.a.g = static_cast<const uint16_t*>(g->base) + g->offset;
+    s.a.row_stride = g->row_stride;
+    s.a.nd = g->nd;
+    s.a.sp = Split{0, 0, 0};
+    s.a.p_in = in->master;
+    s.a.m_in = in->m;
+    s.a.v_in = in->v;
+    s.a.p_out = out->master;
+    s.a.m_out = out->m;
+    s.a.v_out = out->v;
+    s.a.gath = static_cast<uint16_t*>(gathered) + gathered_offset_elems;
+    s.a.k = make_scalars(h, g->nd, loss_scale);
+    s.a.flag = d_nonfinite;
+    s.n = n;
+    s.bucket = bucket_elems;
+    s.phase = g->offset & 7;
+    s.ready = d_ready;
+    s.epoch = epoch;
+    s.timeout_ns = timeout_ns;
+    s.status = d_status;
+    // Every bucket's first vector starts at a shard element b0 + head that is
+    // a multiple of 8 (offset is), so one store width fits all buckets.
+    const uint64_t head0 = (8 - (s.phase & 7)) & 7;
+    const uintptr_t a0 = (uintptr_t)(s.a.gath + head0);
+    const int width = (a0 & 15) == 0 ? 16 : (a0 & 7) == 0 ? 8 : (a0 & 3) == 0 ? 4 : 2;
+    const uint64_t want = (n / 8 + kStreamThreads - 1) / kStreamThreads;
+    const uint64_t cap = (uint64_t)sms_streamed() * kStreamCtasPerSm;
+    const unsigned grid = (unsigned)(want == 0 ? 1 : (want < cap ? want : cap));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+#define ZERO_STREAM_LAUNCH(DT, V8)                                                          \
+    switch (width) {                                                                        \
+    case 16: k_step_streamed<DT, 16, V8><<<grid, kStreamThreads, 0, st>>>(s); break;        \
+    case 8: k_step_streamed<DT, 8, V8><<<grid, kStreamThreads, 0, st>>>(s); break;          \
+    case 4: k_step_streamed<DT, 4, V8><<<grid, kStreamThreads, 0, st>>>(s); break;          \
+    default: k_step_streamed<DT, 2, V8><<<grid, kStreamThreads, 0, st>>>(s); break;         \
+    }
+    const float* const sp[6] = {in->master, in->m, in->v, out->master, out->m, out->v};
+    const bool v8 = state_v8_ok(sp);
+    if (g->dtype == ZERO_F16) {
+        if (v8) {
+            ZERO_STREAM_LAUNCH(ZERO_F16, true)
+        } else {
+            ZERO_STREAM_LAUNCH(ZERO_F16, false)
+        }
+    } else {
+        if (v8) {
+            ZERO_STREAM_LAUNCH(ZERO_BF16, true)
+        } else {
+            ZERO_STREAM_LAUNCH(ZERO_BF16, false)
+        }
+    }
+#undef ZERO_STREAM_LAUNCH
+    return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ERR_CUDA;
+}
+
+extern "C" zero_status_t zero_feed_buckets(const void* host, uint64_t host_row_stride,
+                                           const zero_grads_t* g, uint64_t n,
+                                           uint64_t bucket_elems, uint32_t* d_ready,
+                                           const uint32_t* h_epoch, void* copy_stream)
+{
+    if (!host || !g || !g->base || g->nd == 0 || !d_ready || !h_epoch || bucket_elems == 0)
+        return ZERO_ERR_INVALID_ARG;
+    if (host_row_stride < n || g->row_stride < g->offset + n ||
+        host_row_stride > (1ull << 60) / 2 || g->row_stride > (1ull << 60) / 2)
+        return ZERO_ERR_INVALID_ARG;
+    if (!is_aligned(host, 2) || !is_aligned(g->base, 2) || !is_aligned(d_ready, 4) ||
+        !is_aligned(h_epoch, 4))
+        return ZERO_ERR_ALIGNMENT;
+    cudaStream_t st = static_cast<cudaStream_t>(copy_stream);
+    const char* src = static_cast<const char*>(host);
+    char* dst = const_cast<char*>(static_cast<const char*>(g->base)) + 2 * g->offset;
+    const uint64_t nb = (n + bucket_elems - 1) / bucket_elems;
+    for (uint64_t b = 0; b < nb; ++b) {
+        const uint64_t b0 = b * bucket_elems;
+        const uint64_t len = n - b0 < bucket_elems ? n - b0 : bucket_elems;
+        // the bucket's slice of every contributor row, then its ready word
+        if (cudaMemcpy2DAsync(dst + 2 * b0, 2 * g->row_stride, src + 2 * b0,
+                              2 * host_row_stride, 2 * len, g->nd, cudaMemcpyHostToDevice,
+                              st) != cudaSuccess ||
+            cudaMemcpyAsync(d_ready + b, h_epoch, sizeof(uint32_t), cudaMemcpyHostToDevice,
+                            st) != cudaSuccess)
+            return ZERO_ERR_CUDA;
+    }
+    return ZERO_OK;
+}

@@ -91,7 +91,9 @@ class DataParallelStep:
     ranks        the ranks held here (all of range(nd) for full emulation)
     gathered     "full": one flat fp16/bf16 buffer of nd * S parameters that
                  every rank writes its slot of; "slot": one S-element buffer
-                 per rank (the persistent parameters of a ZeRO-3 rank)
+                 per rank (the persistent parameters of a ZeRO-3 rank);
+                 "pitched": the ranks' slots as rows of one [nd, pitch] buffer
+                 (what zero_gather_range collects a layer from)
     fused        zero_step_shard (default) or zero_step_shard_unfused
     process_group  if given, the skip flag is OR-ed over it every step
     """
@@ -115,6 +117,10 @@ class DataParallelStep:
         if gathered == "full":
             n = nd * s + 8
             self.gathered = [torch.zeros(n, dtype=tdt, device=self.device) for _ in range(2)]
+        elif gathered == "pitched":
+            pitch = int(self.layouts[self.ranks[0]].row_pitch)
+            self.gathered = [torch.zeros(nd, max(pitch, 8), dtype=tdt, device=self.device)
+                             for _ in range(2)]
         elif gathered == "slot":
             self.gathered = [{r: torch.zeros(max(s, 1) + 8, dtype=tdt, device=self.device)
                               for r in self.ranks} for _ in range(2)]
@@ -138,13 +144,15 @@ class DataParallelStep:
 
     def gathered_view(self, rank=None, which: str = "cur") -> torch.Tensor:
         i = self.gcur if which == "cur" else 1 - self.gcur
-        if self.gathered_mode == "full":
+        if self.gathered_mode in ("full", "pitched"):
             return self.gathered[i]
         return self.gathered[i][rank]
 
     def _gathered_target(self, r, i):
         if self.gathered_mode == "full":
             return self.gathered[i], int(self.layouts[r].begin)
+        if self.gathered_mode == "pitched":
+            return self.gathered[i], r * int(self.gathered[i].shape[1])
         return self.gathered[i][r], 0
 
     # -- the step ------------------------------------------------------------
@@ -191,6 +199,80 @@ class DataParallelStep:
             st.cur = 1 - st.cur
         self.gcur = 1 - self.gcur
         self.t += 1
+
+    # -- gradients fed from host memory, bucket by bucket ----------------------
+
+    def launch_host_fed(self, rank: int, host_rows, dev_grads, stream_bucket: int,
+                        copy_stream, timeout_ns: int = 10_000_000_000) -> int:
+        """Launch rank's step with its gradients still in (pinned) host memory:
+        the bucket-ready kernel runs on ``self.stream`` while the feeder lands
+        each bucket's contributions on ``copy_stream`` and marks it ready, so
+        the optimizer overlaps the transfer.  ``host_rows`` is [nd, m] pinned
+        (contributor j's shard at row j); ``dev_grads`` the Grads descriptor of
+        the device rows they land in.  Returns the kernel launches issued."""
+        L = self.layouts[rank]
+        n = int(L.length)
+        nb = -(-n // stream_bucket) if n else 0
+        if not hasattr(self, "_ready") or self._ready.numel() < max(nb, 1):
+            self._ready = torch.zeros(max(nb, 1), dtype=torch.int32, device=self.device)
+            self._epoch = 0
+            self._epoch_host = torch.zeros(1, dtype=torch.int32, pin_memory=True)
+            self._status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self._epoch += 1
+        self._epoch_host[0] = self._epoch
+        self.h.step = self.t + 1
+        st = self.state[rank]
+        gbuf, goff = self._gathered_target(rank, 1 - self.gcur)
+        start = torch.cuda.Event()
+        start.record(self.stream)
+        copy_stream.wait_event(start)      # the feed starts after earlier work on self.stream
+        _abi.zero_step_shard_streamed(dev_grads, L, st.states[st.cur], st.states[1 - st.cur],
+                                      gbuf, goff, stream_bucket, self.loss_scale, self.h,
+                                      self._ready, self._epoch, timeout_ns, self.flag,
+                                      self._status, self.stream)
+        _abi.zero_feed_buckets(host_rows, int(host_rows.shape[1]), dev_grads, n, stream_bucket,
+                               self._ready, self._epoch_host, copy_stream)
+        return 1
+
+    def host_fed_status(self) -> int:
+        """ZERO_OK, or ZERO_ERR_TIMEOUT if a bucket never arrived (read after
+        the stream work completed)."""
+        return int(self._status.item()) if hasattr(self, "_status") else 0
+
+    # -- sharded checkpoints ---------------------------------------------------
+
+    def checkpoint_paths(self, directory: str, nd: int | None = None) -> list:
+        import os
+        nd = self.nd if nd is None else nd
+        return [os.path.join(directory, f"zero_rank{r:05d}_of_{nd:05d}.zck") for r in range(nd)]
+
+    def save_checkpoint(self, directory: str) -> list:
+        """Each held rank writes its committed state to its own file."""
+        import os
+        os.makedirs(directory, exist_ok=True)
+        paths = self.checkpoint_paths(directory)
+        h = _abi.adamw(self.hp["lr"], self.hp["beta1"], self.hp["beta2"], self.hp["eps"],
+                       self.hp["weight_decay"], self.t)
+        self.stream.synchronize()
+        for r in self.ranks:
+            host = [t.cpu().numpy() for t in self.state[r].tensors("cur")]
+            _abi.zero_checkpoint_save(paths[r], self.layouts[r], h, *host)
+        return [paths[r] for r in self.ranks]
+
+    def load_checkpoint(self, paths: list) -> None:
+        """Loads every held rank's state from a checkpoint saved with
+        len(paths) ranks (resharding if that differs from nd)."""
+        import numpy as np
+        step = None
+        for r in self.ranks:
+            n = int(self.layouts[r].length)
+            host = [np.empty(max(n, 1), np.float32) for _ in range(3)]
+            h = _abi.zero_checkpoint_load(paths, self.layouts[r], *host)
+            step = int(h.step)
+            with torch.cuda.stream(self.stream):
+                self.state[r].load(*(torch.from_numpy(a[:n]) for a in host))
+        self.stream.synchronize()
+        self.t = step
 
     def step(self, grads: dict) -> bool:
         """One full step: launch, global decision, commit.  Returns True if skipped."""
