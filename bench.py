@@ -153,8 +153,8 @@ def run_gpu(args) -> None:
 
     import synth
     from zero_sharded_optimizer_02_gb300 import build
-    from zero_sharded_optimizer_02_gb300.step import (DataParallelStep, data_parallel_rank,
-                                                      max_over_ranks)
+    from zero_sharded_optimizer_02_gb300.step import (DataParallelStep, PipelinedStep,
+                                                      data_parallel_rank, max_over_ranks)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -184,41 +184,65 @@ def run_gpu(args) -> None:
         st = dps.state[dp_rank]
         for row, which in zip(st.bufs[st.cur], ("master", "m", "v")):
             synth.fill_shard_state(w, dp_rank, which, row)
-        grads = torch.empty(w.nd, pitch, dtype=synth.WORKLOADS[args.config].torch_grad_dtype,
-                            device=dev)
+        row_stride = pitch + args.row_pad
+        grads = torch.empty(w.nd, row_stride, dtype=w.torch_grad_dtype, device=dev)
         synth.fill_shard_rows(w, 0, dp_rank, grads)
         from zero_sharded_optimizer_02_gb300 import _abi
-        desc = {dp_rank: _abi.grads(grads, pitch, 0, w.nd, w.grad_dtype)}
+        desc = {dp_rank: _abi.grads(grads, row_stride, 0, w.nd, w.grad_dtype)}
+        pipe = PipelinedStep(w.psi, w.nd, [dp_rank], w.grad_dtype, w.hparams, w.loss_scale,
+                             w.bucket, dev, gathered="slot", process_group=group,
+                             stream=stream)
+        pipe.state[dp_rank].bufs[0].copy_(st.bufs[st.cur])
     torch.cuda.synchronize(dev)
 
-    # -- warm-up, then K timed steps ------------------------------------------
+    # -- warm-up, then K timed steps.  The pipelined driver launches step k+1
+    #    before it reads step k's flag (a skip re-runs the speculative step),
+    #    so the GPU never waits for the host; every step is the whole path:
+    #    fused kernel, flag read, commit or global skip. -----------------------
     for _ in range(args.warmup):
-        dps.step(desc)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+        pipe.launch(desc)
+    pipe.finish()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(smi_index(local)) if rank == 0 else None
     time.sleep(0.3 if sampler else 0.0)
-    launches = 0
-    skipped = 0
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
+    launched0 = pipe.launched
     wall0 = time.time()
     t_start.record(stream)
+    decided = []
     for k in range(args.steps):
-        ev[k][0].record(stream)
-        launches += dps.launch(desc)
-        ev[k][1].record(stream)
-        s = dps.decide()
-        dps.commit(s)
-        skipped += int(s)
+        decided += pipe.launch(desc)
+    decided += pipe.finish()
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     wall1 = time.time()
     if world > 1:
         dist.barrier()
     total_ms = t_start.elapsed_time(t_end)
+    launches = pipe.launched - launched0
+    skipped = sum(decided)
+    assert len(decided) == args.steps
+
+    # -- the same steps with the synchronous driver (flag read before the next
+    #    launch), for comparison; per-launch events inside its steps ----------
+    for _ in range(args.warmup):
+        dps.step(desc)
+    nsync = max(1, min(args.steps, 100))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(nsync)]
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    s0.record(stream)
+    for k in range(nsync):
+        ev[k][0].record(stream)
+        dps.launch(desc)
+        ev[k][1].record(stream)
+        dps.commit(dps.decide())
+    s1.record(stream)
+    torch.cuda.synchronize(dev)
+    sync_ms = max_over_ranks(s0.elapsed_time(s1) / nsync, group, dev)
     kernel_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = max_over_ranks(total_ms, group, dev)
 
@@ -283,7 +307,8 @@ def run_gpu(args) -> None:
         assert dps.host_fed_status() == 0, "a bucket never arrived"
         seq_ms = max_over_ranks(timed(sequential), group, dev)
         e2e = {"value": world * n / (fed_ms * 1e-3), "unit": UNIT,
-               "h2d_bytes_per_step": host_grads.numel() * host_grads.element_size(),
+               "h2d_bytes_per_step": w.nd * n * host_grads.element_size() + 4 * (
+                   -(-n // stream_bucket)),
                "d2h_bytes_per_step": n * host_params.element_size() + 4,
                "ms_per_step": fed_ms, "steps": args.e2e_steps,
                "path": f"zero_feed_buckets + zero_step_shard_streamed, "
@@ -324,6 +349,7 @@ def run_gpu(args) -> None:
         "config": {"workload": f"{args.config}: {w.title}", "psi": w.psi, "nd": w.nd,
                    "rank": dp_rank, "shard_params": n, "grad_dtype": w.grad_dtype,
                    "bucket": w.bucket, "loss_scale": w.loss_scale,
+                   "row_stride_elems": row_stride,
                    "l2": f"inputs larger than L2 ({bytes_per_param * n / 1e9:.1f} GB per step),"
                          " no flush",
                    "parallelism": f"zero-dp{w.nd} emulated, {world} process(es)"},
@@ -337,6 +363,8 @@ def run_gpu(args) -> None:
                      "algorithmic_bytes_per_launch": bytes_per_param * n},
         "e2e": e2e,
         "gpu_launches": launches,
+        "driver": "pipelined (step k+1 launched before step k's flag is read)",
+        "ms_per_step_sync_driver": sync_ms,
         "build_flags": os.environ.get("ZERO_NVCC_FLAGS", ""),
         "skipped_steps": skipped,
         "clocks": clocks,
@@ -432,6 +460,89 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+def run_gather(args) -> None:
+    """ZeRO-3 on-demand gather: zero_gather_range collecting the whole flat
+    fp16 parameter vector of a workload from its Nd pitched shards (the worst
+    case of a layer gather: every shard segment).  HBM roofline: 2 B read +
+    2 B written per parameter."""
+    import torch
+
+    import synth
+    from zero_sharded_optimizer_02_gb300 import _abi, build
+    build.build()
+    dev = torch.device("cuda", 0)
+    w = synth.WORKLOADS[args.config]
+    L = _abi.zero_partition_layout(w.psi, w.nd, 0, 8)
+    pitch = int(L.row_pitch)
+    shards = torch.randint(-30000, 30000, (w.nd, pitch), dtype=torch.int16, device=dev)
+    out = torch.empty(w.psi, dtype=torch.int16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        _abi.zero_gather_range(shards, pitch, w.psi, w.nd, 0, w.psi, 2, out, stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(args.steps):
+        _abi.zero_gather_range(shards, pitch, w.psi, w.nd, 0, w.psi, 2, out, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / args.steps
+    # spot check against the flat concatenation
+    s = int(L.shard_elems)
+    for i in (0, 1, s - 1, s, w.psi // 2, w.psi - 1):
+        assert int(out[i]) == int(shards[i // s, i % s]), i
+    gbs = 4 * w.psi / (ms * 1e-3) / 1e9
+    peak = measured_peaks().get("hbm_gbs", 6800.0)
+    print(json.dumps({"op": "zero_gather_range", "metric": "params gathered/s", "value":
+                      w.psi / (ms * 1e-3), "unit": "params/s", "ms_per_gather": ms,
+                      "config": {"workload": f"{args.config}: {w.title}", "psi": w.psi,
+                                 "nd": w.nd, "segments": w.nd, "elem_bytes": 2},
+                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak,
+                                   "unit": "GB/s", "frac": gbs / peak,
+                                   "algorithmic_bytes_per_param": 4},
+                      "gpu_launches": args.steps * w.nd}), flush=True)
+
+
+def run_checkpoint(args) -> None:
+    """Sharded checkpoint of one rank's fp32 state (master, m, v): save, then
+    load with resharding to Nd + 1 ranks of the same flat vector (host I/O)."""
+    import tempfile
+
+    import numpy as np
+
+    import synth
+    from zero_sharded_optimizer_02_gb300 import _abi, build
+    build.build()
+    w = synth.WORKLOADS[args.config]
+    nd = w.nd
+    d = tempfile.mkdtemp(prefix="zero_ckpt_")
+    paths, total = [], 0
+    saves = []
+    for r in range(nd):
+        L = _abi.zero_partition_layout(w.psi, nd, r, 8)
+        n = int(L.length)
+        arr = [np.full(n, k + r, np.float32) for k in range(3)]
+        p = os.path.join(d, f"r{r}.zck")
+        t0 = time.perf_counter()
+        _abi.zero_checkpoint_save(p, L, _abi.adamw(**w.hparams, step=7), *arr)
+        saves.append(time.perf_counter() - t0)
+        paths.append(p)
+        total += 12 * n
+    L = _abi.zero_partition_layout(w.psi, nd + 1, 0, 8)
+    buf = [np.empty(int(L.length), np.float32) for _ in range(3)]
+    t0 = time.perf_counter()
+    _abi.zero_checkpoint_load(paths, L, *buf)
+    load_s = time.perf_counter() - t0
+    for p in paths:
+        os.remove(p)
+    os.rmdir(d)
+    print(json.dumps({"op": "zero_checkpoint", "metric": "checkpoint GB/s (host)",
+                      "save_gbs": total / sum(saves) / 1e9,
+                      "load_reshard_gbs": 12 * int(L.length) / load_s / 1e9,
+                      "config": {"workload": f"{args.config}: {w.title}", "nd_saved": nd,
+                                 "nd_loaded": nd + 1, "bytes_saved": total}}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__,
                                  formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -439,8 +550,12 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--op", choices=["step", "gather", "checkpoint"], default="step",
+                    help="step (the benchmark line) or a measurement of another entry point")
     ap.add_argument("--config", default="c4", choices=["c1", "c2", "c3", "c4"])
     ap.add_argument("--rank", type=int, default=0, help="first data-parallel rank to run")
+    ap.add_argument("--row-pad", type=int, default=0,
+                    help="extra elements (multiple of 8) between contribution rows")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--e2e-buckets", type=int, default=16,
                     help="transfer buckets of the host-fed e2e step")
@@ -451,8 +566,14 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
+    if args.row_pad % 8:
+        ap.error("--row-pad must be a multiple of 8 elements")
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "gather":
+        run_gather(args)
+    elif args.op == "checkpoint":
+        run_checkpoint(args)
     else:
         run_gpu(args)
 

@@ -20,6 +20,10 @@ namespace {
 #ifndef ZERO_RANK_UNROLL
 #define ZERO_RANK_UNROLL 8
 #endif
+// L2 prefetch size hint of the ring's cp.async copies (256, 128 or 0 = none).
+#ifndef ZERO_CP_ASYNC_L2_HINT
+#define ZERO_CP_ASYNC_L2_HINT 256
+#endif
 constexpr int kRankUnroll = ZERO_RANK_UNROLL;   // rank rows loaded back to back per thread
 
 // ---------------------------------------------------------------------------
@@ -49,8 +53,15 @@ __device__ __forceinline__ uint16_t ld_grad2(const uint16_t* p)
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem)
 {
     const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+#if ZERO_CP_ASYNC_L2_HINT == 256
     asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" ::"r"(sa), "l"(gmem)
                  : "memory");
+#elif ZERO_CP_ASYNC_L2_HINT == 128
+    asm volatile("cp.async.cg.shared.global.L2::128B [%0], [%1], 16;" ::"r"(sa), "l"(gmem)
+                 : "memory");
+#else
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+#endif
 }
 
 __device__ __forceinline__ void cp_async_commit()

@@ -9,9 +9,10 @@
 // same copy, on 4-byte elements, moves fp32 optimizer state between shard
 // layouts (resharding to another Nd).
 //
-// Each segment is one launch.  Its body is copied in 16-byte destination
-// chunks: when source and destination differ in 16-byte phase by DELTA bytes,
-// each chunk is assembled from two aligned 16-byte source loads with funnel
+// Up to 48 segments go into one launch (the plans ride in the kernel
+// parameters).  A segment's body is copied in 16-byte destination chunks:
+// when source and destination differ in 16-byte phase by DELTA bytes, each
+// chunk is assembled from two aligned 16-byte source loads with funnel
 // shifts, so every global access stays a full 16-byte vector.  Elements at
 // the two ends whose aligned source chunks would extend past the segment are
 // copied one 2-byte unit at a time, so nothing outside the segment is read.
@@ -26,14 +27,28 @@ namespace {
 constexpr int kCopyThreads = 256;
 constexpr int kCopyCtasPerSm = 8;
 
+// One contiguous copy of a segment, planned on the host (see plan_segment).
 struct SegCopy {
     const uint16_t* src;   // segment start (2-byte aligned)
     uint16_t* dst;         // destination start (2-byte aligned)
+    const uint4* a;        // aligned source chunk feeding body chunk 0
+    uint4* d;              // body chunk 0 (16-byte aligned)
+    uint32_t delta;        // source-destination phase difference in bytes (even, < 16)
+    uint32_t pad;
     uint64_t units;        // 2-byte units in the segment
-    const uint4* a;        // aligned source chunk feeding destination chunk k0
-    uint4* d;              // destination chunk k0 (16-byte aligned)
     uint64_t nchunks;      // 16-byte destination chunks in the body
     uint64_t body_lo;      // first unit of the body
+};
+
+// Up to kMaxSegs segments per launch, passed by value in the kernel
+// parameters; chunk_end / edge_end are inclusive prefix sums over segments.
+constexpr int kMaxSegs = 48;
+
+struct SegBatch {
+    int nseg;
+    SegCopy seg[kMaxSegs];
+    uint64_t chunk_end[kMaxSegs];
+    uint64_t edge_end[kMaxSegs];
 };
 
 // Bytes [DELTA, DELTA + 16) of the 32-byte window x:y (DELTA even, 0..14).
@@ -50,22 +65,56 @@ __device__ __forceinline__ uint4 window16(const uint4& x, const uint4& y)
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-template <int DELTA>
-__global__ void __launch_bounds__(kCopyThreads, kCopyCtasPerSm) k_gather_segment(const SegCopy c)
+__device__ __forceinline__ uint4 chunk_at(const SegCopy& c, uint64_t k)
+{
+    const uint4 x = __ldcs(c.a + k);
+    if (c.delta == 0)
+        return x;
+    const uint4 y = __ldcs(c.a + k + 1);
+    switch (c.delta) {      // uniform within a segment
+    case 2: return window16<2>(x, y);
+    case 4: return window16<4>(x, y);
+    case 6: return window16<6>(x, y);
+    case 8: return window16<8>(x, y);
+    case 10: return window16<10>(x, y);
+    case 12: return window16<12>(x, y);
+    default: return window16<14>(x, y);
+    }
+}
+
+// First segment whose inclusive prefix end exceeds i (segments are few).
+__device__ __forceinline__ int find_seg(const uint64_t* ends, int nseg, uint64_t i)
+{
+    int lo = 0, hi = nseg - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (ends[mid] > i)
+            hi = mid;
+        else
+            lo = mid + 1;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(kCopyThreads, kCopyCtasPerSm) k_gather_segments(const SegBatch b)
 {
     const uint64_t tid = (uint64_t)blockIdx.x * kCopyThreads + threadIdx.x;
     const uint64_t nthr = (uint64_t)gridDim.x * kCopyThreads;
-    // edges: units before the body and after it
-    const uint64_t body_hi = c.body_lo + 8 * c.nchunks;
-    const uint64_t edge = c.body_lo + (c.units - body_hi);
-    for (uint64_t t = tid; t < edge; t += nthr) {
-        const uint64_t u = t < c.body_lo ? t : body_hi + (t - c.body_lo);
+    const uint64_t nedge = b.edge_end[b.nseg - 1];
+    for (uint64_t t = tid; t < nedge; t += nthr) {       // edge units, 2 bytes each
+        const int s = find_seg(b.edge_end, b.nseg, t);
+        const SegCopy& c = b.seg[s];
+        const uint64_t local = t - (s ? b.edge_end[s - 1] : 0);
+        const uint64_t body_hi = c.body_lo + 8 * c.nchunks;
+        const uint64_t u = local < c.body_lo ? local : body_hi + (local - c.body_lo);
         c.dst[u] = c.src[u];
     }
-    for (uint64_t k = tid; k < c.nchunks; k += nthr) {
-        const uint4 x = __ldcs(c.a + k);
-        const uint4 y = DELTA ? __ldcs(c.a + k + 1) : x;
-        __stcs(c.d + k, window16<DELTA>(x, y));
+    const uint64_t nchunk = b.chunk_end[b.nseg - 1];
+    for (uint64_t t = tid; t < nchunk; t += nthr) {      // 16-byte body chunks
+        const int s = find_seg(b.chunk_end, b.nseg, t);
+        const SegCopy& c = b.seg[s];
+        const uint64_t k = t - (s ? b.chunk_end[s - 1] : 0);
+        __stcs(c.d + k, chunk_at(c, k));
     }
 }
 
@@ -79,17 +128,17 @@ int sm_count_gather()
     return sms;
 }
 
-// Plans and launches the copy of `units` 2-byte units from src to dst.
-void copy_segment(const uint16_t* src, uint16_t* dst, uint64_t units, cudaStream_t s)
+// Plans the copy of `units` 2-byte units from src to dst: a 16-byte chunk
+// body whose source chunks lie inside the segment, and edge units.
+SegCopy plan_segment(const uint16_t* src, uint16_t* dst, uint64_t units)
 {
-    SegCopy c{src, dst, units, nullptr, nullptr, 0, units};
+    SegCopy c{src, dst, nullptr, nullptr, 0, 0, units, 0, units};
     const uintptr_t S = (uintptr_t)src, D = (uintptr_t)dst;
     const uint64_t nbytes = 2 * units;
     const uint64_t dpre = (16 - (D & 15)) & 15;          // bytes before dst is aligned
-    int delta = 0;
     if (nbytes >= 64 + dpre) {
         const uintptr_t S1 = S + dpre;                    // source byte of dst chunk 0
-        delta = (int)(S1 & 15);
+        const uint32_t delta = (uint32_t)(S1 & 15);
         const uintptr_t A = S1 - delta;                   // aligned source chunk of dst chunk 0
         // dst chunk k reads source chunks A+16k and (delta > 0) A+16(k+1); both
         // must lie inside [S, S + nbytes).
@@ -101,24 +150,33 @@ void copy_segment(const uint16_t* src, uint16_t* dst, uint64_t units, cudaStream
         if (k1 > k0) {
             c.a = reinterpret_cast<const uint4*>(A) + k0;
             c.d = reinterpret_cast<uint4*>(D + dpre) + k0;
+            c.delta = delta;
             c.nchunks = k1 - k0;
             c.body_lo = (dpre + 16 * k0) / 2;
         }
     }
-    const uint64_t work = c.nchunks > 64 ? c.nchunks : 64;
+    return c;
+}
+
+zero_status_t launch_batch(SegBatch& b, cudaStream_t s)
+{
+    if (b.nseg == 0)
+        return ZERO_OK;
+    uint64_t chunks = 0, edges = 0;
+    for (int i = 0; i < b.nseg; ++i) {
+        const SegCopy& c = b.seg[i];
+        chunks += c.nchunks;
+        edges += c.units - 8 * c.nchunks;
+        b.chunk_end[i] = chunks;
+        b.edge_end[i] = edges;
+    }
+    const uint64_t work = chunks > edges ? chunks : edges;
     uint64_t grid = (work + kCopyThreads - 1) / kCopyThreads;
     const uint64_t cap = (uint64_t)sm_count_gather() * kCopyCtasPerSm;
-    grid = grid < cap ? grid : cap;
-    switch (delta) {
-    case 0: k_gather_segment<0><<<(unsigned)grid, kCopyThreads, 0, s>>>(c); break;
-    case 2: k_gather_segment<2><<<(unsigned)grid, kCopyThreads, 0, s>>>(c); break;
-    case 4: k_gather_segment<4><<<(unsigned)grid, kCopyThreads, 0, s>>>(c); break;
-    case 6: k_gather_segment<6><<<(unsigned)grid, kCopyThreads, 0, s>>>(c); break;
-    case 8: k_gather_segment<8><<<(unsigned)grid, kCopyThreads, 0, s>>>(c); break;
-    case 10: k_gather_segment<10><<<(unsigned)grid, kCopyThreads, 0, s>>>(c); break;
-    case 12: k_gather_segment<12><<<(unsigned)grid, kCopyThreads, 0, s>>>(c); break;
-    default: k_gather_segment<14><<<(unsigned)grid, kCopyThreads, 0, s>>>(c); break;
-    }
+    grid = grid < cap ? (grid ? grid : 1) : cap;
+    k_gather_segments<<<(unsigned)grid, kCopyThreads, 0, s>>>(b);
+    b.nseg = 0;
+    return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ERR_CUDA;
 }
 
 }  // namespace
@@ -143,6 +201,8 @@ extern "C" zero_status_t zero_gather_range(const void* shards, uint64_t pitch, u
         return ZERO_ERR_INVALID_ARG;   // out overlaps the shards
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const uint64_t units_per_elem = elem_bytes / 2;
+    zero::SegBatch batch;
+    batch.nseg = 0;
     uint64_t done = 0;
     while (done < len) {
         const uint64_t flat = begin + done;
@@ -151,10 +211,12 @@ extern "C" zero_status_t zero_gather_range(const void* shards, uint64_t pitch, u
         const uint16_t* src = static_cast<const uint16_t*>(shards) +
                               (r * pitch + local) * units_per_elem;
         uint16_t* dst = static_cast<uint16_t*>(out) + done * units_per_elem;
-        zero::copy_segment(src, dst, take * units_per_elem, st);
-        if (cudaGetLastError() != cudaSuccess)
+        batch.seg[batch.nseg++] = zero::plan_segment(src, dst, take * units_per_elem);
+        if (batch.nseg == zero::kMaxSegs && zero::launch_batch(batch, st) != ZERO_OK)
             return ZERO_ERR_CUDA;
         done += take;
     }
+    if (zero::launch_batch(batch, st) != ZERO_OK)
+        return ZERO_ERR_CUDA;
     return ZERO_OK;
 }

@@ -62,14 +62,16 @@ def data_parallel_rank(first_rank: int, process_rank: int, nd: int) -> int:
 
 
 class RankState:
-    """Double-buffered fp32 state (master, m, v) of one rank's shard."""
+    """Double- (or, pipelined, triple-) buffered fp32 state (master, m, v) of
+    one rank's shard."""
 
-    def __init__(self, layout: _abi.Layout, device):
+    def __init__(self, layout: _abi.Layout, device, nbuf: int = 2):
         self.layout = layout
         # One [3, pitch] block per buffer; pitch is a multiple of 8 elements,
         # so every row starts 32-byte aligned.
         pitch = max(int(layout.row_pitch), 8)
-        self.bufs = [torch.zeros(3, pitch, dtype=torch.float32, device=device) for _ in range(2)]
+        self.bufs = [torch.zeros(3, pitch, dtype=torch.float32, device=device)
+                     for _ in range(nbuf)]
         self.states = [_abi.state(b[0], b[1], b[2]) for b in self.bufs]
         self.cur = 0
 
@@ -280,3 +282,115 @@ class DataParallelStep:
         skipped = self.decide()
         self.commit(skipped)
         return skipped
+
+
+class PipelinedStep(DataParallelStep):
+    """DataParallelStep whose host never stalls the GPU between steps.
+
+    Step k+1 is launched on step k's output before the host has read step
+    k's nonfinite flag (speculating that k commits); the host then waits only
+    for step k's flag.  State and parameters are triple-buffered (committed,
+    step k's output, step k+1's output) and the flag alternates between two
+    words.  If step k turns out to be skipped, the committed state stays, the
+    speculative step k+1 is discarded and run again from the committed state,
+    so every step's result and the skip rule are exactly those of
+    DataParallelStep.  Gradient buffers must stay unchanged until the step that
+    reads them has been decided.
+
+    Use: ``launch(grads)`` for each step, then ``finish()`` once; both return
+    the decided steps' skip flags in order.
+    """
+
+    def __init__(self, *args, **kwargs):
+        kwargs.setdefault("gathered", "slot")
+        super().__init__(*args, **kwargs)
+        for r in self.ranks:
+            old = self.state[r]
+            self.state[r] = RankState(self.layouts[r], self.device, nbuf=3)
+            self.state[r].bufs[0].copy_(old.bufs[old.cur])
+            self.state[r].states = [_abi.state(b[0], b[1], b[2]) for b in self.state[r].bufs]
+        if self.gathered_mode == "full":
+            self.gathered.append(torch.zeros_like(self.gathered[0]))
+        elif self.gathered_mode == "pitched":
+            self.gathered.append(torch.zeros_like(self.gathered[0]))
+        else:
+            self.gathered.append({r: torch.zeros_like(t) for r, t in self.gathered[0].items()})
+        self.gathered[0], self.gathered[self.gcur] = self.gathered[self.gcur], self.gathered[0]
+        self.gcur = 0
+        self.flags = torch.zeros(2, dtype=torch.int32, device=self.device)
+        self.flags_host = torch.zeros(2, dtype=torch.int32, pin_memory=True)
+        self.pending = []          # launched, undecided: (buf, t, flag slot, event, grads)
+        self.launched = 0
+
+    def _free_buf(self, exclude):
+        return next(i for i in range(3) if i not in exclude)
+
+    def _launch_one(self, grads, in_buf, out_buf, t):
+        slot = self.launched % 2
+        self.launched += 1
+        self.h.step = t
+        for r in self.ranks:
+            st = self.state[r]
+            gbuf, goff = self._gathered_target(r, out_buf)
+            _abi.zero_step_shard(grads[r], self.layouts[r], st.states[in_buf],
+                                 st.states[out_buf], gbuf, goff, self.bucket, self.loss_scale,
+                                 self.h, self.flags[slot:slot + 1], self.stream)
+        with torch.cuda.stream(self.stream):
+            self.flags_host[slot:slot + 1].copy_(self.flags[slot:slot + 1], non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record(self.stream)
+        self.pending.append((out_buf, t, slot, ev, grads))
+
+    def launch(self, grads: dict) -> list:
+        """Launch one step (speculating that every undecided step commits);
+        decides and returns the steps that can be decided without stalling."""
+        if self.pending:
+            in_buf, t_in = self.pending[-1][0], self.pending[-1][1]
+        else:
+            in_buf, t_in = self.gcur, self.t
+        out_buf = self._free_buf({self.gcur, in_buf} | {p[0] for p in self.pending})
+        self._launch_one(grads, in_buf, out_buf, t_in + 1)
+        decided = []
+        while len(self.pending) > 1:
+            decided.append(self._decide_oldest())
+        return decided
+
+    def _decide_oldest(self) -> bool:
+        out_buf, t, slot, ev, grads = self.pending.pop(0)
+        ev.synchronize()
+        bad = int(self.flags_host[slot]) != 0
+        skipped = global_skip(bad, self.pg, self.device)
+        self.skipped_steps.append(skipped)
+        if not skipped:
+            for r in self.ranks:
+                self.state[r].cur = out_buf
+            self.gcur = out_buf
+            self.t = t
+            return False
+        # skipped: clear its flag word, discard the speculative steps that
+        # built on it and run them again from the committed state
+        with torch.cuda.stream(self.stream):
+            self.flags[slot:slot + 1].zero_()
+        redo = [p[4] for p in self.pending]
+        for p in self.pending:
+            p[3].synchronize()
+            with torch.cuda.stream(self.stream):
+                self.flags[p[2]:p[2] + 1].zero_()
+        self.pending = []
+        for g in redo:
+            in_buf, t_in = (self.pending[-1][0], self.pending[-1][1]) if self.pending else \
+                (self.gcur, self.t)
+            out = self._free_buf({self.gcur, in_buf} | {p[0] for p in self.pending})
+            self._launch_one(g, in_buf, out, t_in + 1)
+        return True
+
+    def finish(self) -> list:
+        """Decide every launched step."""
+        decided = []
+        while self.pending:
+            decided.append(self._decide_oldest())
+        return decided
+
+    def step(self, grads: dict) -> bool:
+        self.launch(grads)
+        return self.finish()[-1]
