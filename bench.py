@@ -83,6 +83,21 @@ def recorded_traffic(workload: str):
     return float(kv["dram_bytes_per_param"])
 
 
+def workload(args):
+    """The named workload, with optional --psi / --grad-dtype overrides (for
+    experiments; the benchmark line uses the named workload as it is)."""
+    import dataclasses
+
+    import synth
+    w = synth.WORKLOADS[args.config]
+    if args.psi:
+        w = dataclasses.replace(w, psi=args.psi, plant=None)
+    if args.grad_dtype and args.grad_dtype != w.grad_dtype:
+        w = dataclasses.replace(w, grad_dtype=args.grad_dtype,
+                                loss_scale=1024.0 if args.grad_dtype == "f16" else 1.0)
+    return w
+
+
 def smi_index(local: int) -> str:
     """nvidia-smi's id of this process's device (honours CUDA_VISIBLE_DEVICES)."""
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
@@ -169,7 +184,7 @@ def run_gpu(args) -> None:
         dist.barrier()
         build.build()          # every rank loads the library (already built)
 
-    w = synth.WORKLOADS[args.config]
+    w = workload(args)
     dp_rank = data_parallel_rank(args.rank, rank, w.nd)
     group = dist.group.WORLD if world > 1 else None
     stream = torch.cuda.Stream(dev)
@@ -332,7 +347,8 @@ def run_gpu(args) -> None:
     peak = peaks.get("hbm_gbs")
     peak_src = "measured" if peak else "fallback"
     peak = peak or 6800.0
-    traffic_pp = recorded_traffic(args.config)
+    traffic_pp = None if (args.psi or args.grad_dtype or args.row_pad) else \
+        recorded_traffic(args.config)
     line = {
         "metric": METRIC,
         "value": world * n / (ms_per_step * 1e-3),
@@ -346,7 +362,9 @@ def run_gpu(args) -> None:
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded counter-based generator; no dataset or weights)",
-        "config": {"workload": f"{args.config}: {w.title}", "psi": w.psi, "nd": w.nd,
+        "config": {"workload": f"{args.config}: {w.title}" + (
+                       " (overridden)" if (args.psi or args.grad_dtype) else ""),
+                   "psi": w.psi, "nd": w.nd,
                    "rank": dp_rank, "shard_params": n, "grad_dtype": w.grad_dtype,
                    "bucket": w.bucket, "loss_scale": w.loss_scale,
                    "row_stride_elems": row_stride,
@@ -381,14 +399,15 @@ def run_gpu(args) -> None:
 # CPU oracle timing (the baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def _oracle_sample(w, dp_rank: int, n_sample: int):
+def _oracle_sample(w, dp_rank: int, n_sample: int, first: int = 0):
     import numpy as np
     import torch
 
     import synth
     s, begin, n = synth.shard_of(w.psi, w.nd, dp_rank)
-    n_sample = min(n_sample, n)
-    idx = torch.arange(begin, begin + n_sample, dtype=torch.int64)
+    first = min(first, n)
+    n_sample = min(n_sample, n - first)
+    idx = torch.arange(begin + first, begin + first + n_sample, dtype=torch.int64)
     rows = np.stack([synth.grad_values(w, 0, j, idx).view(torch.int16).numpy().view(np.uint16)
                      for j in range(w.nd)])
     st = [synth.state_values(w, k, idx).numpy() for k in ("master", "m", "v")]
@@ -402,59 +421,87 @@ def _oracle_step(orc, w, rows, st, n_sample, t):
                          w.bucket, w.loss_scale, w.hparams, t, st[0], st[1], st[2], params, 0)
 
 
-def cpu_baseline(w, dp_rank: int, seconds: float) -> dict:
-    """The oracle as it stands (single-threaded C) on a contiguous sample of
-    this rank's shard, repeated for about ``seconds`` of CPU time."""
+def _oracle_worker(args):
+    """One host core: the oracle, as it stands, on its own contiguous slice of
+    the shard, repeated for `seconds` (or `reps` times)."""
+    key, dp_rank, n_sample, first, seconds, reps = args
+    import torch
+    torch.set_num_threads(1)
+    sys.path.insert(0, ROOT)
+    import oracle
+    import synth
+    w = synth.WORKLOADS[key]
+    rows, st, n = _oracle_sample(w, dp_rank, n_sample, first)
+    _oracle_step(oracle, w, rows, st, n, 1)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_step(oracle, w, rows, st, n, 1 + done)
+        done += 1
+        el = time.perf_counter() - t0
+        if (reps and done >= reps) or (not reps and el >= seconds):
+            return done * n, el
+
+
+def _cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _oracle_pool(key: str, dp_rank: int, n_per_core: int, seconds: float = 0.0,
+                 reps: int = 0):
+    """Run the oracle on every host core (spawned processes, one slice each)."""
+    import multiprocessing as mp
     import oracle
     oracle.build()
-    n_sample = 1 << 18
-    rows, st, n_sample = _oracle_sample(w, dp_rank, n_sample)
-    _oracle_step(oracle, w, rows, st, n_sample, 1)   # warm
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        _oracle_step(oracle, w, rows, st, n_sample, 1 + reps)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    rate = reps * n_sample / el
-    return {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{reps} x {n_sample} contiguous params of rank {dp_rank}'s shard "
-                      f"({w.nd} contributions each), single-threaded C, {el:.1f} s",
+    cores = _cores()
+    jobs = [(key, dp_rank, n_per_core, i * n_per_core, seconds, reps) for i in range(cores)]
+    with mp.get_context("spawn").Pool(cores) as pool:
+        res = pool.map(_oracle_worker, jobs)
+    params = sum(r[0] for r in res)
+    elapsed = max(r[1] for r in res)
+    return params / elapsed, cores, params, elapsed
+
+
+def cpu_baseline(w, dp_rank: int, seconds: float) -> dict:
+    """The oracle as it stands (plain C, one process per host core) on
+    contiguous slices of this rank's shard, each core repeating its slice for
+    about ``seconds``."""
+    n_per_core = 1 << 16
+    rate, cores, params, el = _oracle_pool(w.key, dp_rank, n_per_core, seconds=seconds)
+    return {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{cores} processes x {n_per_core} contiguous params of rank {dp_rank}'s "
+                      f"shard ({w.nd} contributions each), {params} param-steps in {el:.1f} s",
             "gbs": rate * w.bytes_per_param / 1e9}
 
 
 def run_reference(args) -> None:
+    """The reference arm: the CPU oracle, as it stands, on the host cores; each
+    step is every core running the oracle once on its own slice of the bench
+    workload's shard."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     import synth
-    import oracle
-    oracle.build()
     w = synth.WORKLOADS[args.config]
-    n_sample = args.ref_sample
-    rows, st, n_sample = _oracle_sample(w, args.rank, n_sample)
-    for k in range(args.warmup):
-        _oracle_step(oracle, w, rows, st, n_sample, 1 + k)
-    t0 = time.perf_counter()
-    for k in range(args.steps):
-        _oracle_step(oracle, w, rows, st, n_sample, 1 + k)
-    el = time.perf_counter() - t0
+    n_per_core = args.ref_sample
+    _oracle_pool(w.key, args.rank, n_per_core, reps=args.warmup)
+    rate, cores, params, el = _oracle_pool(w.key, args.rank, n_per_core, reps=args.steps)
     ms = el * 1e3 / args.steps
-    value = n_sample / (ms * 1e-3)
-    sample = (f"each step: {n_sample} contiguous params of rank {args.rank}'s shard "
-              f"({w.nd} contributions each), single-threaded C oracle")
+    sample = (f"each step: {cores} processes x {n_per_core} contiguous params of rank "
+              f"{args.rank}'s shard ({w.nd} contributions each), plain C oracle")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded counter-based generator)",
         "config": {"workload": f"{args.config}: {w.title}", "psi": w.psi, "nd": w.nd,
-                   "rank": args.rank, "sample_params_per_step": n_sample},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "rank": args.rank, "sample_params_per_step": params // args.steps},
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
-        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -552,8 +599,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--op", choices=["step", "gather", "checkpoint"], default="step",
                     help="step (the benchmark line) or a measurement of another entry point")
-    ap.add_argument("--config", default="c4", choices=["c1", "c2", "c3", "c4"])
+    ap.add_argument("--config", default="c4", choices=["c0", "c1", "c2", "c3", "c4"])
     ap.add_argument("--rank", type=int, default=0, help="first data-parallel rank to run")
+    ap.add_argument("--psi", type=int, default=0, help="override the parameter count")
+    ap.add_argument("--grad-dtype", choices=["f16", "bf16"], default=None,
+                    help="override the gradient dtype")
     ap.add_argument("--row-pad", type=int, default=0,
                     help="extra elements (multiple of 8) between contribution rows")
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -561,8 +611,8 @@ def main():
                     help="transfer buckets of the host-fed e2e step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-sample", type=int, default=1 << 16,
-                    help="params per step of the reference (oracle) arm")
+    ap.add_argument("--ref-sample", type=int, default=1 << 13,
+                    help="params per core per step of the reference (oracle) arm")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

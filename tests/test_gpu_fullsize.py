@@ -37,11 +37,12 @@ def free_memory():
     torch.cuda.empty_cache()
 
 
-def _sampled_state(dps, idx):
+def _sampled_state(dps, idx, with_params=True):
     """Current state and gathered params of the group at flat indices idx."""
     s = int(dps.layouts[dps.ranks[0]].shard_elems)
     out = [np.empty(idx.size, np.float32) for _ in range(3)]
-    params = u16(dps.gathered_view()[torch.from_numpy(idx).to(dps.device)])
+    params = u16(dps.gathered_view()[torch.from_numpy(idx).to(dps.device)]) if with_params \
+        else None
     for r in dps.ranks:
         sel = (idx // s) == r
         if not sel.any():
@@ -63,11 +64,29 @@ def _check(dps, idx, entry, what):
     assert dps.t == t, what
 
 
-@pytest.mark.parametrize("key,rank", [("c1", 0), ("c1", 5), ("c3", 0), ("c3", 1), ("c4", 0),
-                                      ("c4", 63)])
-def test_shard_view_sampled(key, rank):
+def _bench_driver(w, rank):
+    """The driver configuration bench.py times: PipelinedStep, slot buffers."""
+    from zero_sharded_optimizer_02_gb300.step import PipelinedStep
+    dps = PipelinedStep(w.psi, w.nd, [rank], w.grad_dtype, w.hparams, w.loss_scale, w.bucket,
+                        "cuda", gathered="slot")
+    st = dps.state[rank]
+    for row, which in zip(st.bufs[st.cur], ("master", "m", "v")):
+        synth.fill_shard_state(w, rank, which, row)
+    return dps
+
+
+def _slot_params(dps, rank, idx):
+    s = int(dps.layouts[rank].shard_elems)
+    local = torch.from_numpy(idx - rank * s).to(dps.device)
+    return u16(dps.gathered_view(rank)[local])
+
+
+@pytest.mark.parametrize("key,rank,bench_cfg", [("c1", 0, False), ("c1", 5, False),
+                                                ("c3", 0, False), ("c3", 1, False),
+                                                ("c4", 0, True), ("c4", 63, False)])
+def test_shard_view_sampled(key, rank, bench_cfg):
     w = synth.WORKLOADS[key]
-    dps = make_group(w, ranks=[rank])
+    dps = _bench_driver(w, rank) if bench_cfg else make_group(w, ranks=[rank])
     idx = sample_indices(w.psi, w.nd, [rank], 2048, seed=rank + 17)
     _, hist = oracle_trajectory(w, idx, w.steps)
     buf = None
@@ -76,7 +95,16 @@ def test_shard_view_sampled(key, rank):
             buf, desc = shard_rows(w, dps, rank, k, buf)
         assert not dps.step(desc)
         if k in (0, w.steps - 1) or w.fresh_grads:
-            _check(dps, idx, hist[k], f"{key} rank {rank} step {k}")
+            if bench_cfg:   # slot buffers: the parameters sit at their local index
+                p, m, v, params, t = hist[k]
+                (gp, gm, gv), _ = _sampled_state(dps, idx, with_params=False)
+                assert_state_close(gp, p, 1e-12, f"{key} master step {k}")
+                assert_state_close(gm, m, 1e-20, f"{key} m step {k}")
+                assert_state_close(gv, v, 1e-20, f"{key} v step {k}")
+                assert_params_close(_slot_params(dps, rank, idx), params, f"{key} params")
+                assert dps.t == t
+            else:
+                _check(dps, idx, hist[k], f"{key} rank {rank} step {k}")
     L = dps.layouts[rank]
     n = int(L.length)
     for b in dps.state[rank].bufs:

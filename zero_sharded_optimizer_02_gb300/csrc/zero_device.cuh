@@ -325,6 +325,31 @@ __device__ __forceinline__ bool fused_epilogue(const FusedArgs& a, uint64_t e, c
     return bad;
 }
 
+// Epilogue with the state already loaded (p, m, v of the 8 elements at e,
+// read with ld8_cs before the fold): scale, AdamW, 256-bit streaming stores,
+// cast into the gathered slot.  Returns "any sum nonfinite".
+template <int DT, int W>
+__device__ __forceinline__ bool fused_epilogue_loaded(const FusedArgs& a, uint64_t e,
+                                                      const float (&s)[8], float (&p)[8],
+                                                      float (&m)[8], float (&v)[8])
+{
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        bad |= nonfinite(s[i]);
+        adamw1(a.k, __fmul_rn(s[i], a.k.inv), p[i], m[i], v[i]);
+    }
+    st8_cs(a.p_out + e, p);
+    st8_cs(a.m_out + e, m);
+    st8_cs(a.v_out + e, v);
+    uint32_t out16[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        out16[i] = (uint32_t)narrow1<DT>(p[2 * i]) | ((uint32_t)narrow1<DT>(p[2 * i + 1]) << 16);
+    store8<W>(a.gath + e, out16);
+    return bad;
+}
+
 // True if every state pointer of the fused step is 32-byte aligned (the
 // vectors of every window then are too: they start at multiples of 8
 // elements).

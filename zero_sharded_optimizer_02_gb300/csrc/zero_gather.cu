@@ -10,7 +10,7 @@
 // layouts (resharding to another Nd).
 //
 // Up to 48 segments go into one launch (the plans ride in the kernel
-// parameters).  A segment's body is copied in 16-byte destination chunks:
+// parameters); each CTA copies a contiguous run of one segment.  A segment's body is copied in 16-byte destination chunks:
 // when source and destination differ in 16-byte phase by DELTA bytes, each
 // chunk is assembled from two aligned 16-byte source loads with funnel
 // shifts, so every global access stays a full 16-byte vector.  Elements at
@@ -25,7 +25,6 @@ namespace zero {
 namespace {
 
 constexpr int kCopyThreads = 256;
-constexpr int kCopyCtasPerSm = 8;
 
 // One contiguous copy of a segment, planned on the host (see plan_segment).
 struct SegCopy {
@@ -41,14 +40,17 @@ struct SegCopy {
 };
 
 // Up to kMaxSegs segments per launch, passed by value in the kernel
-// parameters; chunk_end / edge_end are inclusive prefix sums over segments.
+// parameters.  Every CTA copies one contiguous run of kChunksPerCta body
+// chunks of one segment (block_end is the inclusive prefix sum of the CTAs
+// each segment gets); a segment's first CTA also copies its edge units.
 constexpr int kMaxSegs = 48;
+constexpr int kChunksPerThread = 8;
+constexpr uint64_t kChunksPerCta = (uint64_t)kCopyThreads * kChunksPerThread;
 
 struct SegBatch {
     int nseg;
     SegCopy seg[kMaxSegs];
-    uint64_t chunk_end[kMaxSegs];
-    uint64_t edge_end[kMaxSegs];
+    uint64_t block_end[kMaxSegs];
 };
 
 // Bytes [DELTA, DELTA + 16) of the 32-byte window x:y (DELTA even, 0..14).
@@ -65,67 +67,67 @@ __device__ __forceinline__ uint4 window16(const uint4& x, const uint4& y)
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-__device__ __forceinline__ uint4 chunk_at(const SegCopy& c, uint64_t k)
+// Copies body chunks [k0, k1) of segment c, kChunksPerThread per thread.
+template <int DELTA>
+__device__ __forceinline__ void copy_chunks(const SegCopy& c, uint64_t k0, uint64_t k1)
 {
-    const uint4 x = __ldcs(c.a + k);
-    if (c.delta == 0)
-        return x;
-    const uint4 y = __ldcs(c.a + k + 1);
-    switch (c.delta) {      // uniform within a segment
-    case 2: return window16<2>(x, y);
-    case 4: return window16<4>(x, y);
-    case 6: return window16<6>(x, y);
-    case 8: return window16<8>(x, y);
-    case 10: return window16<10>(x, y);
-    case 12: return window16<12>(x, y);
-    default: return window16<14>(x, y);
+    uint4 x[kChunksPerThread], y[kChunksPerThread];
+#pragma unroll
+    for (int i = 0; i < kChunksPerThread; ++i) {
+        const uint64_t k = k0 + (uint64_t)i * kCopyThreads + threadIdx.x;
+        if (k < k1) {
+            x[i] = __ldcs(c.a + k);
+            y[i] = DELTA ? __ldcs(c.a + k + 1) : x[i];
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kChunksPerThread; ++i) {
+        const uint64_t k = k0 + (uint64_t)i * kCopyThreads + threadIdx.x;
+        if (k < k1)
+            __stcs(c.d + k, window16<DELTA>(x[i], y[i]));
     }
 }
 
-// First segment whose inclusive prefix end exceeds i (segments are few).
-__device__ __forceinline__ int find_seg(const uint64_t* ends, int nseg, uint64_t i)
+__global__ void __launch_bounds__(kCopyThreads) k_gather_segments(const SegBatch b)
 {
-    int lo = 0, hi = nseg - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (ends[mid] > i)
-            hi = mid;
-        else
-            lo = mid + 1;
+    __shared__ int s_seg;
+    if (threadIdx.x == 0) {   // the segment this CTA belongs to
+        int lo = 0, hi = b.nseg - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (b.block_end[mid] > blockIdx.x)
+                hi = mid;
+            else
+                lo = mid + 1;
+        }
+        s_seg = lo;
     }
-    return lo;
-}
-
-__global__ void __launch_bounds__(kCopyThreads, kCopyCtasPerSm) k_gather_segments(const SegBatch b)
-{
-    const uint64_t tid = (uint64_t)blockIdx.x * kCopyThreads + threadIdx.x;
-    const uint64_t nthr = (uint64_t)gridDim.x * kCopyThreads;
-    const uint64_t nedge = b.edge_end[b.nseg - 1];
-    for (uint64_t t = tid; t < nedge; t += nthr) {       // edge units, 2 bytes each
-        const int s = find_seg(b.edge_end, b.nseg, t);
-        const SegCopy& c = b.seg[s];
-        const uint64_t local = t - (s ? b.edge_end[s - 1] : 0);
+    __syncthreads();
+    const int si = s_seg;
+    const SegCopy c = b.seg[si];
+    const uint64_t local_block = blockIdx.x - (si ? b.block_end[si - 1] : 0);
+    if (local_block == 0) {   // edge units of the segment, 2 bytes each
         const uint64_t body_hi = c.body_lo + 8 * c.nchunks;
-        const uint64_t u = local < c.body_lo ? local : body_hi + (local - c.body_lo);
-        c.dst[u] = c.src[u];
+        const uint64_t nedge = c.units - 8 * c.nchunks;
+        for (uint64_t t = threadIdx.x; t < nedge; t += kCopyThreads) {
+            const uint64_t u = t < c.body_lo ? t : body_hi + (t - c.body_lo);
+            c.dst[u] = c.src[u];
+        }
     }
-    const uint64_t nchunk = b.chunk_end[b.nseg - 1];
-    for (uint64_t t = tid; t < nchunk; t += nthr) {      // 16-byte body chunks
-        const int s = find_seg(b.chunk_end, b.nseg, t);
-        const SegCopy& c = b.seg[s];
-        const uint64_t k = t - (s ? b.chunk_end[s - 1] : 0);
-        __stcs(c.d + k, chunk_at(c, k));
+    const uint64_t k0 = local_block * kChunksPerCta;
+    const uint64_t k1 = k0 + kChunksPerCta < c.nchunks ? k0 + kChunksPerCta : c.nchunks;
+    if (k0 >= k1)
+        return;
+    switch (c.delta) {        // uniform within the CTA
+    case 0: copy_chunks<0>(c, k0, k1); break;
+    case 2: copy_chunks<2>(c, k0, k1); break;
+    case 4: copy_chunks<4>(c, k0, k1); break;
+    case 6: copy_chunks<6>(c, k0, k1); break;
+    case 8: copy_chunks<8>(c, k0, k1); break;
+    case 10: copy_chunks<10>(c, k0, k1); break;
+    case 12: copy_chunks<12>(c, k0, k1); break;
+    default: copy_chunks<14>(c, k0, k1); break;
     }
-}
-
-int sm_count_gather()
-{
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        sms <= 0)
-        sms = 1;
-    return sms;
 }
 
 // Plans the copy of `units` 2-byte units from src to dst: a 16-byte chunk
@@ -162,19 +164,15 @@ zero_status_t launch_batch(SegBatch& b, cudaStream_t s)
 {
     if (b.nseg == 0)
         return ZERO_OK;
-    uint64_t chunks = 0, edges = 0;
+    uint64_t blocks = 0;
     for (int i = 0; i < b.nseg; ++i) {
-        const SegCopy& c = b.seg[i];
-        chunks += c.nchunks;
-        edges += c.units - 8 * c.nchunks;
-        b.chunk_end[i] = chunks;
-        b.edge_end[i] = edges;
+        const uint64_t nb = (b.seg[i].nchunks + kChunksPerCta - 1) / kChunksPerCta;
+        blocks += nb ? nb : 1;                 // at least one CTA: the edge units
+        b.block_end[i] = blocks;
     }
-    const uint64_t work = chunks > edges ? chunks : edges;
-    uint64_t grid = (work + kCopyThreads - 1) / kCopyThreads;
-    const uint64_t cap = (uint64_t)sm_count_gather() * kCopyCtasPerSm;
-    grid = grid < cap ? (grid ? grid : 1) : cap;
-    k_gather_segments<<<(unsigned)grid, kCopyThreads, 0, s>>>(b);
+    if (blocks > 0x7FFFFFFFull)
+        return ZERO_ERR_INVALID_ARG;
+    k_gather_segments<<<(unsigned)blocks, kCopyThreads, 0, s>>>(b);
     b.nseg = 0;
     return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ERR_CUDA;
 }
@@ -212,11 +210,15 @@ extern "C" zero_status_t zero_gather_range(const void* shards, uint64_t pitch, u
                               (r * pitch + local) * units_per_elem;
         uint16_t* dst = static_cast<uint16_t*>(out) + done * units_per_elem;
         batch.seg[batch.nseg++] = zero::plan_segment(src, dst, take * units_per_elem);
-        if (batch.nseg == zero::kMaxSegs && zero::launch_batch(batch, st) != ZERO_OK)
-            return ZERO_ERR_CUDA;
+        if (batch.nseg == zero::kMaxSegs) {
+            const zero_status_t r2 = zero::launch_batch(batch, st);
+            if (r2 != ZERO_OK)
+                return r2;
+        }
         done += take;
     }
-    if (zero::launch_batch(batch, st) != ZERO_OK)
-        return ZERO_ERR_CUDA;
+    const zero_status_t r3 = zero::launch_batch(batch, st);
+    if (r3 != ZERO_OK)
+        return r3;
     return ZERO_OK;
 }

@@ -52,6 +52,13 @@ constexpr int kCtasPerSmLight = 8;
 #ifndef ZERO_RING_THREADS
 #define ZERO_RING_THREADS 512
 #endif
+// 1: with 32-byte aligned state, the ring kernel loads a vector's p, m, v when
+// it starts folding the vector, so their latency hides behind the fold.  Off
+// by default: measured about 1% slower on every workload (the ring already
+// keeps the next vector's rows in flight during the epilogue).
+#ifndef ZERO_STATE_PREFETCH
+#define ZERO_STATE_PREFETCH 0
+#endif
 constexpr int kRingRows = ZERO_RING_ROWS;
 constexpr int kRingDepth = ZERO_RING_DEPTH;
 constexpr int kRingThreads = ZERO_RING_THREADS;
@@ -126,9 +133,17 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_step_fused_ring(const Fused
     int slot_c = 0;
     uint32_t gc = 0;
     float acc[8];
+    float sp[8], sm[8], sv[8];     // the current vector's state (prefetch mode)
+    constexpr bool kPrefetch = V8 && ZERO_STATE_PREFETCH;
     for (uint64_t qc = tid; qc < a.sp.nvec;) {
         issue();
         cp_async_wait<kRingDepth - 1>();     // the oldest group has landed
+        if (kPrefetch && gc == 0) {
+            const uint64_t e = a.sp.head + 8 * qc;
+            ld8_cs(a.p_in + e, sp);
+            ld8_cs(a.m_in + e, sm);
+            ld8_cs(a.v_in + e, sv);
+        }
 #pragma unroll
         for (int u = 0; u < kRingRows; ++u) {
             const uint32_t j = gc * kRingRows + u;
@@ -143,7 +158,10 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_step_fused_ring(const Fused
         slot_c = slot_c + 1 == kRingDepth ? 0 : slot_c + 1;
         if (++gc == groups) {
             gc = 0;
-            bad |= fused_epilogue<DT, W, V8>(a, a.sp.head + 8 * qc, acc);
+            if (kPrefetch)
+                bad |= fused_epilogue_loaded<DT, W>(a, a.sp.head + 8 * qc, acc, sp, sm, sv);
+            else
+                bad |= fused_epilogue<DT, W, V8>(a, a.sp.head + 8 * qc, acc);
             qc += nthr;
         }
     }
