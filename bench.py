@@ -223,7 +223,7 @@ def run_gpu(args) -> None:
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    launched0 = pipe.launched
+    launched0 = pipe.kernel_launches
     wall0 = time.time()
     t_start.record(stream)
     decided = []
@@ -236,7 +236,7 @@ def run_gpu(args) -> None:
     if world > 1:
         dist.barrier()
     total_ms = t_start.elapsed_time(t_end)
-    launches = pipe.launched - launched0
+    launches = pipe.kernel_launches - launched0
     skipped = sum(decided)
     assert len(decided) == args.steps
 

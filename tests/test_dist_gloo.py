@@ -112,3 +112,45 @@ def test_two_gloo_ranks():
     import oracle
     oracle.build()
     mp.spawn(_worker, args=(2, _free_port()), nprocs=2, join=True)
+
+
+def _worker_leaves(rank: int, world: int, port: int, result_path: str):
+    import datetime
+    import sys
+    import time
+    sys.path.insert(0, ROOT)
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=3))
+    from zero_sharded_optimizer_02_gb300.step import global_skip
+    g = dist.group.WORLD
+    assert global_skip(False, g) is False          # one step with both ranks
+    if rank == 1:
+        os._exit(0)                                # rank 1 leaves between steps
+    t0 = time.monotonic()
+    try:
+        global_skip(False, g)                      # the survivor's next skip exchange
+        outcome = "completed"
+    except Exception as e:                         # the process group reports the loss
+        outcome = f"error:{type(e).__name__}"
+    with open(result_path, "w") as f:
+        f.write(f"{outcome} {time.monotonic() - t0:.2f}")
+    os._exit(0)
+
+
+def test_a_rank_that_leaves_is_detected(tmp_path):
+    """A rank leaving between steps: the survivor's next skip exchange ends
+    with an error within the process group's timeout instead of hanging."""
+    result = tmp_path / "result.txt"
+    ctx = mp.get_context("spawn")
+    port = _free_port()
+    procs = [ctx.Process(target=_worker_leaves, args=(r, 2, port, str(result))) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=60)
+        assert not p.is_alive(), "a rank hung"
+    outcome, seconds = result.read_text().split()
+    assert outcome.startswith("error:"), outcome
+    assert float(seconds) < 30

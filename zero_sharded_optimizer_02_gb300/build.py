@@ -64,21 +64,24 @@ def _stale(target: str, deps: list[str]) -> bool:
 
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile what is stale and link libzero.so.  Extra nvcc flags (e.g. -D
-    tuning macros of zero_kernels.cu) may be given in ZERO_NVCC_FLAGS; a
-    change of flags forces a rebuild."""
+    tuning macros of zero_kernels.cu) may be given in ZERO_NVCC_FLAGS, and an
+    alternative source directory in ZERO_CSRC_DIR (for experiments kept out
+    of the package); a change of either forces a rebuild."""
     os.makedirs(BUILD, exist_ok=True)
     extra = os.environ.get("ZERO_NVCC_FLAGS", "").split()
+    csrc = os.environ.get("ZERO_CSRC_DIR") or CSRC
     stamp = os.path.join(BUILD, "nvcc_flags.txt")
     old = open(stamp).read() if os.path.exists(stamp) else None
-    if old != " ".join(extra):
+    key = " ".join(extra) + ("" if csrc == CSRC else f" [csrc={csrc}]")
+    if old != key:
         force = True
         with open(stamp, "w") as f:
-            f.write(" ".join(extra))
-    headers = [os.path.join(INCLUDE, "zero.h"), os.path.join(CSRC, "zero_internal.h"),
-               os.path.join(CSRC, "zero_device.cuh")]
+            f.write(key)
+    headers = [os.path.join(INCLUDE, "zero.h"), os.path.join(csrc, "zero_internal.h"),
+               os.path.join(csrc, "zero_device.cuh")]
     objs, procs = [], []
     for src, cmd in SOURCES.items():
-        path = os.path.join(CSRC, src)
+        path = os.path.join(csrc, src)
         obj = os.path.join(BUILD, src + ".o")
         objs.append(obj)
         if force or _stale(obj, [path, *headers, __file__]):

@@ -320,7 +320,8 @@ class PipelinedStep(DataParallelStep):
         self.flags = torch.zeros(2, dtype=torch.int32, device=self.device)
         self.flags_host = torch.zeros(2, dtype=torch.int32, pin_memory=True)
         self.pending = []          # launched, undecided: (buf, t, flag slot, event, grads)
-        self.launched = 0
+        self.launched = 0          # steps launched (speculative re-runs included)
+        self.kernel_launches = 0   # kernels launched (one per rank and bucket)
 
     def _free_buf(self, exclude):
         return next(i for i in range(3) if i not in exclude)
@@ -328,6 +329,9 @@ class PipelinedStep(DataParallelStep):
     def _launch_one(self, grads, in_buf, out_buf, t):
         slot = self.launched % 2
         self.launched += 1
+        for r in self.ranks:
+            n = int(self.layouts[r].length)
+            self.kernel_launches += -(-n // self.bucket) if n else 0
         self.h.step = t
         for r in self.ranks:
             st = self.state[r]
