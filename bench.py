@@ -55,11 +55,16 @@ def kernel_name() -> str:
 
 
 def kernel_source_hash() -> str:
-    """Hash of the sources the fused kernel is compiled from."""
+    """Hash of the code (comments and whitespace removed) of the sources the
+    fused kernel is compiled from: any change of the kernel's code changes it."""
+    import re
     h = hashlib.sha256()
     for path in KERNEL_SRCS:
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
@@ -92,6 +97,8 @@ def workload(args):
     w = synth.WORKLOADS[args.config]
     if args.psi:
         w = dataclasses.replace(w, psi=args.psi, plant=None)
+    if args.bucket:
+        w = dataclasses.replace(w, bucket=args.bucket)
     if args.grad_dtype and args.grad_dtype != w.grad_dtype:
         w = dataclasses.replace(w, grad_dtype=args.grad_dtype,
                                 loss_scale=1024.0 if args.grad_dtype == "f16" else 1.0)
@@ -347,7 +354,7 @@ def run_gpu(args) -> None:
     peak = peaks.get("hbm_gbs")
     peak_src = "measured" if peak else "fallback"
     peak = peak or 6800.0
-    traffic_pp = None if (args.psi or args.grad_dtype or args.row_pad) else \
+    traffic_pp = None if (args.psi or args.grad_dtype or args.row_pad or args.bucket) else \
         recorded_traffic(args.config)
     line = {
         "metric": METRIC,
@@ -363,7 +370,7 @@ def run_gpu(args) -> None:
         "dtype": "f32",
         "data": "synthetic (seeded counter-based generator; no dataset or weights)",
         "config": {"workload": f"{args.config}: {w.title}" + (
-                       " (overridden)" if (args.psi or args.grad_dtype) else ""),
+                       " (overridden)" if (args.psi or args.grad_dtype or args.bucket) else ""),
                    "psi": w.psi, "nd": w.nd,
                    "rank": dp_rank, "shard_params": n, "grad_dtype": w.grad_dtype,
                    "bucket": w.bucket, "loss_scale": w.loss_scale,
@@ -602,6 +609,7 @@ def main():
     ap.add_argument("--config", default="c4", choices=["c0", "c1", "c2", "c3", "c4"])
     ap.add_argument("--rank", type=int, default=0, help="first data-parallel rank to run")
     ap.add_argument("--psi", type=int, default=0, help="override the parameter count")
+    ap.add_argument("--bucket", type=int, default=0, help="override the bucket size")
     ap.add_argument("--grad-dtype", choices=["f16", "bf16"], default=None,
                     help="override the gradient dtype")
     ap.add_argument("--row-pad", type=int, default=0,

@@ -8,8 +8,12 @@
 //
 // The step is elementwise and HBM-bound: at Nd = 64 a parameter costs
 // 2*Nd + 26 bytes (Nd 2-byte gradient reads, 12 B of fp32 state read, 12 B
-// written, 2 B cast out) for ~Nd + 30 flops, so the kernels are 128-bit
-// streaming loops over a grid sized to the SM count, not tensor-core work.
+// written, 2 B cast out) for ~Nd + 30 flops, so it is not tensor-core work.
+// The fused step (k_step_fused_ring) is a persistent grid of one 512-thread
+// CTA per SM that stages the Nd contribution rows through a per-thread
+// cp.async ring in shared memory (16-byte copies, two row groups deep) and
+// moves the fp32 state with 256-bit streaming accesses; the unfused
+// primitives are 128-bit grid-stride loops sized to the SM count.
 //
 // Bit-exactness: every fp32 operation is an explicit correctly rounded
 // intrinsic (__fadd_rn/__fmul_rn/__fdiv_rn/__fsqrt_rn), so no multiply-add is
