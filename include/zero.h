@@ -161,9 +161,13 @@ zero_status_t zero_gather_params_shard(const float* master, uint64_t n, void* ga
 
 /* The fused shard step: reduce (1) + scale + AdamW (2) + cast into the
  * gathered slot (3) in one pass per bucket, with the reduced gradient kept in
- * registers (never materialised).  Shard length and Nd come from L (L->nd must
- * equal g->nd).  The shard is walked in buckets of bucket_elems elements, one
- * launch per bucket; results do not depend on bucket_elems.
+ * registers (never materialised).  The shard length comes from L; the g->nd
+ * contribution rows are folded.  g->nd is normally L->nd (Stage 2: one
+ * contribution per rank) but need not be: under Stage 1 every rank holds the
+ * gradient already all-reduced, so it folds a single row (g->nd = 1) and
+ * passes loss_scale * Nd to keep the 1/Nd averaging.  The shard is walked in
+ * buckets of bucket_elems elements, one launch per bucket; results do not
+ * depend on bucket_elems.
  * The new state goes to `out` and the cast parameters to
  * gathered[gathered_offset_elems + i].  *d_nonfinite |= 1 if any reduced sum
  * is nonfinite; the step is then to be skipped on every shard: with out != in

@@ -117,7 +117,7 @@ def _state(z, base):
     ("null_base", "ZERO_ERR_INVALID_ARG"), ("misaligned_base", "ZERO_ERR_ALIGNMENT"),
     ("odd_row_stride", "ZERO_ERR_ALIGNMENT"), ("odd_offset", "ZERO_ERR_ALIGNMENT"),
     ("bad_dtype", "ZERO_ERR_INVALID_ARG"), ("nd_zero", "ZERO_ERR_INVALID_ARG"),
-    ("nd_mismatch", "ZERO_ERR_INVALID_ARG"), ("misaligned_state", "ZERO_ERR_ALIGNMENT"),
+    ("shard_longer_than_s", "ZERO_ERR_INVALID_ARG"), ("misaligned_state", "ZERO_ERR_ALIGNMENT"),
     ("overlap_state", "ZERO_ERR_INVALID_ARG"), ("bucket_zero", "ZERO_ERR_INVALID_ARG"),
     ("step_zero", "ZERO_ERR_INVALID_ARG"), ("bad_beta", "ZERO_ERR_INVALID_ARG"),
     ("bad_loss_scale", "ZERO_ERR_INVALID_ARG"), ("odd_gathered", "ZERO_ERR_ALIGNMENT"),
@@ -140,8 +140,8 @@ def test_step_shard_rejects(z, case, status):
         g.dtype = 7
     elif case == "nd_zero":
         g.nd = 0
-    elif case == "nd_mismatch":
-        g.nd = 3
+    elif case == "shard_longer_than_s":
+        L.length = L.shard_elems + 1
     elif case == "misaligned_state":
         s_out.m = s_out.m + 4
     elif case == "overlap_state":

@@ -531,8 +531,6 @@ zero_status_t check_step_common(const zero_grads_t* g, const zero_layout_t* L,
     zero_status_t st = check_grads(g, 0, L->length);
     if (st != ZERO_OK)
         return st;
-    if (g->nd != L->nd)
-        return ZERO_ERR_INVALID_ARG;
     if (!aligned(gathered, 2) || !aligned(flag, 4))
         return ZERO_ERR_ALIGNMENT;
     return check_state(in, out, L->length, 16);

@@ -189,7 +189,7 @@ extern "C" zero_status_t zero_step_shard_streamed(
         return ZERO_ERR_INVALID_ARG;
     if (timeout_ns == 0 || timeout_ns > ZERO_MAX_WAIT_NS)
         return ZERO_ERR_INVALID_ARG;   // every device wait must stay bounded
-    if (!g->base || g->nd == 0 || g->nd != L->nd || (g->dtype != ZERO_F16 && g->dtype != ZERO_BF16) ||
+    if (!g->base || g->nd == 0 || (g->dtype != ZERO_F16 && g->dtype != ZERO_BF16) ||
         L->length > L->shard_elems)
         return ZERO_ERR_INVALID_ARG;
     if (!is_aligned(g->base, 16) || (g->row_stride & 7) || (g->offset & 7) ||
