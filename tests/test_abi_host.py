@@ -208,3 +208,12 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(abi, "LIB_PATH", str(tmp_path / "libzero.so"))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         abi.lib()
+
+
+def test_binding_constants_match_header(z):
+    text = open(os.path.join(ROOT, "include", "zero.h")).read()
+    for name in ("ZERO_FUSED_WINDOW_ELEMS", "ZERO_STATIC_CB_ELEMS"):
+        m = re.search(rf"#define {name} (\d+)ull", text)
+        assert m and int(m.group(1)) == getattr(z._abi, name), name
+    assert z._abi.fused_launch_count(117_187_500, 500_000_000) == 7
+    assert z._abi.fused_launch_count(16, 1) == 16 and z._abi.fused_launch_count(0, 8) == 0

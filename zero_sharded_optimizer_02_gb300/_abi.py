@@ -87,6 +87,25 @@ _SIGNATURES = {
                                         vp, vp], i32),
 }
 
+# Longest launch window of the fused step (include/zero.h).
+ZERO_FUSED_WINDOW_ELEMS = 16777216
+
+
+def fused_launch_count(n: int, bucket: int, offset: int = 0) -> int:
+    """Kernel launches zero_step_shard issues for a shard of n elements whose
+    rows start at element `offset` (the same window split as the library)."""
+    count = 0
+    for b0 in range(0, n, bucket):
+        length = min(bucket, n - b0)
+        phase = (offset + b0) & 7
+        w0 = 0
+        while w0 < length:
+            cap = ZERO_FUSED_WINDOW_ELEMS - phase if w0 == 0 else ZERO_FUSED_WINDOW_ELEMS
+            w0 += min(length - w0, cap)
+            count += 1
+    return count
+
+
 # Capacity of the library's own fusion buffer (include/zero.h).
 ZERO_STATIC_CB_ELEMS = 4194304
 ZERO_STATIC_CB_MAX_BUCKET = ZERO_STATIC_CB_ELEMS - 4

@@ -63,6 +63,12 @@ constexpr int kCtasPerSmLight = 8;
 #ifndef ZERO_STATE_PREFETCH
 #define ZERO_STATE_PREFETCH 0
 #endif
+// Longest launch window of the fused step (elements, a multiple of 8).
+#ifndef ZERO_WINDOW_ELEMS
+#define ZERO_WINDOW_ELEMS ZERO_FUSED_WINDOW_ELEMS
+#endif
+constexpr uint64_t kWindow = ZERO_WINDOW_ELEMS;
+static_assert(kWindow % 8 == 0 && kWindow >= 64, "window must be a multiple of 8");
 constexpr int kRingRows = ZERO_RING_ROWS;
 constexpr int kRingDepth = ZERO_RING_DEPTH;
 constexpr int kRingThreads = ZERO_RING_THREADS;
@@ -642,21 +648,30 @@ extern "C" zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layou
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const uint16_t* rows = static_cast<const uint16_t*>(g->base) + g->offset;
     uint16_t* gath = static_cast<uint16_t*>(gathered) + gathered_offset_elems;
+    const float* const sp[6] = {in->master, in->m, in->v, out->master, out->m, out->v};
+    const bool v8 = state_v8_ok(sp);
     for (uint64_t b0 = 0; b0 < n; b0 += bucket_elems) {
         const uint64_t len = n - b0 < bucket_elems ? n - b0 : bucket_elems;
-        FusedArgs a{rows + b0, g->row_stride, g->nd, split_window(g->offset + b0, len),
-                    in->master + b0, in->m + b0, in->v + b0, out->master + b0, out->m + b0,
-                    out->v + b0, gath + b0, k, d_nonfinite};
-        const int width = store_width(gath + b0 + a.sp.head);
-        const float* const sp[6] = {in->master, in->m, in->v, out->master, out->m, out->v};
-        const bool v8 = state_v8_ok(sp);
-        if (g->dtype == ZERO_F16)
-            launch_fused_dt<ZERO_F16>(a, width, v8, s);
-        else
-            launch_fused_dt<ZERO_BF16>(a, width, v8, s);
-        st = launch_status();
-        if (st != ZERO_OK)
-            return st;
+        // launch windows of at most kWindow elements; windows after the first
+        // start at 8-element boundaries of the rows
+        const uint64_t phase = (g->offset + b0) & 7;
+        for (uint64_t w0 = 0; w0 < len;) {
+            const uint64_t cap = w0 == 0 ? kWindow - phase : kWindow;
+            const uint64_t wl = len - w0 < cap ? len - w0 : cap;
+            const uint64_t e0 = b0 + w0;
+            FusedArgs a{rows + e0, g->row_stride, g->nd, split_window(g->offset + e0, wl),
+                        in->master + e0, in->m + e0, in->v + e0, out->master + e0, out->m + e0,
+                        out->v + e0, gath + e0, k, d_nonfinite};
+            const int width = store_width(gath + e0 + a.sp.head);
+            if (g->dtype == ZERO_F16)
+                launch_fused_dt<ZERO_F16>(a, width, v8, s);
+            else
+                launch_fused_dt<ZERO_BF16>(a, width, v8, s);
+            st = launch_status();
+            if (st != ZERO_OK)
+                return st;
+            w0 += wl;
+        }
         if (len < bucket_elems)
             break;
     }

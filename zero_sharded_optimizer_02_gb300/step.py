@@ -179,8 +179,10 @@ class DataParallelStep:
                                              self.loss_scale, self.h, self.cb, self.cb_elems,
                                              self.flag, self.stream)
             n = int(L.length)
-            nb = -(-n // self.bucket) if n else 0
-            launches += nb * (1 if self.fused else 3)
+            if self.fused:
+                launches += _abi.fused_launch_count(n, self.bucket, int(grads[r].offset))
+            else:
+                launches += 3 * (-(-n // self.bucket) if n else 0)
         return launches
 
     def decide(self) -> bool:
@@ -330,8 +332,8 @@ class PipelinedStep(DataParallelStep):
         slot = self.launched % 2
         self.launched += 1
         for r in self.ranks:
-            n = int(self.layouts[r].length)
-            self.kernel_launches += -(-n // self.bucket) if n else 0
+            self.kernel_launches += _abi.fused_launch_count(int(self.layouts[r].length),
+                                                            self.bucket, int(grads[r].offset))
         self.h.step = t
         for r in self.ranks:
             st = self.state[r]
