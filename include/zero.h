@@ -166,10 +166,11 @@ zero_status_t zero_gather_params_shard(const float* master, uint64_t n, void* ga
  * contribution per rank) but need not be: under Stage 1 every rank holds the
  * gradient already all-reduced, so it folds a single row (g->nd = 1) and
  * passes loss_scale * Nd to keep the 1/Nd averaging.  The shard is walked in
- * buckets of bucket_elems elements; each bucket runs as launches of at most
- * ZERO_FUSED_WINDOW_ELEMS elements (kernel boundaries keep every SM at the
- * same place in the rows; single launches much longer than this read several
- * percent more DRAM than the data).  Results depend on neither size.
+ * buckets of bucket_elems elements; each bucket runs as the fewest equal
+ * launches of at most ZERO_FUSED_WINDOW_ELEMS elements (kernel boundaries keep
+ * every SM at the same place in the rows; single launches much longer than
+ * this read several percent more DRAM than the data).  Results depend on
+ * neither size.
  * The new state goes to `out` and the cast parameters to
  * gathered[gathered_offset_elems + i].  *d_nonfinite |= 1 if any reduced sum
  * is nonfinite; the step is then to be skipped on every shard: with out != in
@@ -184,7 +185,7 @@ zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layout_t* L,
                               void* stream);
 
 /* Longest launch window of the fused step, in elements (see zero_step_shard). */
-#define ZERO_FUSED_WINDOW_ELEMS 16777216ull
+#define ZERO_FUSED_WINDOW_ELEMS 25165824ull
 
 /* The same step unfused, through the constant-size fusion buffer: per bucket,
  * zero_reduce_scatter_bucket into cb, then zero_adam_step_shard from cb, then

@@ -215,5 +215,6 @@ def test_binding_constants_match_header(z):
     for name in ("ZERO_FUSED_WINDOW_ELEMS", "ZERO_STATIC_CB_ELEMS"):
         m = re.search(rf"#define {name} (\d+)ull", text)
         assert m and int(m.group(1)) == getattr(z._abi, name), name
-    assert z._abi.fused_launch_count(117_187_500, 500_000_000) == 7
+    assert z._abi.fused_launch_count(117_187_500, 500_000_000) == 5
+    assert z._abi.fused_launch_count(23_437_500, 50_000_000) == 1
     assert z._abi.fused_launch_count(16, 1) == 16 and z._abi.fused_launch_count(0, 8) == 0

@@ -88,7 +88,7 @@ _SIGNATURES = {
 }
 
 # Longest launch window of the fused step (include/zero.h).
-ZERO_FUSED_WINDOW_ELEMS = 16777216
+ZERO_FUSED_WINDOW_ELEMS = 25165824
 
 
 def fused_launch_count(n: int, bucket: int, offset: int = 0) -> int:
@@ -98,10 +98,14 @@ def fused_launch_count(n: int, bucket: int, offset: int = 0) -> int:
     for b0 in range(0, n, bucket):
         length = min(bucket, n - b0)
         phase = (offset + b0) & 7
-        w0 = 0
+        nwin = -(-length // ZERO_FUSED_WINDOW_ELEMS)
+        target = -(-(-(-length // nwin)) // 8) * 8
+        cut, w0 = target - phase, 0
         while w0 < length:
-            cap = ZERO_FUSED_WINDOW_ELEMS - phase if w0 == 0 else ZERO_FUSED_WINDOW_ELEMS
-            w0 += min(length - w0, cap)
+            w1 = min(cut, length)
+            if length - w1 < 64:
+                w1 = length
+            w0, cut = w1, cut + target
             count += 1
     return count
 

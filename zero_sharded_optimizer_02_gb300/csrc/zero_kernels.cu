@@ -63,7 +63,8 @@ constexpr int kCtasPerSmLight = 8;
 #ifndef ZERO_STATE_PREFETCH
 #define ZERO_STATE_PREFETCH 0
 #endif
-// Longest launch window of the fused step (elements, a multiple of 8).
+// Longest launch window of the fused step (elements, a multiple of 8; a
+// window can exceed it by under 64 elements when a bucket's remainder joins it).
 #ifndef ZERO_WINDOW_ELEMS
 #define ZERO_WINDOW_ELEMS ZERO_FUSED_WINDOW_ELEMS
 #endif
@@ -652,14 +653,19 @@ extern "C" zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layou
     const bool v8 = state_v8_ok(sp);
     for (uint64_t b0 = 0; b0 < n; b0 += bucket_elems) {
         const uint64_t len = n - b0 < bucket_elems ? n - b0 : bucket_elems;
-        // launch windows of at most kWindow elements; windows after the first
-        // start at 8-element boundaries of the rows
+        // the fewest equal launch windows of at most kWindow elements; every
+        // cut falls on an 8-element boundary of the rows, and a remainder of
+        // under 64 elements joins the last window
         const uint64_t phase = (g->offset + b0) & 7;
-        for (uint64_t w0 = 0; w0 < len;) {
-            const uint64_t cap = w0 == 0 ? kWindow - phase : kWindow;
-            const uint64_t wl = len - w0 < cap ? len - w0 : cap;
+        const uint64_t nwin = (len + kWindow - 1) / kWindow;
+        const uint64_t target = ((len + nwin - 1) / nwin + 7) / 8 * 8;
+        uint64_t cut = target - phase;
+        for (uint64_t w0 = 0; w0 < len; cut += target) {
+            uint64_t w1 = cut < len ? cut : len;
+            if (len - w1 < 64)
+                w1 = len;
             const uint64_t e0 = b0 + w0;
-            FusedArgs a{rows + e0, g->row_stride, g->nd, split_window(g->offset + e0, wl),
+            FusedArgs a{rows + e0, g->row_stride, g->nd, split_window(g->offset + e0, w1 - w0),
                         in->master + e0, in->m + e0, in->v + e0, out->master + e0, out->m + e0,
                         out->v + e0, gath + e0, k, d_nonfinite};
             const int width = store_width(gath + e0 + a.sp.head);
@@ -670,7 +676,7 @@ extern "C" zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layou
             st = launch_status();
             if (st != ZERO_OK)
                 return st;
-            w0 += wl;
+            w0 = w1;
         }
         if (len < bucket_elems)
             break;
