@@ -349,8 +349,11 @@ def run_gpu(args) -> None:
     ms_per_step = total_ms / args.steps
     bytes_per_param = w.bytes_per_param
     kern_step_ms = statistics.fmean(kernel_ms)
-    kern_avg_ms = back_to_back_ms
-    achieved = bytes_per_param * n / (kern_avg_ms * 1e-3) / 1e9
+    from zero_sharded_optimizer_02_gb300 import _abi
+    per_step = _abi.fused_launch_count(n, w.bucket, 0)     # launch windows of one step
+    kern_avg_ms = back_to_back_ms / per_step                # average launch duration
+    launch_bytes = bytes_per_param * n / per_step           # algorithmic bytes per launch
+    achieved = launch_bytes / (kern_avg_ms * 1e-3) / 1e9
     peak = peaks.get("hbm_gbs")
     peak_src = "measured" if peak else "fallback"
     peak = peak or 6800.0
@@ -382,10 +385,13 @@ def run_gpu(args) -> None:
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src,
                      "frac_of_nominal_7900": achieved / NOMINAL_HBM_GBS,
-                     "traffic": None if traffic_pp is None else traffic_pp * n,
+                     "traffic": None if traffic_pp is None else traffic_pp * n / per_step,
                      "kernel": kernel_name(), "kernel_ms": kern_avg_ms,
-                     "kernel_ms_in_step": kern_step_ms, "kernel_launches_timed": nk,
-                     "algorithmic_bytes_per_launch": bytes_per_param * n},
+                     "launches_per_step": per_step,
+                     "kernel_ms_per_step": back_to_back_ms,
+                     "kernel_ms_in_sync_step": kern_step_ms,
+                     "steps_timed_back_to_back": nk,
+                     "algorithmic_bytes_per_launch": launch_bytes},
         "e2e": e2e,
         "gpu_launches": launches,
         "driver": "pipelined (step k+1 launched before step k's flag is read)",
