@@ -296,8 +296,10 @@ class PipelinedStep(DataParallelStep):
     words.  If step k turns out to be skipped, the committed state stays, the
     speculative step k+1 is discarded and run again from the committed state,
     so every step's result and the skip rule are exactly those of
-    DataParallelStep.  Gradient buffers must stay unchanged until the step that
-    reads them has been decided.
+    DataParallelStep.  The flag words are copied to the host on a side stream
+    after each step's kernels, so consecutive steps' kernels run back to back.
+    Gradient buffers must stay unchanged until the step that reads them has
+    been decided.
 
     Use: ``launch(grads)`` for each step, then ``finish()`` once; both return
     the decided steps' skip flags in order.
@@ -321,6 +323,9 @@ class PipelinedStep(DataParallelStep):
         self.gcur = 0
         self.flags = torch.zeros(2, dtype=torch.int32, device=self.device)
         self.flags_host = torch.zeros(2, dtype=torch.int32, pin_memory=True)
+        # the flag words travel to the host on a side stream, so the next
+        # step's kernels never wait behind a copy
+        self.flag_stream = torch.cuda.Stream(self.device)
         self.pending = []          # launched, undecided: (buf, t, flag slot, event, grads)
         self.launched = 0          # steps launched (speculative re-runs included)
         self.kernel_launches = 0   # kernels launched (one per rank and bucket)
@@ -341,10 +346,13 @@ class PipelinedStep(DataParallelStep):
             _abi.zero_step_shard(grads[r], self.layouts[r], st.states[in_buf],
                                  st.states[out_buf], gbuf, goff, self.bucket, self.loss_scale,
                                  self.h, self.flags[slot:slot + 1], self.stream)
-        with torch.cuda.stream(self.stream):
+        done = torch.cuda.Event()
+        done.record(self.stream)
+        self.flag_stream.wait_event(done)
+        with torch.cuda.stream(self.flag_stream):
             self.flags_host[slot:slot + 1].copy_(self.flags[slot:slot + 1], non_blocking=True)
-        ev = torch.cuda.Event()
-        ev.record(self.stream)
+        ev = torch.cuda.Event()              # this step's kernels and flag copy are done
+        ev.record(self.flag_stream)
         self.pending.append((out_buf, t, slot, ev, grads))
 
     def launch(self, grads: dict) -> list:
