@@ -197,7 +197,7 @@ def run_gpu(args) -> None:
     stream = torch.cuda.Stream(dev)
     with torch.cuda.stream(stream):
         dps = DataParallelStep(w.psi, w.nd, [dp_rank], w.grad_dtype, w.hparams, w.loss_scale,
-                               w.bucket, dev, gathered="slot", fused=True,
+                               w.bucket, dev, gathered=args.gathered, fused=True,
                                process_group=group,
                                stream=stream)
         L = dps.layouts[dp_rank]
@@ -212,7 +212,7 @@ def run_gpu(args) -> None:
         from zero_sharded_optimizer_02_gb300 import _abi
         desc = {dp_rank: _abi.grads(grads, row_stride, 0, w.nd, w.grad_dtype)}
         pipe = PipelinedStep(w.psi, w.nd, [dp_rank], w.grad_dtype, w.hparams, w.loss_scale,
-                             w.bucket, dev, gathered="slot", process_group=group,
+                             w.bucket, dev, gathered=args.gathered, process_group=group,
                              stream=stream)
         pipe.state[dp_rank].bufs[0].copy_(st.bufs[st.cur])
     torch.cuda.synchronize(dev)
@@ -302,6 +302,7 @@ def run_gpu(args) -> None:
         host_params = torch.empty(n, dtype=grads.dtype, pin_memory=True)
         copy_stream = torch.cuda.Stream(dev)
         stream_bucket = max(8, -(-(-(-n // args.e2e_buckets)) // 8) * 8)
+        slot0 = int(L.begin) if args.gathered == "full" else 0   # the rank's parameters
 
         def timed(fn):
             for it in range(args.e2e_steps + 1):      # first iteration untimed
@@ -312,7 +313,8 @@ def run_gpu(args) -> None:
                     t0 = time.perf_counter()
                 fn()
                 with torch.cuda.stream(stream):
-                    host_params.copy_(dps.gathered_view(dp_rank)[:n], non_blocking=True)
+                    host_params.copy_(dps.gathered_view(dp_rank)[slot0:slot0 + n],
+                                      non_blocking=True)
                 stream.synchronize()
             return (time.perf_counter() - t0) * 1e3 / args.e2e_steps
 
@@ -328,6 +330,26 @@ def run_gpu(args) -> None:
         fed_ms = max_over_ranks(timed(host_fed), group, dev)
         assert dps.host_fed_status() == 0, "a bucket never arrived"
         seq_ms = max_over_ranks(timed(sequential), group, dev)
+
+        # the host link alone: the step's gradient bytes host -> device and
+        # its parameters device -> host, each one plain copy (best of 3)
+        def copy_ms(copy):
+            best = float("inf")
+            for _ in range(3):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize(dev)
+                a.record(stream)
+                with torch.cuda.stream(stream):
+                    copy()
+                b.record(stream)
+                b.synchronize()
+                best = min(best, a.elapsed_time(b))
+            return best
+        gview = dps.gathered_view(dp_rank)
+        h2d_ms = copy_ms(lambda: grads.copy_(host_grads, non_blocking=True))
+        d2h_ms = copy_ms(lambda: host_params.copy_(gview[slot0:slot0 + n], non_blocking=True))
+        link_ms = max_over_ranks(h2d_ms + d2h_ms, group, dev)
         e2e = {"value": world * n / (fed_ms * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": w.nd * n * host_grads.element_size() + 4 * (
                    -(-n // stream_bucket)),
@@ -336,7 +358,11 @@ def run_gpu(args) -> None:
                "path": f"zero_feed_buckets + zero_step_shard_streamed, "
                        f"{-(-n // stream_bucket)} transfer buckets",
                "sequential_ms_per_step": seq_ms,
-               "sequential_value": world * n / (seq_ms * 1e-3)}
+               "sequential_value": world * n / (seq_ms * 1e-3),
+               "link": {"h2d_gbs": grads.numel() * grads.element_size() / (h2d_ms * 1e-3) / 1e9,
+                        "d2h_gbs": n * host_params.element_size() / (d2h_ms * 1e-3) / 1e9,
+                        "copies_alone_ms_per_step": link_ms,
+                        "frac": link_ms / fed_ms}}
         del host_grads, host_params
 
     if rank != 0:
@@ -378,6 +404,10 @@ def run_gpu(args) -> None:
                    "rank": dp_rank, "shard_params": n, "grad_dtype": w.grad_dtype,
                    "bucket": w.bucket, "loss_scale": w.loss_scale,
                    "row_stride_elems": row_stride,
+                   "gathered": args.gathered + (
+                       f" (slot at element {int(L.begin)}, 16-byte phase "
+                       f"{(int(L.begin) * 2) % 16} B)" if args.gathered == "full" else
+                       " (the rank's own S-element buffer)"),
                    "l2": f"inputs larger than L2 ({bytes_per_param * n / 1e9:.1f} GB per step),"
                          " no flush",
                    "parallelism": f"zero-dp{w.nd} emulated, {world} process(es)"},
@@ -390,6 +420,8 @@ def run_gpu(args) -> None:
                      "launches_per_step": per_step,
                      "kernel_ms_per_step": back_to_back_ms,
                      "kernel_ms_in_sync_step": kern_step_ms,
+                     "kernel_ms_in_sync_step_median": statistics.median(kernel_ms),
+                     "kernel_ms_in_sync_step_min": min(kernel_ms),
                      "steps_timed_back_to_back": nk,
                      "algorithmic_bytes_per_launch": launch_bytes},
         "e2e": e2e,
@@ -560,12 +592,15 @@ def run_gather(args) -> None:
                       "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak,
                                    "unit": "GB/s", "frac": gbs / peak,
                                    "algorithmic_bytes_per_param": 4},
-                      "gpu_launches": args.steps * w.nd}), flush=True)
+                      "gpu_launches": args.steps * _abi.gather_launch_count(
+                          w.psi, w.nd, 0, w.psi)}), flush=True)
 
 
 def run_checkpoint(args) -> None:
-    """Sharded checkpoint of one rank's fp32 state (master, m, v): save, then
-    load with resharding to Nd + 1 ranks of the same flat vector (host I/O)."""
+    """Sharded checkpoint of every rank's fp32 state (master, m, v): each rank
+    saves its file, then one rank of Nd + 1 loads its range from the old
+    files (resharding).  Host I/O, timed beside a plain write and read of the
+    same bytes in the same directory (the I/O bound of this host)."""
     import tempfile
 
     import numpy as np
@@ -575,6 +610,9 @@ def run_checkpoint(args) -> None:
     build.build()
     w = synth.WORKLOADS[args.config]
     nd = w.nd
+    if 12 * w.psi > 16e9:
+        sys.exit(f"--op checkpoint writes 12 B per parameter ({12 * w.psi / 1e9:.0f} GB for "
+                 f"{args.config}); use a workload of at most 1.3e9 parameters")
     d = tempfile.mkdtemp(prefix="zero_ckpt_")
     paths, total = [], 0
     saves = []
@@ -593,14 +631,37 @@ def run_checkpoint(args) -> None:
     t0 = time.perf_counter()
     _abi.zero_checkpoint_load(paths, L, *buf)
     load_s = time.perf_counter() - t0
+    # the reshard read every old file it overlaps whole (checksum) plus its range
+    s_old = -(-w.psi // nd)
+    lo, hi = int(L.begin), int(L.begin) + int(L.length)
+    read_files = [r for r in range(nd) if r * s_old < hi and lo < min((r + 1) * s_old, w.psi)]
+    load_bytes = sum(os.path.getsize(paths[r]) for r in read_files) + 12 * int(L.length)
+    # plain I/O of the same sizes: rank 0's bytes written and read back
+    n0 = int(_abi.zero_partition_layout(w.psi, nd, 0, 8).length)
+    plain = np.full(3 * n0, 1.0, np.float32)
+    q = os.path.join(d, "plain.bin")
+    t0 = time.perf_counter()
+    with open(q, "wb") as f:
+        plain.tofile(f)
+        f.flush()
+    plain_w = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    back = np.fromfile(q, np.float32)
+    plain_r = time.perf_counter() - t0
+    assert back.size == plain.size
+    os.remove(q)
     for p in paths:
         os.remove(p)
     os.rmdir(d)
     print(json.dumps({"op": "zero_checkpoint", "metric": "checkpoint GB/s (host)",
                       "save_gbs": total / sum(saves) / 1e9,
-                      "load_reshard_gbs": 12 * int(L.length) / load_s / 1e9,
+                      "load_reshard_gbs": load_bytes / load_s / 1e9,
+                      "load_reshard_s": load_s, "files_read": len(read_files),
+                      "plain_write_gbs": plain.nbytes / plain_w / 1e9,
+                      "plain_read_gbs": plain.nbytes / plain_r / 1e9,
                       "config": {"workload": f"{args.config}: {w.title}", "nd_saved": nd,
-                                 "nd_loaded": nd + 1, "bytes_saved": total}}), flush=True)
+                                 "nd_loaded": nd + 1, "bytes_saved": total,
+                                 "dir": "tempfile.mkdtemp() (page cache)"}}), flush=True)
 
 
 def main():
@@ -614,6 +675,10 @@ def main():
                     help="step (the benchmark line) or a measurement of another entry point")
     ap.add_argument("--config", default="c4", choices=["c0", "c1", "c2", "c3", "c4"])
     ap.add_argument("--rank", type=int, default=0, help="first data-parallel rank to run")
+    ap.add_argument("--gathered", choices=["slot", "full"], default="slot",
+                    help="slot: the rank's own S-element parameter buffer; full: its slot at "
+                         "r*S of the flat Nd*S buffer (odd ranks then start off the 16-byte "
+                         "boundary when S mod 8 != 0)")
     ap.add_argument("--psi", type=int, default=0, help="override the parameter count")
     ap.add_argument("--bucket", type=int, default=0, help="override the bucket size")
     ap.add_argument("--grad-dtype", choices=["f16", "bf16"], default=None,

@@ -291,9 +291,11 @@ zero_status_t zero_feed_buckets(const void* host, uint64_t host_row_stride,
  * shards[r * pitch + local], local < S, pitch >= S.  elem_bytes is 2 (fp16 or
  * bf16 parameters) or 4 (fp32 state, e.g. to reshard to another nd).
  * shards and out: device, aligned to elem_bytes; out must not overlap the
- * shards; only the range's own elements are read.  One launch per shard
- * segment of the range (at most ceil(len / S) + 1).  ZERO_ERR_INVALID_ARG on a
- * range outside [0, psi), pitch < S, NULL pointers or overlap. */
+ * shards; only the range's own elements are read.  The range spans at most
+ * ceil(len / S) + 1 shard segments; one launch copies up to
+ * ZERO_GATHER_SEGMENTS_PER_LAUNCH of them.  ZERO_ERR_INVALID_ARG on a range
+ * outside [0, psi), pitch < S, NULL pointers or overlap. */
+#define ZERO_GATHER_SEGMENTS_PER_LAUNCH 48ull
 zero_status_t zero_gather_range(const void* shards, uint64_t pitch, uint64_t psi, uint32_t nd,
                                 uint64_t begin, uint64_t len, uint32_t elem_bytes, void* out,
                                 void* stream);
@@ -307,7 +309,7 @@ zero_status_t zero_gather_range(const void* shards, uint64_t pitch, uint64_t psi
  * weights, m and v, `length` elements each, in that order. */
 typedef struct zero_ckpt_header {
     char magic[8];              /* "ZEROCKPT" */
-    uint32_t version;           /* 1 */
+    uint32_t version;           /* 2 */
     uint32_t header_bytes;      /* sizeof(zero_ckpt_header_t) */
     uint64_t psi;               /* flat parameters of the model */
     uint32_t nd;                /* data-parallel degree when saved */
@@ -317,8 +319,15 @@ typedef struct zero_ckpt_header {
     uint64_t length;            /* elements of each array in the payload */
     uint64_t step;              /* committed optimizer steps t */
     double lr, beta1, beta2, eps, weight_decay;   /* AdamW hyperparameters */
-    uint64_t payload_checksum;  /* FNV-1a (64-bit) over the payload's 32-bit words */
+    uint64_t payload_checksum;  /* 8-lane FNV-1a of the payload, defined below */
 } zero_ckpt_header_t;
+
+/* payload_checksum: the payload read as little-endian 32-bit words w_0,
+ * w_1, ...  is split into 8 lanes (word k goes to lane k mod 8); each lane
+ * runs 64-bit FNV-1a over its words, h = (h ^ w) * 0x100000001B3 from
+ * h = 0xCBF29CE484222325; the checksum is 64-bit FNV-1a over the 64 bytes of
+ * the 8 lane states (lane 0 first, each little-endian).  The lanes make the
+ * multiply chains independent, so the sum keeps up with the file write. */
 
 /* Writes rank L->rank's state (host fp32 arrays of L->length elements) and
  * h's hyperparameters, with h->step = the committed step count t, to `path`

@@ -212,9 +212,16 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
 
 def test_binding_constants_match_header(z):
     text = open(os.path.join(ROOT, "include", "zero.h")).read()
-    for name in ("ZERO_FUSED_WINDOW_ELEMS", "ZERO_STATIC_CB_ELEMS"):
+    for name in ("ZERO_FUSED_WINDOW_ELEMS", "ZERO_STATIC_CB_ELEMS",
+                 "ZERO_GATHER_SEGMENTS_PER_LAUNCH"):
         m = re.search(rf"#define {name} (\d+)ull", text)
         assert m and int(m.group(1)) == getattr(z._abi, name), name
     assert z._abi.fused_launch_count(117_187_500, 500_000_000) == 5
     assert z._abi.fused_launch_count(23_437_500, 50_000_000) == 1
     assert z._abi.fused_launch_count(16, 1) == 16 and z._abi.fused_launch_count(0, 8) == 0
+    # a whole 64-shard vector is 64 segments: two gather launches; a layer
+    # range inside one shard is one
+    assert z._abi.gather_launch_count(1_500_000_000, 64, 0, 1_500_000_000) == 2
+    assert z._abi.gather_launch_count(1000, 10, 95, 10) == 1
+    assert z._abi.gather_launch_count(1000, 10, 0, 0) == 0
+    assert z._abi.gather_launch_count(1000, 1000, 0, 1000) == 21

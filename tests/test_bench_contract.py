@@ -1,0 +1,74 @@
+"""The benchmark's one JSON line, as a user or a driver reads it.
+
+The reference arm (the CPU oracle on a tiny sample of the 4-rank workload)
+runs here on two host cores; the GPU arm runs the GPT-2-small-sized shard
+(psi = 124,439,808, Nd = 8, bf16) for a few steps on a GPU.
+"""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+BASE_KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+             "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "e2e",
+             "cpu_baseline"}
+
+
+def _run(args, cores: int, timeout: int = 900) -> dict:
+    def limit_cores():
+        os.sched_setaffinity(0, set(sorted(os.sched_getaffinity(0))[:cores]))
+
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args,
+                         capture_output=True, text=True, timeout=timeout, cwd=ROOT,
+                         preexec_fn=limit_cores)
+    assert out.returncode == 0, out.stderr[-3000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, out.stdout[-3000:]
+    return json.loads(lines[0])
+
+
+def test_reference_arm_line():
+    d = _run(["--impl", "reference", "--config", "c0", "--steps", "2", "--warmup", "3",
+              "--ref-sample", "512"], cores=2)
+    assert BASE_KEYS <= d.keys()
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "params/s"
+    assert d["higher_is_better"] is True and d["scaling"] == "weak"
+    assert (d["steps"], d["warmup"], d["n_gpus"]) == (2, 3, 1)
+    assert d["vs_baseline"] is None
+    assert d["config"]["workload"].startswith("c0")
+    assert d["config"]["sample_params_per_step"] == 2 * 512
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 2 and cb["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+@pytest.mark.gpu
+def test_gpu_arm_line():
+    from zero_sharded_optimizer_02_gb300 import _abi
+    d = _run(["--config", "c1", "--steps", "6", "--warmup", "3", "--e2e-steps", "1",
+              "--cpu-seconds", "1"], cores=4)
+    assert BASE_KEYS | {"roofline", "gpu_launches", "clocks"} <= d.keys()
+    n = 15_554_976
+    assert d["config"]["shard_params"] == n and d["config"]["workload"].startswith("c1")
+    assert d["value"] == pytest.approx(n / (d["ms_per_step"] * 1e-3), rel=1e-9)
+    assert d["higher_is_better"] is True and d["skipped_steps"] == 0
+    r = d["roofline"]
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] > 0
+    assert r["frac"] == pytest.approx(r["achieved"] / r["peak"], rel=1e-9)
+    per_step = _abi.fused_launch_count(n, 50_000_000, 0)
+    assert r["launches_per_step"] == per_step == 1
+    assert r["algorithmic_bytes_per_launch"] == (2 * 8 + 26) * n / per_step
+    # the timed region launches exactly one fused step per timed step
+    assert d["gpu_launches"] == 6 * per_step
+    e = d["e2e"]
+    assert e["value"] > 0 and e["unit"] == d["unit"]
+    assert e["h2d_bytes_per_step"] >= 8 * n * 2 and e["d2h_bytes_per_step"] == 2 * n + 4
+    assert 0 < e["link"]["frac"] <= 1.5
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 4 and cb["value"] > 0
+    assert set(d["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}

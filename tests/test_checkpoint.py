@@ -66,7 +66,7 @@ def test_header_round_trip(z, tmp_path):
     flat = [np.arange(100, dtype=np.float32) * k for k in (1, 2, 3)]
     paths = _save_all(z, tmp_path, flat, 100, 3, step=42)
     hd = z.zero_checkpoint_read_header(paths[2])
-    assert hd.magic == b"ZEROCKPT" and hd.version == 1 and hd.header_bytes == 112
+    assert hd.magic == b"ZEROCKPT" and hd.version == 2 and hd.header_bytes == 112
     assert (hd.psi, hd.nd, hd.rank, hd.shard_elems, hd.begin, hd.length, hd.step) == \
         (100, 3, 2, 34, 68, 32, 42)
     assert os.path.getsize(paths[2]) == 112 + 3 * 32 * 4
@@ -119,3 +119,37 @@ def test_detects_corruption_and_bad_sets(z, tmp_path):
         bad.length = 5
         z.zero_checkpoint_save(str(tmp_path / "x"), bad, z.adamw(**H, step=1), *buf)
     assert e.value.status == z.ZERO_ERR_INVALID_ARG
+
+
+def _checksum_by_definition(arrays) -> int:
+    """The payload checksum as the header defines it, written out: 8 FNV-1a
+    lanes over the little-endian 32-bit words (word k to lane k mod 8), then
+    FNV-1a over the 64 bytes of the lane states."""
+    mask, basis, prime = (1 << 64) - 1, 0xCBF29CE484222325, 0x100000001B3
+    words = np.concatenate([np.asarray(a, "<f4").view("<u4") for a in arrays]).tolist()
+    lanes = []
+    for lane in range(8):
+        h = basis
+        for w in words[lane::8]:
+            h = ((h ^ w) * prime) & mask
+        lanes.append(h)
+    x = basis
+    for h in lanes:
+        for k in range(8):
+            x = ((x ^ ((h >> (8 * k)) & 0xFF)) * prime) & mask
+    return x
+
+
+@pytest.mark.parametrize("psi,nd", [(3001, 3), (40, 5), (7, 8)])
+def test_payload_checksum_matches_its_definition(z, tmp_path, psi, nd):
+    # lengths that are not multiples of 8 move the lane phase between the
+    # three arrays and between the loader's chunks
+    rng = np.random.default_rng(psi)
+    flat = [rng.standard_normal(psi).astype(np.float32) for _ in range(3)]
+    paths = _save_all(z, tmp_path, flat, psi, nd)
+    for r, p in enumerate(paths):
+        L = z.zero_partition_layout(psi, nd, r, 8)
+        b, n = int(L.begin), int(L.length)
+        h = z.zero_checkpoint_read_header(p)
+        assert h.version == 2
+        assert int(h.payload_checksum) == _checksum_by_definition([a[b:b + n] for a in flat])

@@ -110,6 +110,21 @@ def fused_launch_count(n: int, bucket: int, offset: int = 0) -> int:
     return count
 
 
+# Shard segments that one zero_gather_range launch copies (include/zero.h).
+ZERO_GATHER_SEGMENTS_PER_LAUNCH = 48
+
+
+def gather_launch_count(psi: int, nd: int, begin: int, length: int) -> int:
+    """Kernel launches zero_gather_range issues for the flat range
+    [begin, begin + length): one per ZERO_GATHER_SEGMENTS_PER_LAUNCH shard
+    segments the range spans."""
+    if length == 0:
+        return 0
+    s = -(-psi // nd)
+    segments = (begin + length - 1) // s - begin // s + 1
+    return -(-segments // ZERO_GATHER_SEGMENTS_PER_LAUNCH)
+
+
 # Capacity of the library's own fusion buffer (include/zero.h).
 ZERO_STATIC_CB_ELEMS = 4194304
 ZERO_STATIC_CB_MAX_BUCKET = ZERO_STATIC_CB_ELEMS - 4

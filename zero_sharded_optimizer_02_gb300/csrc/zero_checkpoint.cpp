@@ -18,26 +18,67 @@
 #include <string.h>
 
 #include <string>
+#include <vector>
 
 #include "zero.h"
 
 namespace {
 
 const char kMagic[8] = {'Z', 'E', 'R', 'O', 'C', 'K', 'P', 'T'};
+constexpr uint32_t kVersion = 2;
+constexpr uint64_t kFnvBasis = 0xCBF29CE484222325ull;
+constexpr uint64_t kFnvPrime = 0x100000001B3ull;
 
-// FNV-1a (64-bit state) over the payload's 32-bit words.  Every payload is a
-// whole number of fp32 values, so the result does not depend on how the
-// payload is split into chunks.
-struct Fnv {
-    uint64_t h = 0xCBF29CE484222325ull;
+// The payload checksum: 8 FNV-1a lanes over the payload's 32-bit words (word
+// k to lane k mod 8), folded by FNV-1a over the lanes' bytes.  Every payload
+// is a whole number of fp32 values and the lane follows the global word
+// index, so the result does not depend on how the payload is split into
+// chunks.
+struct Fnv8 {
+    uint64_t h[8] = {kFnvBasis, kFnvBasis, kFnvBasis, kFnvBasis,
+                     kFnvBasis, kFnvBasis, kFnvBasis, kFnvBasis};
+    uint64_t words = 0;
+
     void add(const void* p, size_t bytes)
     {
         const unsigned char* b = static_cast<const unsigned char*>(p);
-        for (size_t i = 0; i + 4 <= bytes; i += 4) {
-            uint32_t w;
-            memcpy(&w, b + i, 4);
-            h = (h ^ w) * 0x100000001B3ull;
+        const size_t nw = bytes / 4;
+        size_t i = 0;
+        for (; i < nw && (words & 7); ++i, ++words)   // up to lane 0
+            h[words & 7] = (h[words & 7] ^ word(b + 4 * i)) * kFnvPrime;
+        uint64_t a0 = h[0], a1 = h[1], a2 = h[2], a3 = h[3];
+        uint64_t a4 = h[4], a5 = h[5], a6 = h[6], a7 = h[7];
+        for (; i + 8 <= nw; i += 8) {
+            const unsigned char* q = b + 4 * i;
+            a0 = (a0 ^ word(q)) * kFnvPrime;
+            a1 = (a1 ^ word(q + 4)) * kFnvPrime;
+            a2 = (a2 ^ word(q + 8)) * kFnvPrime;
+            a3 = (a3 ^ word(q + 12)) * kFnvPrime;
+            a4 = (a4 ^ word(q + 16)) * kFnvPrime;
+            a5 = (a5 ^ word(q + 20)) * kFnvPrime;
+            a6 = (a6 ^ word(q + 24)) * kFnvPrime;
+            a7 = (a7 ^ word(q + 28)) * kFnvPrime;
+            words += 8;
         }
+        h[0] = a0, h[1] = a1, h[2] = a2, h[3] = a3;
+        h[4] = a4, h[5] = a5, h[6] = a6, h[7] = a7;
+        for (; i < nw; ++i, ++words)
+            h[words & 7] = (h[words & 7] ^ word(b + 4 * i)) * kFnvPrime;
+    }
+
+    uint64_t value() const
+    {
+        uint64_t x = kFnvBasis;
+        for (int l = 0; l < 8; ++l)
+            for (int k = 0; k < 8; ++k)
+                x = (x ^ ((h[l] >> (8 * k)) & 0xFF)) * kFnvPrime;
+        return x;
+    }
+
+    static uint32_t word(const unsigned char* q)   // little-endian, any alignment
+    {
+        return (uint32_t)q[0] | (uint32_t)q[1] << 8 | (uint32_t)q[2] << 16 |
+               (uint32_t)q[3] << 24;
     }
 };
 
@@ -64,7 +105,7 @@ zero_status_t read_header(FILE* f, zero_ckpt_header_t* h)
 {
     if (!read_all(f, h, sizeof(*h)))
         return ZERO_ERR_IO;
-    if (memcmp(h->magic, kMagic, 8) != 0 || h->version != 1 ||
+    if (memcmp(h->magic, kMagic, 8) != 0 || h->version != kVersion ||
         h->header_bytes != sizeof(zero_ckpt_header_t))
         return ZERO_ERR_IO;
     zero_layout_t L;
@@ -74,22 +115,39 @@ zero_status_t read_header(FILE* f, zero_ckpt_header_t* h)
     return ZERO_OK;
 }
 
-// Streams the payload of an open file (positioned after the header) through
-// the checksum and compares.
-zero_status_t verify_payload(FILE* f, const zero_ckpt_header_t& h)
+// Streams the payload of an open file (positioned after the header) once:
+// every chunk goes through the checksum, and the elements [r0, r1) of each of
+// the three arrays are read straight into dst[a] + (element - r0).  Chunks
+// are cut at r0 and r1, so a chunk lies wholly inside or wholly outside the
+// range; those outside pass through a bounce buffer for the checksum alone.
+// ZERO_ERR_IO on a short read or a checksum mismatch (dst is then
+// unspecified).
+zero_status_t load_payload(FILE* f, const zero_ckpt_header_t& h, uint64_t r0, uint64_t r1,
+                           float* const dst[3])
 {
-    Fnv c;
-    static const size_t kChunk = 1 << 22;
-    std::string buf(kChunk, '\0');
-    uint64_t left = 3 * h.length * sizeof(float);
-    while (left) {
-        const size_t take = left < kChunk ? (size_t)left : kChunk;
-        if (!read_all(f, &buf[0], take))
-            return ZERO_ERR_IO;
-        c.add(buf.data(), take);
-        left -= take;
+    Fnv8 c;
+    static const uint64_t kChunkElems = 1 << 20;
+    std::vector<float> bounce;
+    for (int a = 0; a < 3; ++a) {
+        for (uint64_t e = 0; e < h.length;) {
+            const uint64_t edge = e < r0 ? r0 : (e < r1 ? r1 : h.length);
+            uint64_t take = edge - e < kChunkElems ? edge - e : kChunkElems;
+            const bool inside = e >= r0 && e < r1;
+            float* target;
+            if (inside) {
+                target = dst[a] + (e - r0);
+            } else {
+                if (bounce.empty())
+                    bounce.resize(kChunkElems);
+                target = bounce.data();
+            }
+            if (!read_all(f, target, (size_t)take * sizeof(float)))
+                return ZERO_ERR_IO;
+            c.add(target, (size_t)take * sizeof(float));
+            e += take;
+        }
     }
-    return c.h == h.payload_checksum ? ZERO_OK : ZERO_ERR_IO;
+    return c.value() == h.payload_checksum ? ZERO_OK : ZERO_ERR_IO;
 }
 
 }  // namespace
@@ -107,7 +165,7 @@ extern "C" zero_status_t zero_checkpoint_save(const char* path, const zero_layou
     zero_ckpt_header_t hd;
     memset(&hd, 0, sizeof(hd));
     memcpy(hd.magic, kMagic, 8);
-    hd.version = 1;
+    hd.version = kVersion;
     hd.header_bytes = sizeof(hd);
     hd.psi = L->psi;
     hd.nd = L->nd;
@@ -121,21 +179,33 @@ extern "C" zero_status_t zero_checkpoint_save(const char* path, const zero_layou
     hd.beta2 = h->beta2;
     hd.eps = h->eps;
     hd.weight_decay = h->weight_decay;
-    const size_t bytes = (size_t)L->length * sizeof(float);
-    Fnv c;
-    c.add(master, bytes);
-    c.add(m, bytes);
-    c.add(v, bytes);
-    hd.payload_checksum = c.h;
-    // write to a temporary name, then rename: a crash never leaves a torn file
+    // One pass over the payload: each chunk goes into the checksum and then
+    // to the file; the header, written first with a zero checksum, is
+    // rewritten at the end.  The file is written under a temporary name and
+    // renamed, so a crash never leaves a torn file at `path`.
     const std::string tmp = std::string(path) + ".tmp";
     {
         File f;
         f.f = fopen(tmp.c_str(), "wb");
         if (!f.f)
             return ZERO_ERR_IO;
-        if (!write_all(f.f, &hd, sizeof(hd)) || !write_all(f.f, master, bytes) ||
-            !write_all(f.f, m, bytes) || !write_all(f.f, v, bytes) || fflush(f.f) != 0) {
+        bool ok = write_all(f.f, &hd, sizeof(hd));
+        Fnv8 c;
+        static const size_t kChunk = 1 << 22;
+        const size_t bytes = (size_t)L->length * sizeof(float);
+        const float* arrays[3] = {master, m, v};
+        for (int a = 0; a < 3 && ok; ++a) {
+            const unsigned char* p = reinterpret_cast<const unsigned char*>(arrays[a]);
+            for (size_t off = 0; off < bytes && ok; off += kChunk) {
+                const size_t take = bytes - off < kChunk ? bytes - off : kChunk;
+                c.add(p + off, take);
+                ok = write_all(f.f, p + off, take);
+            }
+        }
+        hd.payload_checksum = c.value();
+        ok = ok && fseeko(f.f, 0, SEEK_SET) == 0 && write_all(f.f, &hd, sizeof(hd)) &&
+             fflush(f.f) == 0;
+        if (!ok) {
             remove(tmp.c_str());
             return ZERO_ERR_IO;
         }
@@ -200,16 +270,13 @@ extern "C" zero_status_t zero_checkpoint_load(const char* const* paths, uint32_t
         const uint64_t hi = hi_old < hi_new ? hi_old : hi_new;
         if (lo >= hi)
             continue;
-        zero_status_t st = verify_payload(f.f, hd);   // every file read is checked whole
+        // one pass over the file: checked whole, its part of the new range read
+        // into place
+        float* const at[3] = {dst[0] + (lo - lo_new), dst[1] + (lo - lo_new),
+                              dst[2] + (lo - lo_new)};
+        const zero_status_t st = load_payload(f.f, hd, lo - lo_old, hi - lo_old, at);
         if (st != ZERO_OK)
             return st;
-        for (int a = 0; a < 3; ++a) {
-            const long long off = (long long)sizeof(hd) +
-                                  (long long)((a * hd.length + (lo - lo_old)) * sizeof(float));
-            if (fseeko(f.f, off, SEEK_SET) != 0 ||
-                !read_all(f.f, dst[a] + (lo - lo_new), (size_t)(hi - lo) * sizeof(float)))
-                return ZERO_ERR_IO;
-        }
     }
     if (h_out) {
         h_out->lr = first.lr;

@@ -43,7 +43,7 @@ struct SegCopy {
 // parameters.  Every CTA copies one contiguous run of kChunksPerCta body
 // chunks of one segment (block_end is the inclusive prefix sum of the CTAs
 // each segment gets); a segment's first CTA also copies its edge units.
-constexpr int kMaxSegs = 48;
+constexpr int kMaxSegs = (int)ZERO_GATHER_SEGMENTS_PER_LAUNCH;
 constexpr int kChunksPerThread = 8;
 constexpr uint64_t kChunksPerCta = (uint64_t)kCopyThreads * kChunksPerThread;
 

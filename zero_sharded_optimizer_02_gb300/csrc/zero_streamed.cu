@@ -9,8 +9,8 @@
 // the shard's buckets in order and, before each, waits for that word.
 //
 // Every wait is bounded: thread 0 of each CTA polls the word with an acquire
-// load, sleeping between polls, for at most timeout_ns of %globaltimer time
-// and a matching iteration cap.  On expiry it records ZERO_ERR_TIMEOUT in the
+// load, sleeping between polls (64 ns, doubling up to about 2 us), for at most
+// timeout_ns of %globaltimer time and an iteration cap.  On expiry it records ZERO_ERR_TIMEOUT in the
 // status word and the CTA returns without touching that bucket or later ones;
 // the context stays usable.  The kernel never waits on another kernel: only on
 // a word written by a copy engine or the host.
@@ -51,17 +51,28 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p)
     return v;
 }
 
-// Bounded wait for *word >= epoch (by wrap-around comparison).
+// Longest sleep between two polls of a ready word.  A bucket takes
+// milliseconds to land over the host link, so polling every couple of
+// microseconds loses nothing and keeps the CTAs' polls off the L2.
+#ifndef ZERO_POLL_MAX_NS
+#define ZERO_POLL_MAX_NS 2048
+#endif
+
+// Bounded wait for *word >= epoch (by wrap-around comparison).  The sleep
+// between polls doubles from 64 ns up to ZERO_POLL_MAX_NS.
 __device__ bool wait_ready(const uint32_t* word, uint32_t epoch, uint64_t timeout_ns)
 {
     const uint64_t t0 = global_ns();
-    const uint64_t max_polls = timeout_ns / 64 + 16;   // each poll sleeps >= ~64 ns
+    const uint64_t max_polls = timeout_ns / 64 + 16;   // backstop to the time limit
+    unsigned sleep_ns = 64;
     for (uint64_t i = 0; i < max_polls; ++i) {
         if ((int32_t)(ld_acquire(word) - epoch) >= 0)
             return true;
         if (global_ns() - t0 > timeout_ns)
             return false;
-        __nanosleep(64);
+        __nanosleep(sleep_ns);
+        if (sleep_ns < ZERO_POLL_MAX_NS)
+            sleep_ns *= 2;
     }
     return (int32_t)(ld_acquire(word) - epoch) >= 0;
 }
