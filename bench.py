@@ -304,64 +304,72 @@ def run_gpu(args) -> None:
         stream_bucket = max(8, -(-(-(-n // args.e2e_buckets)) // 8) * 8)
         slot0 = int(L.begin) if args.gathered == "full" else 0   # the rank's parameters
 
-        def timed(fn):
-            for it in range(args.e2e_steps + 1):      # first iteration untimed
-                if it == 1:
-                    if world > 1:
-                        dist.barrier()
-                    torch.cuda.synchronize(dev)
-                    t0 = time.perf_counter()
-                fn()
-                with torch.cuda.stream(stream):
-                    host_params.copy_(dps.gathered_view(dp_rank)[slot0:slot0 + n],
-                                      non_blocking=True)
-                stream.synchronize()
-            return (time.perf_counter() - t0) * 1e3 / args.e2e_steps
+        gview = dps.gathered_view(dp_rank)
+
+        def read_back():
+            with torch.cuda.stream(stream):
+                host_params.copy_(gview[slot0:slot0 + n], non_blocking=True)
+            stream.synchronize()
 
         def host_fed():
             dps.launch_host_fed(dp_rank, host_grads, desc[dp_rank], stream_bucket, copy_stream)
             dps.commit(dps.decide())
+            read_back()
 
         def sequential():
             with torch.cuda.stream(stream):
                 grads.copy_(host_grads, non_blocking=True)
             dps.step(desc)
+            read_back()
 
-        fed_ms = max_over_ranks(timed(host_fed), group, dev)
-        assert dps.host_fed_status() == 0, "a bucket never arrived"
-        seq_ms = max_over_ranks(timed(sequential), group, dev)
+        host_desc = {dp_rank: _abi.grads(host_grads, row_stride, 0, w.nd, w.grad_dtype)}
 
-        # the host link alone: the step's gradient bytes host -> device and
-        # its parameters device -> host, each one plain copy (best of 3)
-        def copy_ms(copy):
-            best = float("inf")
-            for _ in range(3):
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
+        def zero_copy():      # the fused kernels read the gradients in host memory
+            dps.step(host_desc)
+            read_back()
+
+        def copies_alone():   # the host link alone: the same bytes, no step
+            with torch.cuda.stream(stream):
+                grads.copy_(host_grads, non_blocking=True)
+            read_back()
+
+        # The three forms run interleaved, one of each per iteration, so that
+        # they see the same host-memory conditions (the host is shared); the
+        # first iteration is untimed.  Each is timed on the host around the
+        # whole call, its final synchronisation included.
+        forms = {"fed": host_fed, "sequential": sequential, "zero_copy": zero_copy,
+                 "copies": copies_alone}
+        times = {k: [] for k in forms}
+        for it in range(args.e2e_steps + 1):
+            for k, fn in forms.items():
+                if world > 1:
+                    dist.barrier()
                 torch.cuda.synchronize(dev)
-                a.record(stream)
-                with torch.cuda.stream(stream):
-                    copy()
-                b.record(stream)
-                b.synchronize()
-                best = min(best, a.elapsed_time(b))
-            return best
-        gview = dps.gathered_view(dp_rank)
-        h2d_ms = copy_ms(lambda: grads.copy_(host_grads, non_blocking=True))
-        d2h_ms = copy_ms(lambda: host_params.copy_(gview[slot0:slot0 + n], non_blocking=True))
-        link_ms = max_over_ranks(h2d_ms + d2h_ms, group, dev)
+                t0 = time.perf_counter()
+                fn()
+                if it:
+                    times[k].append((time.perf_counter() - t0) * 1e3)
+        assert dps.host_fed_status() == 0, "a bucket never arrived"
+        mean = {k: max_over_ranks(statistics.fmean(v), group, dev) for k, v in times.items()}
+        fed_ms, seq_ms, link_ms = mean["fed"], mean["sequential"], mean["copies"]
         e2e = {"value": world * n / (fed_ms * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": w.nd * n * host_grads.element_size() + 4 * (
                    -(-n // stream_bucket)),
                "d2h_bytes_per_step": n * host_params.element_size() + 4,
-               "ms_per_step": fed_ms, "steps": args.e2e_steps,
+               "ms_per_step": fed_ms, "ms_per_step_min": min(times["fed"]),
+               "steps": args.e2e_steps,
                "path": f"zero_feed_buckets + zero_step_shard_streamed, "
                        f"{-(-n // stream_bucket)} transfer buckets",
                "sequential_ms_per_step": seq_ms,
                "sequential_value": world * n / (seq_ms * 1e-3),
-               "link": {"h2d_gbs": grads.numel() * grads.element_size() / (h2d_ms * 1e-3) / 1e9,
-                        "d2h_gbs": n * host_params.element_size() / (d2h_ms * 1e-3) / 1e9,
-                        "copies_alone_ms_per_step": link_ms,
+               "zero_copy_ms_per_step": mean["zero_copy"],
+               "zero_copy_min_ms": min(times["zero_copy"]),
+               "zero_copy_value": world * n / (mean["zero_copy"] * 1e-3),
+               "ms_per_iteration": {k: [round(x, 3) for x in v] for k, v in times.items()},
+               "link": {"copies_alone_ms_per_step": link_ms,
+                        "copies_alone_min_ms": min(times["copies"]),
+                        "h2d_plus_d2h_gbs": (grads.numel() + n) * grads.element_size() /
+                        (link_ms * 1e-3) / 1e9,
                         "frac": link_ms / fed_ms}}
         del host_grads, host_params
 
@@ -685,7 +693,7 @@ def main():
                     help="override the gradient dtype")
     ap.add_argument("--row-pad", type=int, default=0,
                     help="extra elements (multiple of 8) between contribution rows")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--e2e-buckets", type=int, default=16,
                     help="transfer buckets of the host-fed e2e step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -73,16 +73,21 @@ typedef struct zero_layout {
     uint64_t row_pitch;    /* S rounded up to row_align_elems: the emulated row pitch */
 } zero_layout_t;
 
-/* The Nd gradient contributions to one rank's shard, in device memory.  The
- * contribution of rank j to shard element i is the 2-byte element
+/* The Nd gradient contributions to one rank's shard.  The contribution of
+ * rank j to shard element i is the 2-byte element
  *     base[j * row_stride + offset + i],   0 <= j < nd.
  * Full emulation (every rank's whole gradient resident): row j is rank j's
  * gradient in padded-partition layout, row_stride = nd * row_pitch,
  * offset = rank * row_pitch.  Shard view: row j holds only this shard,
  * row_stride = row_pitch, offset = 0.
- * Alignment: base 16-byte aligned; row_stride and offset multiples of 8. */
+ * Alignment: base 16-byte aligned; row_stride and offset multiples of 8.
+ * Memory: device (or managed) memory, or page-locked host memory registered
+ * with CUDA (cudaHostAlloc, cudaHostRegister), which the kernels then read in
+ * place over the host link (zero-copy: no device copy of the gradients).  Any
+ * other pointer, pageable host memory included, is ZERO_ERR_INVALID_ARG
+ * before anything is launched. */
 typedef struct zero_grads {
-    const void* base;     /* device, read-only */
+    const void* base;     /* device or page-locked host memory, read-only */
     uint64_t row_stride;  /* elements between consecutive ranks' rows */
     uint64_t offset;      /* element offset of this shard within every row */
     uint32_t nd;          /* number of contributions (>= 1) */

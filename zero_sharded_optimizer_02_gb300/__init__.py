@@ -6,11 +6,13 @@ of ``include/zero.h``); ``_abi`` binds it with the same function names and
 fallback: without the built library every entry point raises.
 """
 from ._abi import (  # noqa: F401
-    ZERO_BF16, ZERO_ERR_ALIGNMENT, ZERO_ERR_CUDA, ZERO_ERR_INVALID_ARG, ZERO_ERR_TIMEOUT,
-    ZERO_ERR_UNSUPPORTED, ZERO_F16, ZERO_OK, AdamW, Grads, Layout, State, ZeroError, adamw,
-    exported_names, grads, lib, state, zero_adam_step_shard, zero_check_nonfinite,
-    zero_comm_volume_elems, zero_gather_range, zero_model_state_bytes_mp, ZERO_ERR_IO,
-    CkptHeader, zero_step_shard_streamed, zero_feed_buckets, zero_checkpoint_save, zero_checkpoint_read_header, zero_checkpoint_load,
-    zero_gather_params_shard, zero_model_state_bytes, zero_partition_layout,
-    zero_reduce_scatter_bucket, zero_status_string, zero_step_shard, zero_step_shard_unfused,
-    zero_step_shard_unfused_static, ZERO_STATIC_CB_ELEMS, ZERO_STATIC_CB_MAX_BUCKET)
+    ZERO_BF16, ZERO_ERR_ALIGNMENT, ZERO_ERR_CUDA, ZERO_ERR_INVALID_ARG, ZERO_ERR_IO,
+    ZERO_ERR_TIMEOUT, ZERO_ERR_UNSUPPORTED, ZERO_F16, ZERO_FUSED_WINDOW_ELEMS,
+    ZERO_GATHER_SEGMENTS_PER_LAUNCH, ZERO_OK, ZERO_STATIC_CB_ELEMS, ZERO_STATIC_CB_MAX_BUCKET,
+    AdamW, CkptHeader, Grads, Layout, State, ZeroError, adamw, exported_names,
+    fused_launch_count, gather_launch_count, grads, lib, state, zero_adam_step_shard,
+    zero_check_nonfinite, zero_checkpoint_load, zero_checkpoint_read_header,
+    zero_checkpoint_save, zero_comm_volume_elems, zero_feed_buckets, zero_gather_params_shard,
+    zero_gather_range, zero_model_state_bytes, zero_model_state_bytes_mp,
+    zero_partition_layout, zero_reduce_scatter_bucket, zero_status_string, zero_step_shard,
+    zero_step_shard_streamed, zero_step_shard_unfused, zero_step_shard_unfused_static)

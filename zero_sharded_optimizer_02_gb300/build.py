@@ -28,8 +28,8 @@ SOURCES = {
                        "-Xptxas", "-v", "-I", INCLUDE, "-c"],
     "zero_host.cpp": ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-Wextra", "-I", INCLUDE,
                       "-c"],
-    "zero_checkpoint.cpp": ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-Wextra", "-I",
-                            INCLUDE, "-c"],
+    "zero_checkpoint.cpp": ["g++", "-O2", "-std=c++17", "-fPIC", "-pthread", "-Wall",
+                            "-Wextra", "-I", INCLUDE, "-c"],
 }
 
 
@@ -104,7 +104,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         raise RuntimeError(f"compilation failed: {failed}")
     if force or _stale(OUT, objs):
         tmp = OUT + f".tmp{os.getpid()}"
-        subprocess.check_call([_nvcc(), "-shared", *ARCH, "-o", tmp, *objs])
+        subprocess.check_call([_nvcc(), "-shared", *ARCH, "-o", tmp, *objs, "-lpthread"])
         os.replace(tmp, OUT)
     return OUT
 

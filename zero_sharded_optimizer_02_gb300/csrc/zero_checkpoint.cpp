@@ -18,6 +18,7 @@
 #include <string.h>
 
 #include <string>
+#include <thread>
 #include <vector>
 
 #include "zero.h"
@@ -179,36 +180,43 @@ extern "C" zero_status_t zero_checkpoint_save(const char* path, const zero_layou
     hd.beta2 = h->beta2;
     hd.eps = h->eps;
     hd.weight_decay = h->weight_decay;
-    // One pass over the payload: each chunk goes into the checksum and then
-    // to the file; the header, written first with a zero checksum, is
-    // rewritten at the end.  The file is written under a temporary name and
-    // renamed, so a crash never leaves a torn file at `path`.
+    // The checksum runs on a second thread over the in-memory arrays while
+    // this one writes them; the header, written first with a zero checksum,
+    // is rewritten at the end.  The file is written under a temporary name
+    // and renamed, so a crash never leaves a torn file at `path`.
+    const size_t bytes = (size_t)L->length * sizeof(float);
+    const float* arrays[3] = {master, m, v};
+    uint64_t sum = 0;
+    auto checksum = [&]() {
+        Fnv8 c;
+        for (const float* a : arrays)
+            c.add(a, bytes);
+        sum = c.value();
+    };
+    std::thread worker;
+    try {
+        worker = std::thread(checksum);
+    } catch (...) {   // no thread to be had: sum inline after the writes
+    }
     const std::string tmp = std::string(path) + ".tmp";
+    bool ok;
     {
         File f;
         f.f = fopen(tmp.c_str(), "wb");
-        if (!f.f)
-            return ZERO_ERR_IO;
-        bool ok = write_all(f.f, &hd, sizeof(hd));
-        Fnv8 c;
-        static const size_t kChunk = 1 << 22;
-        const size_t bytes = (size_t)L->length * sizeof(float);
-        const float* arrays[3] = {master, m, v};
-        for (int a = 0; a < 3 && ok; ++a) {
-            const unsigned char* p = reinterpret_cast<const unsigned char*>(arrays[a]);
-            for (size_t off = 0; off < bytes && ok; off += kChunk) {
-                const size_t take = bytes - off < kChunk ? bytes - off : kChunk;
-                c.add(p + off, take);
-                ok = write_all(f.f, p + off, take);
-            }
-        }
-        hd.payload_checksum = c.value();
+        ok = f.f != nullptr && write_all(f.f, &hd, sizeof(hd));
+        for (int a = 0; a < 3 && ok; ++a)
+            ok = write_all(f.f, arrays[a], bytes);
+        if (worker.joinable())
+            worker.join();
+        else
+            checksum();
+        hd.payload_checksum = sum;
         ok = ok && fseeko(f.f, 0, SEEK_SET) == 0 && write_all(f.f, &hd, sizeof(hd)) &&
              fflush(f.f) == 0;
-        if (!ok) {
-            remove(tmp.c_str());
-            return ZERO_ERR_IO;
-        }
+    }
+    if (!ok) {
+        remove(tmp.c_str());
+        return ZERO_ERR_IO;
     }
     if (rename(tmp.c_str(), path) != 0) {
         remove(tmp.c_str());

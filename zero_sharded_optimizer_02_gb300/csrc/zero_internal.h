@@ -31,4 +31,12 @@ bool adamw_valid(const zero_adamw_t* h);
 // (pass nd = 1, loss_scale = 1 when the gradient is already scaled).
 StepScalars make_scalars(const zero_adamw_t* h, uint32_t nd, double loss_scale);
 
+// The descriptor the kernels read: g with base replaced by the address the
+// device reads it at.  Device and managed memory are read where they are;
+// page-locked host memory registered with CUDA is read in place over the
+// host link (zero-copy) at its device-mapped address; anything else
+// (pageable host memory, unknown pointers) is ZERO_ERR_INVALID_ARG, since the
+// GPU must not touch it.
+zero_status_t resolve_grads(const zero_grads_t* g, zero_grads_t* out);
+
 }  // namespace zero

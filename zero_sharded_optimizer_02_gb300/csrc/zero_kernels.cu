@@ -27,6 +27,29 @@
 #include "zero_device.cuh"
 
 namespace zero {
+
+zero_status_t resolve_grads(const zero_grads_t* g, zero_grads_t* out)
+{
+    *out = *g;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, g->base) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return ZERO_ERR_INVALID_ARG;
+    }
+    switch (at.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged:
+        return ZERO_OK;
+    case cudaMemoryTypeHost:
+        if (!at.devicePointer || ((uintptr_t)at.devicePointer & 15) != 0)
+            return ZERO_ERR_INVALID_ARG;
+        out->base = at.devicePointer;
+        return ZERO_OK;
+    default:
+        return ZERO_ERR_INVALID_ARG;
+    }
+}
+
 namespace {
 
 constexpr int kThreads = 256;       // threads per CTA
@@ -566,7 +589,11 @@ extern "C" zero_status_t zero_reduce_scatter_bucket(const zero_grads_t* g, uint6
         return ZERO_ERR_ALIGNMENT;
     if (bucket_len == 0)
         return ZERO_OK;
-    const uint16_t* first = static_cast<const uint16_t*>(g->base) + g->offset + bucket_begin;
+    zero_grads_t gr;   // the rows at the address the device reads them
+    st = resolve_grads(g, &gr);
+    if (st != ZERO_OK)
+        return st;
+    const uint16_t* first = static_cast<const uint16_t*>(gr.base) + g->offset + bucket_begin;
     ReduceArgs a{first, g->row_stride, g->nd, split_window(g->offset + bucket_begin, bucket_len),
                  inv_scale, cb_out, d_nonfinite};
     launch_reduce(a, g->dtype, static_cast<cudaStream_t>(stream));
@@ -585,7 +612,11 @@ extern "C" zero_status_t zero_check_nonfinite(const zero_grads_t* g, uint64_t be
         return ZERO_ERR_ALIGNMENT;
     if (n == 0)
         return ZERO_OK;
-    const uint16_t* first = static_cast<const uint16_t*>(g->base) + g->offset + begin;
+    zero_grads_t gr;   // the rows at the address the device reads them
+    st = resolve_grads(g, &gr);
+    if (st != ZERO_OK)
+        return st;
+    const uint16_t* first = static_cast<const uint16_t*>(gr.base) + g->offset + begin;
     ReduceArgs a{first, g->row_stride, g->nd, split_window(g->offset + begin, n), 1.0f, nullptr,
                  d_nonfinite};
     launch_reduce(a, g->dtype, static_cast<cudaStream_t>(stream));
@@ -645,9 +676,13 @@ extern "C" zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layou
     const uint64_t n = L->length;
     if (n == 0)
         return ZERO_OK;
+    zero_grads_t gr;   // the rows at the address the device reads them
+    st = resolve_grads(g, &gr);
+    if (st != ZERO_OK)
+        return st;
     const StepScalars k = make_scalars(h, g->nd, loss_scale);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const uint16_t* rows = static_cast<const uint16_t*>(g->base) + g->offset;
+    const uint16_t* rows = static_cast<const uint16_t*>(gr.base) + g->offset;
     uint16_t* gath = static_cast<uint16_t*>(gathered) + gathered_offset_elems;
     const float* const sp[6] = {in->master, in->m, in->v, out->master, out->m, out->v};
     const bool v8 = state_v8_ok(sp);
@@ -704,10 +739,14 @@ extern "C" zero_status_t zero_step_shard_unfused(const zero_grads_t* g, const ze
         return ZERO_ERR_ALIGNMENT;
     if (n == 0)
         return ZERO_OK;
+    zero_grads_t gr;   // the rows at the address the device reads them
+    st = resolve_grads(g, &gr);
+    if (st != ZERO_OK)
+        return st;
     const StepScalars k = make_scalars(h, g->nd, loss_scale);
     const StepScalars k_adam_only = make_scalars(h, 1, 1.0);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const uint16_t* rows = static_cast<const uint16_t*>(g->base) + g->offset;
+    const uint16_t* rows = static_cast<const uint16_t*>(gr.base) + g->offset;
     uint16_t* gath = static_cast<uint16_t*>(gathered) + gathered_offset_elems;
     for (uint64_t b0 = 0; b0 < n; b0 += bucket_elems) {
         const uint64_t len = n - b0 < bucket_elems ? n - b0 : bucket_elems;

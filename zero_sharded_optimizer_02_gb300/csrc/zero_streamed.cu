@@ -9,7 +9,7 @@
 // the shard's buckets in order and, before each, waits for that word.
 //
 // Every wait is bounded: thread 0 of each CTA polls the word with an acquire
-// load, sleeping between polls (64 ns, doubling up to about 2 us), for at most
+// load, sleeping between polls (64 ns, doubling up to about 16 us), for at most
 // timeout_ns of %globaltimer time and an iteration cap.  On expiry it records ZERO_ERR_TIMEOUT in the
 // status word and the CTA returns without touching that bucket or later ones;
 // the context stays usable.  The kernel never waits on another kernel: only on
@@ -51,11 +51,12 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p)
     return v;
 }
 
-// Longest sleep between two polls of a ready word.  A bucket takes
-// milliseconds to land over the host link, so polling every couple of
-// microseconds loses nothing and keeps the CTAs' polls off the L2.
+// Longest sleep between two polls of a ready word.  Every CTA polls the same
+// word, so frequent polls pile onto one L2 slice and slow the copy engine's
+// writes of the bucket itself.  A bucket takes milliseconds to land over the
+// host link; polling every ~16 us delays only the last bucket, by as much.
 #ifndef ZERO_POLL_MAX_NS
-#define ZERO_POLL_MAX_NS 2048
+#define ZERO_POLL_MAX_NS 16384
 #endif
 
 // Bounded wait for *word >= epoch (by wrap-around comparison).  The sleep
@@ -225,8 +226,12 @@ extern "C" zero_status_t zero_step_shard_streamed(
     }
     if (n == 0)
         return ZERO_OK;
+    zero_grads_t gr;   // the rows at the address the device reads them
+    const zero_status_t rs = resolve_grads(g, &gr);
+    if (rs != ZERO_OK)
+        return rs;
     StreamArgs s;
-    s.a.g = static_cast<const uint16_t*>(g->base) + g->offset;
+    s.a.g = static_cast<const uint16_t*>(gr.base) + g->offset;
     s.a.row_stride = g->row_stride;
     s.a.nd = g->nd;
     s.a.sp = Split{0, 0, 0};
