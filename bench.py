@@ -176,15 +176,24 @@ def run_gpu(args) -> None:
     import synth
     from zero_sharded_optimizer_02_gb300 import build
     from zero_sharded_optimizer_02_gb300.step import (DataParallelStep, PipelinedStep,
-                                                      data_parallel_rank, max_over_ranks)
+                                                      data_parallel_rank, max_over_ranks,
+                                                      sum_over_ranks)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    # One process per GPU over NCCL.  ZERO_DIST_BACKEND=gloo runs the same
+    # choreography with host collectives, and then processes may share a GPU
+    # (no kernel of this path waits on another process's kernels).
+    backend = os.environ.get("ZERO_DIST_BACKEND", "nccl")
+    gpu = local % torch.cuda.device_count() if backend == "gloo" else local
     if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
+        if backend == "nccl":
+            dist.init_process_group("nccl", device_id=torch.device("cuda", gpu))
+        else:
+            dist.init_process_group(backend)
+    torch.cuda.set_device(gpu)
+    dev = torch.device("cuda", gpu)
     if rank == 0 or world == 1:
         build.build()
     if world > 1:
@@ -225,7 +234,7 @@ def run_gpu(args) -> None:
         pipe.launch(desc)
     pipe.finish()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(smi_index(local)) if rank == 0 else None
+    sampler = ClockSampler(smi_index(gpu)) if rank == 0 else None
     time.sleep(0.3 if sampler else 0.0)
     if world > 1:
         dist.barrier()
@@ -243,7 +252,7 @@ def run_gpu(args) -> None:
     if world > 1:
         dist.barrier()
     total_ms = t_start.elapsed_time(t_end)
-    launches = pipe.kernel_launches - launched0
+    launches = sum_over_ranks(pipe.kernel_launches - launched0, group, dev)   # whole job
     skipped = sum(decided)
     assert len(decided) == args.steps
 

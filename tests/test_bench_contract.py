@@ -72,3 +72,31 @@ def test_gpu_arm_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] == 4 and cb["value"] > 0
     assert set(d["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
+
+
+@pytest.mark.gpu
+def test_gpu_arm_two_processes():
+    """The N > 1 choreography of the benchmark (barriers, max over ranks, one
+    line from rank 0, whole-job value) with two processes.  One GPU is shared
+    through host (gloo) collectives: each process runs its own rank's shard,
+    and no kernel waits on the other process."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    env = dict(os.environ, ZERO_DIST_BACKEND="gloo")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.join(ROOT, "bench.py"), "--gpus", "2", "--config", "c1", "--steps", "6",
+           "--warmup", "3", "--e2e-steps", "1", "--cpu-seconds", "1"]
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=900, cwd=ROOT, env=env)
+    assert out.returncode == 0, out.stderr[-3000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, out.stdout[-3000:]
+    d = json.loads(lines[0])
+    n = 15_554_976
+    assert d["n_gpus"] == 2 and d["scaling"] == "weak"
+    assert d["value"] == pytest.approx(2 * n / (d["ms_per_step"] * 1e-3), rel=1e-9)
+    assert d["config"]["rank"] == 0 and d["skipped_steps"] == 0
+    assert d["gpu_launches"] == 2 * 6          # both processes' launches
+    assert d["e2e"]["value"] > 0

@@ -45,13 +45,14 @@ def _checks(rank: int, world: int):
     import synth
     import zero_sharded_optimizer_02_gb300 as z
     from zero_sharded_optimizer_02_gb300.step import (data_parallel_rank, global_skip,
-                                                      max_over_ranks)
+                                                      max_over_ranks, sum_over_ranks)
     g = dist.group.WORLD
     # skip decision: one rank's overflow skips everyone; clean everywhere commits
     assert global_skip(False, g) is False
     assert global_skip(rank == 1, g) is True
     assert global_skip(rank == 0, g) is True
     assert max_over_ranks(rank + 1.5, g) == world - 1 + 1.5
+    assert sum_over_ranks(rank + 5, g) == sum(r + 5 for r in range(world))
     assert data_parallel_rank(0, rank, 64) == rank
     assert data_parallel_rank(62, rank, 64) == 62 + rank
     with pytest.raises(ValueError):

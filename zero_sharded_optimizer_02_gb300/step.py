@@ -52,6 +52,16 @@ def max_over_ranks(x: float, group=None, device=None) -> float:
     return float(t.item())
 
 
+def sum_over_ranks(x: int, group=None, device=None) -> int:
+    """The sum of a per-rank count over ``group`` (identity without one)."""
+    if group is None:
+        return int(x)
+    import torch.distributed as dist
+    t = torch.tensor([int(x)], dtype=torch.int64, device=_collective_device(group, device))
+    dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
+    return int(t.item())
+
+
 def data_parallel_rank(first_rank: int, process_rank: int, nd: int) -> int:
     """The data-parallel rank a process runs: process k of a launch runs rank
     first_rank + k of the emulated Nd-way group."""
