@@ -360,26 +360,37 @@ def run_gpu(args) -> None:
                     times[k].append((time.perf_counter() - t0) * 1e3)
         assert dps.host_fed_status() == 0, "a bucket never arrived"
         mean = {k: max_over_ranks(statistics.fmean(v), group, dev) for k, v in times.items()}
-        fed_ms, seq_ms, link_ms = mean["fed"], mean["sequential"], mean["copies"]
-        e2e = {"value": world * n / (fed_ms * 1e-3), "unit": UNIT,
-               "h2d_bytes_per_step": w.nd * n * host_grads.element_size() + 4 * (
-                   -(-n // stream_bucket)),
+        best = {k: max_over_ranks(min(v), group, dev) for k, v in times.items()}
+        grad_bytes = w.nd * n * host_grads.element_size()
+        nbk = -(-n // stream_bucket)
+
+        def form(k, path, h2d):
+            return {"ms_per_step": mean[k], "ms_per_step_min": best[k],
+                    "value": world * n / (mean[k] * 1e-3), "path": path,
+                    "h2d_bytes_per_step": h2d}
+        # The headline is the zero-copy form: the kernels read the step's
+        # gradients in place in pinned host memory, so the same bytes cross
+        # the host link every step without a device copy; it runs steadily
+        # where the copy engines' time varies with the shared host.
+        e2e = {"value": world * n / (mean["zero_copy"] * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": grad_bytes,
                "d2h_bytes_per_step": n * host_params.element_size() + 4,
-               "ms_per_step": fed_ms, "ms_per_step_min": min(times["fed"]),
+               "ms_per_step": mean["zero_copy"], "ms_per_step_min": best["zero_copy"],
                "steps": args.e2e_steps,
-               "path": f"zero_feed_buckets + zero_step_shard_streamed, "
-                       f"{-(-n // stream_bucket)} transfer buckets",
-               "sequential_ms_per_step": seq_ms,
-               "sequential_value": world * n / (seq_ms * 1e-3),
-               "zero_copy_ms_per_step": mean["zero_copy"],
-               "zero_copy_min_ms": min(times["zero_copy"]),
-               "zero_copy_value": world * n / (mean["zero_copy"] * 1e-3),
+               "path": "zero_step_shard reading the Nd gradient rows in place in pinned host "
+                       "memory (zero-copy over the host link), then the flag and the new "
+                       "parameters device-to-host",
+               "other_forms": {
+                   "fed": form("fed", f"zero_feed_buckets (DMA, {nbk} transfer buckets) + "
+                                      "zero_step_shard_streamed", grad_bytes + 4 * nbk),
+                   "sequential": form("sequential", "one DMA copy of the gradients, then "
+                                                    "zero_step_shard", grad_bytes),
+                   "copies_alone": form("copies", "the DMA copies alone, no step",
+                                        grads.numel() * grads.element_size())},
                "ms_per_iteration": {k: [round(x, 3) for x in v] for k, v in times.items()},
-               "link": {"copies_alone_ms_per_step": link_ms,
-                        "copies_alone_min_ms": min(times["copies"]),
-                        "h2d_plus_d2h_gbs": (grads.numel() + n) * grads.element_size() /
-                        (link_ms * 1e-3) / 1e9,
-                        "frac": link_ms / fed_ms}}
+               "link": {"bound_ms": best["copies"],
+                        "bound": "the fastest iteration of the DMA copies alone",
+                        "frac": best["copies"] / mean["zero_copy"]}}
         del host_grads, host_params
 
     if rank != 0:

@@ -67,8 +67,10 @@ def test_gpu_arm_line():
     assert d["gpu_launches"] == 6 * per_step
     e = d["e2e"]
     assert e["value"] > 0 and e["unit"] == d["unit"]
-    assert e["h2d_bytes_per_step"] >= 8 * n * 2 and e["d2h_bytes_per_step"] == 2 * n + 4
+    assert e["h2d_bytes_per_step"] == 8 * n * 2 and e["d2h_bytes_per_step"] == 2 * n + 4
     assert 0 < e["link"]["frac"] <= 1.5
+    assert set(e["other_forms"]) == {"fed", "sequential", "copies_alone"}
+    assert all(len(v) == 1 for v in e["ms_per_iteration"].values())
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] == 4 and cb["value"] > 0
     assert set(d["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}

@@ -36,7 +36,8 @@ StepScalars make_scalars(const zero_adamw_t* h, uint32_t nd, double loss_scale);
 // page-locked host memory registered with CUDA is read in place over the
 // host link (zero-copy) at its device-mapped address; anything else
 // (pageable host memory, unknown pointers) is ZERO_ERR_INVALID_ARG, since the
-// GPU must not touch it.
-zero_status_t resolve_grads(const zero_grads_t* g, zero_grads_t* out);
+// GPU must not touch it.  *in_host (if given) tells whether the rows are in
+// host memory.
+zero_status_t resolve_grads(const zero_grads_t* g, zero_grads_t* out, bool* in_host = nullptr);
 
 }  // namespace zero

