@@ -82,10 +82,10 @@ def recorded_traffic(workload: str):
         return None
     if kv.get("kernel_source_sha256_16") != kernel_source_hash():
         return None
-    if kv.get("workload") != workload or kv.get("build_flags", "") != os.environ.get(
-            "ZERO_NVCC_FLAGS", ""):
+    if kv.get("build_flags", "") != os.environ.get("ZERO_NVCC_FLAGS", ""):
         return None
-    return float(kv["dram_bytes_per_param"])
+    v = kv.get(f"dram_bytes_per_param.{workload}")
+    return None if v is None else float(v)
 
 
 def workload(args):
