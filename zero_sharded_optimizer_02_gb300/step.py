@@ -232,6 +232,10 @@ class DataParallelStep:
             self._epoch = 0
             self._epoch_host = torch.zeros(1, dtype=torch.int32, pin_memory=True)
             self._status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        if getattr(self, "_feed_done", None) is not None:
+            # the previous feed's copies read _epoch_host; they are done unless
+            # that step timed out, and must be before it is overwritten
+            self._feed_done.synchronize()
         self._epoch += 1
         self._epoch_host[0] = self._epoch
         self.h.step = self.t + 1
@@ -246,6 +250,8 @@ class DataParallelStep:
                                       self._status, self.stream)
         _abi.zero_feed_buckets(host_rows, int(host_rows.shape[1]), dev_grads, n, stream_bucket,
                                self._ready, self._epoch_host, copy_stream)
+        self._feed_done = torch.cuda.Event()
+        self._feed_done.record(copy_stream)
         return 1
 
     def host_fed_status(self) -> int:
