@@ -189,6 +189,12 @@ zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layout_t* L,
                               double loss_scale, const zero_adamw_t* h, uint32_t* d_nonfinite,
                               void* stream);
 
+/* Bit of *d_nonfinite that a step kernel sets, besides the nonfinite bit, if
+ * it gave up waiting on its own copy pipeline (a bounded wait that never
+ * expires in a healthy run).  The step must then be skipped, like any nonzero
+ * flag, and the caller should report ZERO_ERR_TIMEOUT. */
+#define ZERO_STEP_FLAG_WAIT_TIMEOUT 0x80000000u
+
 /* Longest launch window of the fused step, in elements (see zero_step_shard). */
 #define ZERO_FUSED_WINDOW_ELEMS 25165824ull
 

@@ -216,6 +216,13 @@ def test_binding_constants_match_header(z):
                  "ZERO_GATHER_SEGMENTS_PER_LAUNCH"):
         m = re.search(rf"#define {name} (\d+)ull", text)
         assert m and int(m.group(1)) == getattr(z._abi, name), name
+    m = re.search(r"#define ZERO_STEP_FLAG_WAIT_TIMEOUT (0x[0-9A-Fa-f]+)u", text)
+    assert m and int(m.group(1), 16) == z._abi.ZERO_STEP_FLAG_WAIT_TIMEOUT
+    # the flag word: zero commits, any nonfinite bit skips, the wait bit raises
+    assert z._abi.check_step_flag(0) is False and z._abi.check_step_flag(1) is True
+    with pytest.raises(z.ZeroError) as e:
+        z._abi.check_step_flag(-(1 << 31) | 1)      # as an int32 read back from the device
+    assert e.value.status == z.ZERO_ERR_TIMEOUT
     assert z._abi.fused_launch_count(117_187_500, 500_000_000) == 5
     assert z._abi.fused_launch_count(23_437_500, 50_000_000) == 1
     assert z._abi.fused_launch_count(16, 1) == 16 and z._abi.fused_launch_count(0, 8) == 0

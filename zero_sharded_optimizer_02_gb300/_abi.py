@@ -110,6 +110,19 @@ def fused_launch_count(n: int, bucket: int, offset: int = 0) -> int:
     return count
 
 
+# Bit of the step flag word set when a step kernel gave up waiting on its own
+# copy pipeline (include/zero.h).
+ZERO_STEP_FLAG_WAIT_TIMEOUT = 0x80000000
+
+
+def check_step_flag(word: int, where: str = "step kernel") -> bool:
+    """The skip decision of one flag word (nonzero: skip); raises ZeroError
+    (ZERO_ERR_TIMEOUT) if the kernel reported a pipeline wait that expired."""
+    if int(word) & ZERO_STEP_FLAG_WAIT_TIMEOUT:
+        raise ZeroError(ZERO_ERR_TIMEOUT, where)
+    return int(word) != 0
+
+
 # Shard segments that one zero_gather_range launch copies (include/zero.h).
 ZERO_GATHER_SEGMENTS_PER_LAUNCH = 48
 

@@ -103,6 +103,35 @@ constexpr int kRingThreads = ZERO_RING_THREADS;
 constexpr size_t kRingBytes = (size_t)kRingDepth * kRingRows * kRingThreads * 16;
 static_assert(kRingBytes <= 227 * 1024, "ring exceeds shared memory");
 
+// Fused step, bulk-copy variant (ZERO_FUSED_IMPL 2): a producer warp streams
+// each tile's rows into a kTmaStages-deep ring of shared-memory stages with
+// cp.async.bulk (one copy per rank row, completion counted on the stage's
+// mbarrier); kTmaConsumers consumer threads fold them, one 8-element vector
+// each per tile.
+#ifndef ZERO_TMA_CONSUMERS
+#define ZERO_TMA_CONSUMERS 256
+#endif
+#ifndef ZERO_TMA_ROWS
+#define ZERO_TMA_ROWS 8
+#endif
+#ifndef ZERO_TMA_STAGES
+#define ZERO_TMA_STAGES 5
+#endif
+constexpr int kTmaConsumers = ZERO_TMA_CONSUMERS;
+constexpr int kTmaThreads = kTmaConsumers + 32;          // + the producer warp
+constexpr int kTmaRows = ZERO_TMA_ROWS;                  // rank rows per stage
+constexpr int kTmaStages = ZERO_TMA_STAGES;
+constexpr uint32_t kTmaRowBytes = kTmaConsumers * 16;    // one row of one tile
+constexpr size_t kTmaStageBytes = (size_t)kTmaRows * kTmaRowBytes;
+constexpr size_t kTmaBytes = kTmaStages * kTmaStageBytes + 2 * kTmaStages * sizeof(uint64_t);
+static_assert(kTmaConsumers % 32 == 0 && kTmaStages <= 32, "TMA pipeline shape");
+static_assert(kTmaBytes <= 227 * 1024, "TMA ring exceeds shared memory");
+static_assert((size_t)kTmaRows * kTmaRowBytes < (1u << 20), "stage exceeds an mbarrier phase");
+// Longest wait on a pipeline barrier before the kernel gives up (a healthy
+// wait lasts microseconds), and on each in-flight copy after giving up.
+constexpr uint64_t kTmaWaitNs = 10ull * 1000 * 1000 * 1000;
+constexpr uint64_t kTmaDrainNs = 1000ull * 1000 * 1000;
+
 // K4, register variant: fused reduce + scale + AdamW + cast, one pass over
 // the window; each thread loads kRankUnroll rows of 16 bytes back to back.
 template <int DT, int W, bool V8>
@@ -204,6 +233,124 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_step_fused_ring(const Fused
         }
     }
     cp_async_wait<0>();
+    flag_if_any(bad, a.flag);
+}
+
+// K4, bulk-copy variant.  Tiles of kTmaConsumers vectors are dealt to the
+// CTAs round robin, so the grid moves through the rows together.  For each
+// tile the producer thread copies row groups of kTmaRows rows into the ring
+// (a stage is free once all consumers arrived on its "empty" barrier; its
+// "full" barrier completes when the copies' bytes have landed).  Consumers
+// fold the rows in rank order, release the stage, and after the last group
+// run the epilogue of their vector with 256-bit state accesses.  Every
+// barrier wait is bounded: on expiry ZERO_STEP_FLAG_WAIT_TIMEOUT is set in the
+// flag word, the producer waits (bounded) for the copies it issued, and the
+// CTA ends.
+template <int DT, int W, bool V8>
+__global__ void __launch_bounds__(kTmaThreads, 1) k_step_fused_tma(const FusedArgs a)
+{
+    extern __shared__ __align__(128) unsigned char tma_smem[];
+    const uint4* stages = reinterpret_cast<const uint4*>(tma_smem);   // [stage][row][consumer]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(tma_smem + kTmaStages * kTmaStageBytes);
+    const uint32_t full0 = smem_u32(bars);                // full[s] = full0 + 8 s
+    const uint32_t empty0 = smem_u32(bars + kTmaStages);  // empty[s] = empty0 + 8 s
+    const int t = threadIdx.x;
+    if (t == 0) {
+        for (int s = 0; s < kTmaStages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, kTmaConsumers);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+    const uint32_t groups = (a.nd + kTmaRows - 1) / kTmaRows;
+    const uint64_t ntiles = (a.sp.nvec + kTmaConsumers - 1) / kTmaConsumers;
+
+    if (t >= kTmaConsumers) {                             // producer warp: one thread issues
+        if (t != kTmaConsumers)
+            return;
+        const uint64_t pol = l2_evict_first();
+        const uint16_t* base = a.g + a.sp.head;
+        int stage = 0;
+        uint32_t phase = 0, armed = 0, armed_parity = 0;
+        bool ok = true;
+        for (uint64_t tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            const uint64_t q0 = tile * kTmaConsumers;
+            const uint64_t left = a.sp.nvec - q0;
+            const uint32_t bytes = (uint32_t)(left < (uint64_t)kTmaConsumers ? left : kTmaConsumers) * 16;
+            const uint16_t* src = base + 8 * q0;
+            for (uint32_t gi = 0; gi < groups; ++gi) {
+                if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, kTmaWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t j0 = gi * kTmaRows;
+                const uint32_t rows = a.nd - j0 < (uint32_t)kTmaRows ? a.nd - j0 : kTmaRows;
+                const uint32_t full = full0 + 8 * stage;
+                mbar_arrive_expect_tx(full, rows * bytes);
+                const uint32_t dst = smem_u32(stages + (size_t)stage * kTmaRows * kTmaConsumers);
+                for (uint32_t r = 0; r < rows; ++r)
+                    bulk_g2s(dst + r * kTmaRowBytes, src + (uint64_t)(j0 + r) * a.row_stride,
+                             bytes, full, pol);
+                armed |= 1u << stage;
+                armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == kTmaStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        if (!ok) {
+            atomicOr(a.flag, ZERO_STEP_FLAG_WAIT_TIMEOUT);
+            for (int s = 0; s < kTmaStages; ++s)      // copies still in flight land first
+                if ((armed >> s) & 1)
+                    (void)mbar_wait(full0 + 8 * s, (armed_parity >> s) & 1, kTmaDrainNs);
+        }
+        return;
+    }
+
+    // consumers
+    bool bad = false;
+    const uint64_t gid = (uint64_t)blockIdx.x * kTmaConsumers + t;
+    if (gid < a.sp.nscalar())
+        bad |= fused_scalar<DT>(a, a.sp.scalar_elem(gid));
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (uint64_t tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const uint64_t q = tile * kTmaConsumers + t;
+        const bool mine = q < a.sp.nvec;
+        float acc[8];
+        for (uint32_t gi = 0; gi < groups; ++gi) {
+            if (!mbar_wait(full0 + 8 * stage, phase, kTmaWaitNs)) {
+                ok = false;
+                break;
+            }
+            if (mine) {
+                const uint4* row = stages + (size_t)stage * kTmaRows * kTmaConsumers + t;
+#pragma unroll
+                for (int r = 0; r < kTmaRows; ++r) {
+                    const uint32_t j = gi * kTmaRows + r;
+                    if (j < a.nd) {
+                        const uint4 w = row[r * kTmaConsumers];
+                        if (j == 0)
+                            set8<DT>(acc, w);
+                        else
+                            add8<DT>(acc, w);
+                    }
+                }
+            }
+            mbar_arrive(empty0 + 8 * stage);
+            if (++stage == kTmaStages) {
+                stage = 0;
+                phase ^= 1;
+            }
+        }
+        if (ok && mine)
+            bad |= fused_epilogue<DT, W, V8>(a, a.sp.head + 8 * q, acc);
+    }
+    if (!ok)
+        atomicOr(a.flag, ZERO_STEP_FLAG_WAIT_TIMEOUT);
     flag_if_any(bad, a.flag);
 }
 
@@ -462,7 +609,14 @@ template <int DT, int W, bool V8>
 void launch_fused_w(const FusedArgs& a, bool host_rows, cudaStream_t s)
 {
     const uint64_t work = a.sp.nvec > a.sp.nscalar() ? a.sp.nvec : a.sp.nscalar();
-    if (ZERO_FUSED_IMPL == 1 && !host_rows) {
+    if (ZERO_FUSED_IMPL == 2 && !host_rows) {
+        cudaFuncSetAttribute(k_step_fused_tma<DT, W, V8>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmaBytes);
+        const uint64_t tiles = (a.sp.nvec + kTmaConsumers - 1) / kTmaConsumers;
+        const uint64_t cap = (uint64_t)sm_count();
+        const unsigned grid = (unsigned)(tiles < cap ? (tiles ? tiles : 1) : cap);
+        k_step_fused_tma<DT, W, V8><<<grid, kTmaThreads, kTmaBytes, s>>>(a);
+    } else if (ZERO_FUSED_IMPL >= 1 && !host_rows) {
         // one resident CTA per SM; the ring needs the opt-in shared memory
         // size (a per-device function attribute, so set on every launch)
         cudaFuncSetAttribute(k_step_fused_ring<DT, W, V8>,

@@ -37,13 +37,6 @@ __device__ __forceinline__ uint16_t ld_grad2_cg(const uint16_t* p)
     return __ldcg(reinterpret_cast<const unsigned short*>(p));
 }
 
-__device__ __forceinline__ uint64_t global_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p)
 {
     uint32_t v;

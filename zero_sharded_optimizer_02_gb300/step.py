@@ -200,7 +200,7 @@ class DataParallelStep:
         with torch.cuda.stream(self.stream):
             self.flag_host.copy_(self.flag, non_blocking=True)
         self.stream.synchronize()
-        bad = int(self.flag_host[0]) != 0
+        bad = _abi.check_step_flag(self.flag_host[0])
         return global_skip(bad, self.pg, self.device)
 
     def commit(self, skipped: bool) -> None:
@@ -388,7 +388,7 @@ class PipelinedStep(DataParallelStep):
     def _decide_oldest(self) -> bool:
         out_buf, t, slot, ev, grads = self.pending.pop(0)
         ev.synchronize()
-        bad = int(self.flags_host[slot]) != 0
+        bad = _abi.check_step_flag(self.flags_host[slot])
         skipped = global_skip(bad, self.pg, self.device)
         self.skipped_steps.append(skipped)
         if not skipped:
