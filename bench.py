@@ -50,8 +50,12 @@ def measured_peaks() -> dict:
 
 
 def kernel_name() -> str:
-    flags = os.environ.get("ZERO_NVCC_FLAGS", "")
-    return "k_step_fused_ring" if "ZERO_FUSED_IMPL=0" not in flags else "k_step_fused"
+    """The fused-step kernel the build runs (ZERO_FUSED_IMPL: 0 registers,
+    1 cp.async ring (default), 2 bulk copies)."""
+    import re
+    m = re.search(r"ZERO_FUSED_IMPL=(\d)", os.environ.get("ZERO_NVCC_FLAGS", ""))
+    impl = int(m.group(1)) if m else 1
+    return {0: "k_step_fused", 2: "k_step_fused_tma"}.get(impl, "k_step_fused_ring")
 
 
 def kernel_source_hash() -> str:

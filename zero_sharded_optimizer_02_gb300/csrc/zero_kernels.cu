@@ -104,10 +104,11 @@ constexpr size_t kRingBytes = (size_t)kRingDepth * kRingRows * kRingThreads * 16
 static_assert(kRingBytes <= 227 * 1024, "ring exceeds shared memory");
 
 // Fused step, bulk-copy variant (ZERO_FUSED_IMPL 2): a producer warp streams
-// each tile's rows into a kTmaStages-deep ring of shared-memory stages with
-// cp.async.bulk (one copy per rank row, completion counted on the stage's
-// mbarrier); kTmaConsumers consumer threads fold them, one 8-element vector
-// each per tile.
+// each tile's fp32 state (master, m, v) into a 2-slot ring and its rank rows
+// into a kTmaStages-deep ring of shared-memory stages, with cp.async.bulk
+// (completion counted on each slot's mbarrier); kTmaConsumers consumer
+// threads fold the rows, one 8-element vector each per tile, and run the
+// epilogue from the staged state.
 #ifndef ZERO_TMA_CONSUMERS
 #define ZERO_TMA_CONSUMERS 256
 #endif
@@ -121,14 +122,18 @@ constexpr int kTmaConsumers = ZERO_TMA_CONSUMERS;
 constexpr int kTmaThreads = kTmaConsumers + 32;          // + the producer warp
 constexpr int kTmaRows = ZERO_TMA_ROWS;                  // rank rows per stage
 constexpr int kTmaStages = ZERO_TMA_STAGES;
+constexpr int kTmaStateSlots = 2;
 constexpr uint32_t kTmaRowBytes = kTmaConsumers * 16;    // one row of one tile
 constexpr size_t kTmaStageBytes = (size_t)kTmaRows * kTmaRowBytes;
-constexpr size_t kTmaBytes = kTmaStages * kTmaStageBytes + 2 * kTmaStages * sizeof(uint64_t);
+constexpr uint32_t kTmaStateArrayBytes = kTmaConsumers * 32;   // 8 floats a consumer
+constexpr size_t kTmaStateSlotBytes = 3 * (size_t)kTmaStateArrayBytes;
+constexpr size_t kTmaBarOffset = kTmaStages * kTmaStageBytes + kTmaStateSlots * kTmaStateSlotBytes;
+constexpr size_t kTmaBytes =
+    kTmaBarOffset + 2 * (kTmaStages + kTmaStateSlots) * sizeof(uint64_t);
 static_assert(kTmaConsumers % 32 == 0 && kTmaStages <= 32, "TMA pipeline shape");
-static_assert(kTmaBytes <= 227 * 1024, "TMA ring exceeds shared memory");
-static_assert((size_t)kTmaRows * kTmaRowBytes < (1u << 20), "stage exceeds an mbarrier phase");
-// Longest wait on a pipeline barrier before the kernel gives up (a healthy
-// wait lasts microseconds), and on each in-flight copy after giving up.
+static_assert(kTmaBytes <= 227 * 1024, "TMA rings exceed shared memory");
+static_assert(kTmaStageBytes < (1u << 20) && kTmaStateSlotBytes < (1u << 20),
+              "a slot exceeds an mbarrier phase");
 constexpr uint64_t kTmaWaitNs = 10ull * 1000 * 1000 * 1000;
 constexpr uint64_t kTmaDrainNs = 1000ull * 1000 * 1000;
 
@@ -236,29 +241,75 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_step_fused_ring(const Fused
     flag_if_any(bad, a.flag);
 }
 
+// Epilogue of the bulk-copy variant: the state of the 8 elements at e was
+// staged in shared memory; the new state leaves with streaming stores
+// (32-byte when V8, else two 16-byte halves).  Returns "any sum nonfinite".
+template <int DT, int W, bool V8>
+__device__ __forceinline__ bool tma_epilogue(const FusedArgs& a, uint64_t e, const float (&s)[8],
+                                             float (&p)[8], float (&m)[8], float (&v)[8])
+{
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        bad |= nonfinite(s[i]);
+        adamw1(a.k, __fmul_rn(s[i], a.k.inv), p[i], m[i], v[i]);
+    }
+    if (V8) {
+        st8_cs(a.p_out + e, p);
+        st8_cs(a.m_out + e, m);
+        st8_cs(a.v_out + e, v);
+    } else {
+        float* outs[3] = {a.p_out + e, a.m_out + e, a.v_out + e};
+        const float* vals[3] = {p, m, v};
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            __stcs(reinterpret_cast<float4*>(outs[k]),
+                   make_float4(vals[k][0], vals[k][1], vals[k][2], vals[k][3]));
+            __stcs(reinterpret_cast<float4*>(outs[k]) + 1,
+                   make_float4(vals[k][4], vals[k][5], vals[k][6], vals[k][7]));
+        }
+    }
+    uint32_t out16[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        out16[i] = (uint32_t)narrow1<DT>(p[2 * i]) | ((uint32_t)narrow1<DT>(p[2 * i + 1]) << 16);
+    store8<W>(a.gath + e, out16);
+    return bad;
+}
+
 // K4, bulk-copy variant.  Tiles of kTmaConsumers vectors are dealt to the
 // CTAs round robin, so the grid moves through the rows together.  For each
-// tile the producer thread copies row groups of kTmaRows rows into the ring
-// (a stage is free once all consumers arrived on its "empty" barrier; its
-// "full" barrier completes when the copies' bytes have landed).  Consumers
-// fold the rows in rank order, release the stage, and after the last group
-// run the epilogue of their vector with 256-bit state accesses.  Every
-// barrier wait is bounded: on expiry ZERO_STEP_FLAG_WAIT_TIMEOUT is set in the
-// flag word, the producer waits (bounded) for the copies it issued, and the
-// CTA ends.
+// tile the producer thread first copies the tile's master, m and v into a
+// state slot, then its rank rows, kTmaRows at a time, into the stage ring.  A
+// slot or stage is refilled once all consumers arrived on its "empty"
+// barrier; its "full" barrier completes when the copies' bytes have landed.
+// Consumers fold the rows in rank order and release each stage, then take
+// their vector's state from the slot, release it, and store the new state
+// (256-bit streaming stores when 32-byte aligned) and the cast parameters.
+// Every barrier wait is bounded: on expiry ZERO_STEP_FLAG_WAIT_TIMEOUT is set
+// in the flag word, the producer waits (bounded) for the copies it issued,
+// and the CTA ends.
 template <int DT, int W, bool V8>
 __global__ void __launch_bounds__(kTmaThreads, 1) k_step_fused_tma(const FusedArgs a)
 {
     extern __shared__ __align__(128) unsigned char tma_smem[];
     const uint4* stages = reinterpret_cast<const uint4*>(tma_smem);   // [stage][row][consumer]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(tma_smem + kTmaStages * kTmaStageBytes);
-    const uint32_t full0 = smem_u32(bars);                // full[s] = full0 + 8 s
-    const uint32_t empty0 = smem_u32(bars + kTmaStages);  // empty[s] = empty0 + 8 s
+    const float* slots =                                              // [slot][array][consumer][8]
+        reinterpret_cast<const float*>(tma_smem + kTmaStages * kTmaStageBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(tma_smem + kTmaBarOffset);
+    const uint32_t full0 = smem_u32(bars);                                    // + 8 s
+    const uint32_t empty0 = smem_u32(bars + kTmaStages);                      // + 8 s
+    const uint32_t sfull0 = smem_u32(bars + 2 * kTmaStages);                  // + 8 slot
+    const uint32_t sempty0 = smem_u32(bars + 2 * kTmaStages + kTmaStateSlots);
     const int t = threadIdx.x;
     if (t == 0) {
         for (int s = 0; s < kTmaStages; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, kTmaConsumers);
+        }
+        for (int s = 0; s < kTmaStateSlots; ++s) {
+            mbar_init(sfull0 + 8 * s, 1);
+            mbar_init(sempty0 + 8 * s, kTmaConsumers);
         }
         mbar_fence_init();
     }
@@ -271,13 +322,34 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_step_fused_tma(const FusedAr
             return;
         const uint64_t pol = l2_evict_first();
         const uint16_t* base = a.g + a.sp.head;
-        int stage = 0;
-        uint32_t phase = 0, armed = 0, armed_parity = 0;
+        const float* state_in[3] = {a.p_in + a.sp.head, a.m_in + a.sp.head, a.v_in + a.sp.head};
+        int stage = 0, slot = 0;
+        uint32_t phase = 0, sphase = 0;
+        uint32_t armed = 0, armed_parity = 0, sarmed = 0, sarmed_parity = 0;
         bool ok = true;
         for (uint64_t tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
             const uint64_t q0 = tile * kTmaConsumers;
             const uint64_t left = a.sp.nvec - q0;
-            const uint32_t bytes = (uint32_t)(left < (uint64_t)kTmaConsumers ? left : kTmaConsumers) * 16;
+            const uint32_t nv = (uint32_t)(left < (uint64_t)kTmaConsumers ? left : kTmaConsumers);
+            // the tile's state
+            if (!mbar_wait(sempty0 + 8 * slot, sphase ^ 1, kTmaWaitNs)) {
+                ok = false;
+                break;
+            }
+            const uint32_t sfull = sfull0 + 8 * slot;
+            mbar_arrive_expect_tx(sfull, 3 * nv * 32);
+            const uint32_t sdst = smem_u32(slots + (size_t)slot * 3 * kTmaConsumers * 8);
+            for (int k = 0; k < 3; ++k)
+                bulk_g2s(sdst + k * kTmaStateArrayBytes, state_in[k] + 8 * q0, nv * 32, sfull,
+                         pol);
+            sarmed |= 1u << slot;
+            sarmed_parity = (sarmed_parity & ~(1u << slot)) | (sphase << slot);
+            if (++slot == kTmaStateSlots) {
+                slot = 0;
+                sphase ^= 1;
+            }
+            // its rank rows
+            const uint32_t bytes = nv * 16;
             const uint16_t* src = base + 8 * q0;
             for (uint32_t gi = 0; gi < groups; ++gi) {
                 if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, kTmaWaitNs)) {
@@ -305,6 +377,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_step_fused_tma(const FusedAr
             for (int s = 0; s < kTmaStages; ++s)      // copies still in flight land first
                 if ((armed >> s) & 1)
                     (void)mbar_wait(full0 + 8 * s, (armed_parity >> s) & 1, kTmaDrainNs);
+            for (int s = 0; s < kTmaStateSlots; ++s)
+                if ((sarmed >> s) & 1)
+                    (void)mbar_wait(sfull0 + 8 * s, (sarmed_parity >> s) & 1, kTmaDrainNs);
         }
         return;
     }
@@ -314,8 +389,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_step_fused_tma(const FusedAr
     const uint64_t gid = (uint64_t)blockIdx.x * kTmaConsumers + t;
     if (gid < a.sp.nscalar())
         bad |= fused_scalar<DT>(a, a.sp.scalar_elem(gid));
-    int stage = 0;
-    uint32_t phase = 0;
+    int stage = 0, slot = 0;
+    uint32_t phase = 0, sphase = 0;
     bool ok = true;
     for (uint64_t tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
         const uint64_t q = tile * kTmaConsumers + t;
@@ -346,8 +421,28 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_step_fused_tma(const FusedAr
                 phase ^= 1;
             }
         }
-        if (ok && mine)
-            bad |= fused_epilogue<DT, W, V8>(a, a.sp.head + 8 * q, acc);
+        if (!ok || !mbar_wait(sfull0 + 8 * slot, sphase, kTmaWaitNs)) {
+            ok = false;
+            break;
+        }
+        float st[3][8];
+        if (mine) {
+            const float* sl = slots + (size_t)slot * 3 * kTmaConsumers * 8 + 8 * t;
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+                const float4 lo = *reinterpret_cast<const float4*>(sl + k * kTmaConsumers * 8);
+                const float4 hi = *reinterpret_cast<const float4*>(sl + k * kTmaConsumers * 8 + 4);
+                st[k][0] = lo.x, st[k][1] = lo.y, st[k][2] = lo.z, st[k][3] = lo.w;
+                st[k][4] = hi.x, st[k][5] = hi.y, st[k][6] = hi.z, st[k][7] = hi.w;
+            }
+        }
+        mbar_arrive(sempty0 + 8 * slot);
+        if (++slot == kTmaStateSlots) {
+            slot = 0;
+            sphase ^= 1;
+        }
+        if (mine)
+            bad |= tma_epilogue<DT, W, V8>(a, a.sp.head + 8 * q, acc, st[0], st[1], st[2]);
     }
     if (!ok)
         atomicOr(a.flag, ZERO_STEP_FLAG_WAIT_TIMEOUT);
