@@ -50,12 +50,16 @@ def measured_peaks() -> dict:
 
 
 def kernel_name() -> str:
-    """The fused-step kernel the build runs (ZERO_FUSED_IMPL: 0 registers,
-    1 cp.async ring (default), 2 bulk copies)."""
+    """The fused-step kernel the run uses: ZERO_FUSED_VARIANT if set, else the
+    build's ZERO_FUSED_IMPL (0 registers, 1 cp.async ring (default), 2 bulk
+    copies)."""
     import re
+    names = {0: "k_step_fused", 1: "k_step_fused_ring", 2: "k_step_fused_tma"}
+    v = os.environ.get("ZERO_FUSED_VARIANT")
+    if v in ("registers", "ring", "tma"):
+        return names[{"registers": 0, "ring": 1, "tma": 2}[v]]
     m = re.search(r"ZERO_FUSED_IMPL=(\d)", os.environ.get("ZERO_NVCC_FLAGS", ""))
-    impl = int(m.group(1)) if m else 1
-    return {0: "k_step_fused", 2: "k_step_fused_tma"}.get(impl, "k_step_fused_ring")
+    return names.get(int(m.group(1)) if m else 1, "k_step_fused_ring")
 
 
 def kernel_source_hash() -> str:
@@ -87,6 +91,8 @@ def recorded_traffic(workload: str):
     if kv.get("kernel_source_sha256_16") != kernel_source_hash():
         return None
     if kv.get("build_flags", "") != os.environ.get("ZERO_NVCC_FLAGS", ""):
+        return None
+    if kernel_name() != "k_step_fused_ring":      # recorded for the default kernel
         return None
     v = kv.get(f"dram_bytes_per_param.{workload}")
     return None if v is None else float(v)
@@ -707,6 +713,8 @@ def main():
                     help="step (the benchmark line) or a measurement of another entry point")
     ap.add_argument("--config", default="c4", choices=["c0", "c1", "c2", "c3", "c4"])
     ap.add_argument("--rank", type=int, default=0, help="first data-parallel rank to run")
+    ap.add_argument("--variant", choices=["registers", "ring", "tma"], default=None,
+                    help="fused-step kernel (sets ZERO_FUSED_VARIANT; default: the ring)")
     ap.add_argument("--gathered", choices=["slot", "full"], default="slot",
                     help="slot: the rank's own S-element parameter buffer; full: its slot at "
                          "r*S of the flat Nd*S buffer (odd ranks then start off the 16-byte "
@@ -729,6 +737,8 @@ def main():
         ap.error("at least 3 warm-up steps")
     if args.row_pad % 8:
         ap.error("--row-pad must be a multiple of 8 elements")
+    if args.variant:
+        os.environ["ZERO_FUSED_VARIANT"] = args.variant
     if args.impl == "reference":
         run_reference(args)
     elif args.op == "gather":

@@ -138,3 +138,40 @@ def sample_indices(psi: int, nd: int, ranks, per_rank: int, seed: int, extra=())
             out.add(b + n - 1 - d)
         out.update(int(x) for x in b + rng.integers(0, n, per_rank))
     return np.array(sorted(out), np.int64)
+
+
+# -- whole-group checks ------------------------------------------------------
+
+EDGE_CASES = [
+    # (psi, nd, dtype, bucket): ragged tails, psi < nd, nd = 1, odd slot phases
+    (1000, 3, "bf16", 64),
+    (1001, 7, "f16", 1),         # one launch per element
+    (3, 5, "f16", 7),            # psi < nd: empty shards
+    (4099, 1, "bf16", 1000),     # one rank: plain data parallel
+    (70_001, 16, "f16", 7),      # S mod 8 = 3: every slot phase
+    (130_003, 64, "bf16", 2049), # 64 ranks, S mod 8 = 4
+    (250_000, 2, "f16", 250_000),
+]
+
+
+def check_against_oracle(w, dps, history_entry, what):
+    """The group's whole state, gathered parameters and t against one oracle
+    step, and nothing written outside the shards."""
+    p, m, v, params, t = history_entry
+    gp, gm, gv = flat_state(dps)
+    assert_state_close(gp, p, 1e-12, f"{what} master")
+    assert_state_close(gm, m, 1e-20, f"{what} m")
+    assert_state_close(gv, v, 1e-20, f"{what} v")
+    if params is not None:
+        got = u16(dps.gathered_view()[:dps.psi])
+        assert_params_close(got, params, f"{what} params")
+    assert dps.t == t
+    # nothing written outside the shards: padding of the gathered buffer and
+    # the state rows past each shard's length stay zero
+    s = int(dps.layouts[0].shard_elems)
+    assert not dps.gathered_view()[dps.psi:].view(torch.int16).any(), f"{what} gathered pad"
+    for r in dps.ranks:
+        st = dps.state[r]
+        n = int(dps.layouts[r].length)
+        for b in st.bufs:
+            assert not b[:, n:].any(), f"{what} state pad rank {r}"

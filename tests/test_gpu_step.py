@@ -15,8 +15,9 @@ import torch
 import oracle
 import synth
 import zero_sharded_optimizer_02_gb300 as z
-from gpu_util import (DEV, DT_CODE, TORCH_DT, assert_params_close, assert_state_close, f32,
-                      flat_state, full_rows, make_group, oracle_trajectory, shard_rows, u16)
+from gpu_util import (DEV, DT_CODE, EDGE_CASES, TORCH_DT, assert_params_close,
+                      assert_state_close, check_against_oracle, f32, flat_state, full_rows,
+                      make_group, oracle_trajectory, shard_rows, u16)
 
 pytestmark = pytest.mark.gpu
 
@@ -27,27 +28,6 @@ def built():
     build.build()
     oracle.build()
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
-
-
-def _check_against_oracle(w, dps, history_entry, what):
-    p, m, v, params, t = history_entry
-    gp, gm, gv = flat_state(dps)
-    assert_state_close(gp, p, 1e-12, f"{what} master")
-    assert_state_close(gm, m, 1e-20, f"{what} m")
-    assert_state_close(gv, v, 1e-20, f"{what} v")
-    if params is not None:
-        got = u16(dps.gathered_view()[:dps.psi])
-        assert_params_close(got, params, f"{what} params")
-    assert dps.t == t
-    # nothing written outside the shards: padding of the gathered buffer and
-    # the state rows past each shard's length stay zero
-    s = int(dps.layouts[0].shard_elems)
-    assert not dps.gathered_view()[dps.psi:].view(torch.int16).any(), f"{what} gathered pad"
-    for r in dps.ranks:
-        st = dps.state[r]
-        n = int(dps.layouts[r].length)
-        for b in st.bufs:
-            assert not b[:, n:].any(), f"{what} state pad rank {r}"
 
 
 def test_generator_identical_on_device():
@@ -74,19 +54,9 @@ def test_c0_full_emulation_matches_unsharded_oracle(fused):
     for k in range(w.steps):
         buf, desc = full_rows(w, dps, k, buf)
         assert not dps.step(desc)
-        _check_against_oracle(w, dps, hist[k], f"c0 step {k} fused={fused}")
+        check_against_oracle(w, dps, hist[k], f"c0 step {k} fused={fused}")
 
 
-EDGE_CASES = [
-    # (psi, nd, dtype, bucket): ragged tails, psi < nd, nd = 1, odd slot phases
-    (1000, 3, "bf16", 64),
-    (1001, 7, "f16", 1),         # one launch per element
-    (3, 5, "f16", 7),            # psi < nd: empty shards
-    (4099, 1, "bf16", 1000),     # one rank: plain data parallel
-    (70_001, 16, "f16", 7),      # S mod 8 = 3: every slot phase
-    (130_003, 64, "bf16", 2049), # 64 ranks, S mod 8 = 4
-    (250_000, 2, "f16", 250_000),
-]
 
 
 @pytest.mark.parametrize("psi,nd,dt,bucket", EDGE_CASES)
@@ -100,7 +70,7 @@ def test_edge_shapes(psi, nd, dt, bucket, fused):
     for k in range(2):
         buf, desc = full_rows(w, dps, k, buf)
         assert not dps.step(desc)
-        _check_against_oracle(dataclasses.replace(w, psi=psi, nd=nd), dps, hist[k],
+        check_against_oracle(dataclasses.replace(w, psi=psi, nd=nd), dps, hist[k],
                               f"psi={psi} nd={nd} step {k}")
 
 
@@ -150,7 +120,7 @@ def test_global_skip_keeps_everything(fused):
             rows[7, 7 * s + s // 2] = 0x7C00
         tr.step(rows)
     assert tr.skipped == [False, True, False]
-    _check_against_oracle(w, dps, (tr.p, tr.m, tr.v, tr.params, tr.t), "after skip")
+    check_against_oracle(w, dps, (tr.p, tr.m, tr.v, tr.params, tr.t), "after skip")
 
 
 def test_in_place_with_precheck():

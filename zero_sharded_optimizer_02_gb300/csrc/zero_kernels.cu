@@ -21,6 +21,8 @@
 // 0..Nd-1.  Warp votes are used only for the nonfinite flag.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include <atomic>
 
@@ -70,7 +72,10 @@ constexpr int kCtasPerSmLight = 8;
 // Fused step variant: 0 = rows loaded into registers; 1 = rows staged through
 // a per-thread cp.async ring in shared memory (kRingDepth groups of
 // kRingRows rows of 16 bytes a thread), which keeps more bytes in flight per
-// SM than the register file allows.
+// SM than the register file allows; 2 = rows and state staged by bulk
+// copies.  The environment variable ZERO_FUSED_VARIANT ("registers", "ring",
+// "tma"), read at each call, overrides this default; every variant gives
+// bitwise the same results.
 #ifndef ZERO_FUSED_IMPL
 #define ZERO_FUSED_IMPL 1
 #endif
@@ -697,21 +702,37 @@ int sm_count()
     return sms;
 }
 
-// The ring kernel streams HBM-resident rows best.  Rows read in place from
-// host memory go to the register kernel, whose loads keep the host link
-// busier (about 203 against 183 GB/s on the 7.5B shard's 64 rows).
+// The fused-step variant of a call: ZERO_FUSED_VARIANT if set, else the
+// build's default.  The ring kernel streams HBM-resident rows best.  Rows
+// read in place from host memory always go to the register kernel, whose
+// loads keep the host link busier (about 203 against 183 GB/s on the 7.5B
+// shard's 64 rows).
+int fused_variant(bool host_rows)
+{
+    if (host_rows)
+        return 0;
+    const char* v = getenv("ZERO_FUSED_VARIANT");
+    if (v && strcmp(v, "registers") == 0)
+        return 0;
+    if (v && strcmp(v, "ring") == 0)
+        return 1;
+    if (v && strcmp(v, "tma") == 0)
+        return 2;
+    return ZERO_FUSED_IMPL;
+}
+
 template <int DT, int W, bool V8>
-void launch_fused_w(const FusedArgs& a, bool host_rows, cudaStream_t s)
+void launch_fused_w(const FusedArgs& a, int variant, cudaStream_t s)
 {
     const uint64_t work = a.sp.nvec > a.sp.nscalar() ? a.sp.nvec : a.sp.nscalar();
-    if (ZERO_FUSED_IMPL == 2 && !host_rows) {
+    if (variant == 2) {
         cudaFuncSetAttribute(k_step_fused_tma<DT, W, V8>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmaBytes);
         const uint64_t tiles = (a.sp.nvec + kTmaConsumers - 1) / kTmaConsumers;
         const uint64_t cap = (uint64_t)sm_count();
         const unsigned grid = (unsigned)(tiles < cap ? (tiles ? tiles : 1) : cap);
         k_step_fused_tma<DT, W, V8><<<grid, kTmaThreads, kTmaBytes, s>>>(a);
-    } else if (ZERO_FUSED_IMPL >= 1 && !host_rows) {
+    } else if (variant == 1) {
         // one resident CTA per SM; the ring needs the opt-in shared memory
         // size (a per-device function attribute, so set on every launch)
         cudaFuncSetAttribute(k_step_fused_ring<DT, W, V8>,
@@ -726,23 +747,23 @@ void launch_fused_w(const FusedArgs& a, bool host_rows, cudaStream_t s)
 }
 
 template <int DT, bool V8>
-void launch_fused_v(const FusedArgs& a, int width, bool host_rows, cudaStream_t s)
+void launch_fused_v(const FusedArgs& a, int width, int variant, cudaStream_t s)
 {
     switch (width) {
-    case 16: launch_fused_w<DT, 16, V8>(a, host_rows, s); break;
-    case 8: launch_fused_w<DT, 8, V8>(a, host_rows, s); break;
-    case 4: launch_fused_w<DT, 4, V8>(a, host_rows, s); break;
-    default: launch_fused_w<DT, 2, V8>(a, host_rows, s); break;
+    case 16: launch_fused_w<DT, 16, V8>(a, variant, s); break;
+    case 8: launch_fused_w<DT, 8, V8>(a, variant, s); break;
+    case 4: launch_fused_w<DT, 4, V8>(a, variant, s); break;
+    default: launch_fused_w<DT, 2, V8>(a, variant, s); break;
     }
 }
 
 template <int DT>
-void launch_fused_dt(const FusedArgs& a, int width, bool v8, bool host_rows, cudaStream_t s)
+void launch_fused_dt(const FusedArgs& a, int width, bool v8, int variant, cudaStream_t s)
 {
     if (v8)
-        launch_fused_v<DT, true>(a, width, host_rows, s);
+        launch_fused_v<DT, true>(a, width, variant, s);
     else
-        launch_fused_v<DT, false>(a, width, host_rows, s);
+        launch_fused_v<DT, false>(a, width, variant, s);
 }
 
 void launch_reduce(const ReduceArgs& a, int dtype, cudaStream_t s)
@@ -937,6 +958,7 @@ extern "C" zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layou
     st = resolve_grads(g, &gr, &host_rows);
     if (st != ZERO_OK)
         return st;
+    const int variant = fused_variant(host_rows);
     const StepScalars k = make_scalars(h, g->nd, loss_scale);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const uint16_t* rows = static_cast<const uint16_t*>(gr.base) + g->offset;
@@ -962,9 +984,9 @@ extern "C" zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layou
                         out->v + e0, gath + e0, k, d_nonfinite};
             const int width = store_width(gath + e0 + a.sp.head);
             if (g->dtype == ZERO_F16)
-                launch_fused_dt<ZERO_F16>(a, width, v8, host_rows, s);
+                launch_fused_dt<ZERO_F16>(a, width, v8, variant, s);
             else
-                launch_fused_dt<ZERO_BF16>(a, width, v8, host_rows, s);
+                launch_fused_dt<ZERO_BF16>(a, width, v8, variant, s);
             st = launch_status();
             if (st != ZERO_OK)
                 return st;
