@@ -115,13 +115,13 @@ static_assert(kRingBytes <= 227 * 1024, "ring exceeds shared memory");
 // threads fold the rows, one 8-element vector each per tile, and run the
 // epilogue from the staged state.
 #ifndef ZERO_TMA_CONSUMERS
-#define ZERO_TMA_CONSUMERS 256
+#define ZERO_TMA_CONSUMERS 512
 #endif
 #ifndef ZERO_TMA_ROWS
-#define ZERO_TMA_ROWS 8
+#define ZERO_TMA_ROWS 4
 #endif
 #ifndef ZERO_TMA_STAGES
-#define ZERO_TMA_STAGES 5
+#define ZERO_TMA_STAGES 4
 #endif
 constexpr int kTmaConsumers = ZERO_TMA_CONSUMERS;
 constexpr int kTmaThreads = kTmaConsumers + 32;          // + the producer warp
