@@ -236,10 +236,11 @@ def run_gpu(args) -> None:
         pipe.state[dp_rank].bufs[0].copy_(st.bufs[st.cur])
     torch.cuda.synchronize(dev)
 
-    # -- warm-up, then K timed steps.  The pipelined driver launches step k+1
-    #    before it reads step k's flag (a skip re-runs the speculative step),
-    #    so the GPU never waits for the host; every step is the whole path:
-    #    fused kernel, flag read, commit or global skip. -----------------------
+    # -- warm-up, then K timed steps.  The pipelined driver launches up to two
+    #    steps ahead of the oldest undecided step's flag read (a skip re-runs
+    #    the speculative steps), so the GPU never waits for the host; every
+    #    step is the whole path: fused kernels, flag read, commit or global
+    #    skip. -----------------------------------------------------------------
     for _ in range(args.warmup):
         pipe.launch(desc)
     pipe.finish()
@@ -464,7 +465,8 @@ def run_gpu(args) -> None:
                      "algorithmic_bytes_per_launch": launch_bytes},
         "e2e": e2e,
         "gpu_launches": launches,
-        "driver": "pipelined (step k+1 launched before step k's flag is read)",
+        "driver": f"pipelined (up to {pipe.depth} steps launched ahead of the oldest "
+                  f"undecided step's flag read)",
         "ms_per_step_sync_driver": sync_ms,
         "build_flags": os.environ.get("ZERO_NVCC_FLAGS", ""),
         "skipped_steps": skipped,

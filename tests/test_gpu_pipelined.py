@@ -1,7 +1,7 @@
-"""The pipelined driver (speculative launch of step k+1 before step k's
-flag is read) reproduces the plain driver bit for bit, including a global
-skip in the middle of the sequence, which forces the speculative step to be
-discarded and run again."""
+"""The pipelined driver (speculative launch of up to `depth` steps before the
+oldest one's flag is read) reproduces the plain driver bit for bit,
+including a global skip in the middle of the sequence, which forces the
+speculative steps to be discarded and run again."""
 import dataclasses
 
 import pytest
@@ -21,14 +21,15 @@ def built():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
 
 
+@pytest.mark.parametrize("depth", [1, 2, 3])
 @pytest.mark.parametrize("skip_at", [None, 0, 3, 5])
-def test_pipelined_equals_plain(skip_at):
+def test_pipelined_equals_plain(skip_at, depth):
     w = dataclasses.replace(synth.WORKLOADS["c0"], psi=300_007, nd=8, plant=None,
                             fresh_grads=True)
     steps = 6
     plain = make_group(w, gathered="full", bucket=40_000)
     pipe = PipelinedStep(w.psi, w.nd, range(w.nd), w.grad_dtype, w.hparams, w.loss_scale,
-                         40_000, DEV, gathered="full")
+                         40_000, DEV, gathered="full", depth=depth)
     for r in range(w.nd):
         pipe.state[r].bufs[0].copy_(plain.state[r].bufs[plain.state[r].cur])
     pitch = int(plain.layouts[0].row_pitch)

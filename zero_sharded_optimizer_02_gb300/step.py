@@ -305,52 +305,55 @@ class DataParallelStep:
 class PipelinedStep(DataParallelStep):
     """DataParallelStep whose host never stalls the GPU between steps.
 
-    Step k+1 is launched on step k's output before the host has read step
-    k's nonfinite flag (speculating that k commits); the host then waits only
-    for step k's flag.  State and parameters are triple-buffered (committed,
-    step k's output, step k+1's output) and the flag alternates between two
-    words.  If step k turns out to be skipped, the committed state stays, the
-    speculative step k+1 is discarded and run again from the committed state,
-    so every step's result and the skip rule are exactly those of
-    DataParallelStep.  The flag words are copied to the host on a side stream
-    after each step's kernels, so consecutive steps' kernels run back to back.
-    Gradient buffers must stay unchanged until the step that reads them has
-    been decided.
+    Up to ``depth`` steps are launched ahead of the last decided one, each on
+    its predecessor's output (speculating that every undecided step commits);
+    the host waits only for the oldest undecided step's flag.  State and
+    parameters need depth + 2 buffers (committed, and one per step in
+    flight), and the flag alternates between depth + 1 words.  If a step
+    turns out to be skipped, the committed state stays, the speculative steps
+    built on it are discarded and run again from the committed state, so
+    every step's result and the skip rule are exactly those of
+    DataParallelStep.  The flag words are copied to the host on a side
+    stream after each step's kernels, so consecutive steps' kernels run back
+    to back, and depth 2 leaves the host a whole step of slack.  Gradient
+    buffers must stay unchanged until the step that reads them has been
+    decided.
 
     Use: ``launch(grads)`` for each step, then ``finish()`` once; both return
     the decided steps' skip flags in order.
     """
 
-    def __init__(self, *args, **kwargs):
+    def __init__(self, *args, depth: int = 2, **kwargs):
         kwargs.setdefault("gathered", "slot")
         super().__init__(*args, **kwargs)
+        if depth < 1:
+            raise ValueError("depth must be at least 1")
+        self.depth = depth
+        nbuf = depth + 2
         for r in self.ranks:
             old = self.state[r]
-            self.state[r] = RankState(self.layouts[r], self.device, nbuf=3)
+            self.state[r] = RankState(self.layouts[r], self.device, nbuf=nbuf)
             self.state[r].bufs[0].copy_(old.bufs[old.cur])
             self.state[r].states = [_abi.state(b[0], b[1], b[2]) for b in self.state[r].bufs]
-        if self.gathered_mode == "full":
-            self.gathered.append(torch.zeros_like(self.gathered[0]))
-        elif self.gathered_mode == "pitched":
-            self.gathered.append(torch.zeros_like(self.gathered[0]))
-        else:
-            self.gathered.append({r: torch.zeros_like(t) for r, t in self.gathered[0].items()})
-        self.gathered[0], self.gathered[self.gcur] = self.gathered[self.gcur], self.gathered[0]
+        cur = self.gathered[self.gcur]
+        self.gathered = [cur] + [
+            torch.zeros_like(cur) if self.gathered_mode in ("full", "pitched") else
+            {r: torch.zeros_like(t) for r, t in cur.items()} for _ in range(nbuf - 1)]
         self.gcur = 0
-        self.flags = torch.zeros(2, dtype=torch.int32, device=self.device)
-        self.flags_host = torch.zeros(2, dtype=torch.int32, pin_memory=True)
+        self.flags = torch.zeros(depth + 1, dtype=torch.int32, device=self.device)
+        self.flags_host = torch.zeros(depth + 1, dtype=torch.int32, pin_memory=True)
         # the flag words travel to the host on a side stream, so the next
         # step's kernels never wait behind a copy
         self.flag_stream = torch.cuda.Stream(self.device)
         self.pending = []          # launched, undecided: (buf, t, flag slot, event, grads)
         self.launched = 0          # steps launched (speculative re-runs included)
-        self.kernel_launches = 0   # kernels launched (one per rank and bucket)
+        self.kernel_launches = 0   # kernels launched (one per rank and launch window)
 
     def _free_buf(self, exclude):
-        return next(i for i in range(3) if i not in exclude)
+        return next(i for i in range(self.depth + 2) if i not in exclude)
 
     def _launch_one(self, grads, in_buf, out_buf, t):
-        slot = self.launched % 2
+        slot = self.launched % (self.depth + 1)
         self.launched += 1
         for r in self.ranks:
             self.kernel_launches += _abi.fused_launch_count(int(self.layouts[r].length),
@@ -381,7 +384,7 @@ class PipelinedStep(DataParallelStep):
         out_buf = self._free_buf({self.gcur, in_buf} | {p[0] for p in self.pending})
         self._launch_one(grads, in_buf, out_buf, t_in + 1)
         decided = []
-        while len(self.pending) > 1:
+        while len(self.pending) > self.depth:
             decided.append(self._decide_oldest())
         return decided
 
