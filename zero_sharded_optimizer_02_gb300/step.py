@@ -345,6 +345,14 @@ class PipelinedStep(DataParallelStep):
         # the flag words travel to the host on a side stream, so the next
         # step's kernels never wait behind a copy
         self.flag_stream = torch.cuda.Stream(self.device)
+        # per flag word: its views and events, reused (a word is reused only
+        # after the step that used it has been decided)
+        self._flag_dev = [self.flags[i:i + 1] for i in range(depth + 1)]
+        self._flag_hst = [self.flags_host[i:i + 1] for i in range(depth + 1)]
+        self._flags_np = self.flags_host.numpy()      # the same pinned words
+        self._kernels_done = [torch.cuda.Event() for _ in range(depth + 1)]
+        self._flag_landed = [torch.cuda.Event() for _ in range(depth + 1)]
+        self._launch_counts = {}   # (rank, row offset) -> kernel launches of a step
         self.pending = []          # launched, undecided: (buf, t, flag slot, event, grads)
         self.launched = 0          # steps launched (speculative re-runs included)
         self.kernel_launches = 0   # kernels launched (one per rank and launch window)
@@ -355,22 +363,26 @@ class PipelinedStep(DataParallelStep):
     def _launch_one(self, grads, in_buf, out_buf, t):
         slot = self.launched % (self.depth + 1)
         self.launched += 1
-        for r in self.ranks:
-            self.kernel_launches += _abi.fused_launch_count(int(self.layouts[r].length),
-                                                            self.bucket, int(grads[r].offset))
+        flag = self._flag_dev[slot]
         self.h.step = t
         for r in self.ranks:
+            key = (r, int(grads[r].offset))
+            count = self._launch_counts.get(key)
+            if count is None:
+                count = _abi.fused_launch_count(int(self.layouts[r].length), self.bucket, key[1])
+                self._launch_counts[key] = count
+            self.kernel_launches += count
             st = self.state[r]
             gbuf, goff = self._gathered_target(r, out_buf)
             _abi.zero_step_shard(grads[r], self.layouts[r], st.states[in_buf],
                                  st.states[out_buf], gbuf, goff, self.bucket, self.loss_scale,
-                                 self.h, self.flags[slot:slot + 1], self.stream)
-        done = torch.cuda.Event()
+                                 self.h, flag, self.stream)
+        done = self._kernels_done[slot]
         done.record(self.stream)
         self.flag_stream.wait_event(done)
         with torch.cuda.stream(self.flag_stream):
-            self.flags_host[slot:slot + 1].copy_(self.flags[slot:slot + 1], non_blocking=True)
-        ev = torch.cuda.Event()              # this step's kernels and flag copy are done
+            self._flag_hst[slot].copy_(flag, non_blocking=True)
+        ev = self._flag_landed[slot]         # this step's kernels and flag copy are done
         ev.record(self.flag_stream)
         self.pending.append((out_buf, t, slot, ev, grads))
 
@@ -391,7 +403,7 @@ class PipelinedStep(DataParallelStep):
     def _decide_oldest(self) -> bool:
         out_buf, t, slot, ev, grads = self.pending.pop(0)
         ev.synchronize()
-        bad = _abi.check_step_flag(self.flags_host[slot])
+        bad = _abi.check_step_flag(int(self._flags_np[slot]))
         skipped = global_skip(bad, self.pg, self.device)
         self.skipped_steps.append(skipped)
         if not skipped:
