@@ -549,6 +549,27 @@ def _oracle_pool(key: str, dp_rank: int, n_per_core: int, seconds: float = 0.0,
     return params / elapsed, cores, params, elapsed
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (or the machine type if the OS does not say)."""
+    import platform
+    arm_parts = {"0xd4f": "Arm Neoverse V2", "0xd40": "Arm Neoverse V1",
+                 "0xd0c": "Arm Neoverse N1", "0xd49": "Arm Neoverse N2"}
+    part = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                key = ln.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    return ln.split(":", 1)[1].strip()
+                if key == "cpu part" and part is None:
+                    part = ln.split(":", 1)[1].strip().lower()
+    except OSError:
+        pass
+    if part:
+        return arm_parts.get(part, f"{platform.machine()} (CPU part {part})")
+    return platform.machine()
+
+
 def cpu_baseline(w, dp_rank: int, seconds: float) -> dict:
     """The oracle as it stands (plain C, one process per host core) on
     contiguous slices of this rank's shard, each core repeating its slice for
@@ -558,6 +579,7 @@ def cpu_baseline(w, dp_rank: int, seconds: float) -> dict:
     return {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{cores} processes x {n_per_core} contiguous params of rank {dp_rank}'s "
                       f"shard ({w.nd} contributions each), {params} param-steps in {el:.1f} s",
+            "per_core_value": rate / cores, "cpu_model": cpu_model(),
             "gbs": rate * w.bytes_per_param / 1e9}
 
 
@@ -585,7 +607,8 @@ def run_reference(args) -> None:
         "config": {"workload": f"{args.config}: {w.title}", "psi": w.psi, "nd": w.nd,
                    "rank": args.rank, "sample_params_per_step": params // args.steps},
         "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "per_core_value": rate / cores,
+                         "cpu_model": cpu_model()},
         "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -721,22 +721,38 @@ int fused_variant(bool host_rows)
     return ZERO_FUSED_IMPL;
 }
 
+// Opts kernel `fn` in to `bytes` of dynamic shared memory on the current
+// device, once per device (a per-device function attribute).  `done` holds a
+// bit per device id below 64; higher ids set it on every launch.
+template <typename F>
+void smem_opt_in(F* fn, size_t bytes, std::atomic<uint64_t>& done)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        dev = 64;
+    const uint64_t bit = dev < 64 ? 1ull << dev : 0;
+    if (bit && (done.load(std::memory_order_relaxed) & bit))
+        return;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) ==
+            cudaSuccess && bit)
+        done.fetch_or(bit, std::memory_order_relaxed);
+}
+
 template <int DT, int W, bool V8>
 void launch_fused_w(const FusedArgs& a, int variant, cudaStream_t s)
 {
     const uint64_t work = a.sp.nvec > a.sp.nscalar() ? a.sp.nvec : a.sp.nscalar();
     if (variant == 2) {
-        cudaFuncSetAttribute(k_step_fused_tma<DT, W, V8>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmaBytes);
+        static std::atomic<uint64_t> opted{0};
+        smem_opt_in(k_step_fused_tma<DT, W, V8>, kTmaBytes, opted);
         const uint64_t tiles = (a.sp.nvec + kTmaConsumers - 1) / kTmaConsumers;
         const uint64_t cap = (uint64_t)sm_count();
         const unsigned grid = (unsigned)(tiles < cap ? (tiles ? tiles : 1) : cap);
         k_step_fused_tma<DT, W, V8><<<grid, kTmaThreads, kTmaBytes, s>>>(a);
     } else if (variant == 1) {
-        // one resident CTA per SM; the ring needs the opt-in shared memory
-        // size (a per-device function attribute, so set on every launch)
-        cudaFuncSetAttribute(k_step_fused_ring<DT, W, V8>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingBytes);
+        // one resident CTA per SM; the ring needs the opt-in shared memory size
+        static std::atomic<uint64_t> opted{0};
+        smem_opt_in(k_step_fused_ring<DT, W, V8>, kRingBytes, opted);
         const uint64_t want = (work + kRingThreads - 1) / kRingThreads;
         const uint64_t cap = (uint64_t)sm_count();
         const unsigned grid = (unsigned)(want < cap ? (want ? want : 1) : cap);
