@@ -142,6 +142,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     return false;
 }
 
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) accesses to the same memory: a consumer runs it
+// after reading a stage and before releasing the stage to be refilled.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // L2 policy for data read exactly once.
 __device__ __forceinline__ uint64_t l2_evict_first()
 {

@@ -420,6 +420,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_step_fused_tma(const FusedAr
                     }
                 }
             }
+            fence_proxy_async_smem();       // reads done before the stage is refilled
             mbar_arrive(empty0 + 8 * stage);
             if (++stage == kTmaStages) {
                 stage = 0;
@@ -441,6 +442,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_step_fused_tma(const FusedAr
                 st[k][4] = hi.x, st[k][5] = hi.y, st[k][6] = hi.z, st[k][7] = hi.w;
             }
         }
+        fence_proxy_async_smem();
         mbar_arrive(sempty0 + 8 * slot);
         if (++slot == kTmaStateSlots) {
             slot = 0;
