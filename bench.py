@@ -288,8 +288,9 @@ def run_gpu(args) -> None:
     kernel_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = max_over_ranks(total_ms, group, dev)
 
-    # -- the fused kernel alone: back-to-back launches (no flag read between
-    #    them), timed with events on the launching stream; this removes the
+    # -- the fused kernel alone: back-to-back steps' launches (no flag read
+    #    between them; each step's output is the next one's input, as in real
+    #    steps), timed with events on the launching stream; this removes the
     #    host launch gap that the per-step events above include -----------------
     nk = max(1, min(args.steps, 100))
     k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -297,6 +298,7 @@ def run_gpu(args) -> None:
     k0.record(stream)
     for _ in range(nk):
         dps.launch(desc)
+        dps.commit(False)          # swap the buffers without reading the flag
     k1.record(stream)
     torch.cuda.synchronize(dev)
     back_to_back_ms = k0.elapsed_time(k1) / nk
