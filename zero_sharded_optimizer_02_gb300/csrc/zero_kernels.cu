@@ -12,8 +12,12 @@
 // The fused step (k_step_fused_ring) is a persistent grid of one 512-thread
 // CTA per SM that stages the Nd contribution rows through a per-thread
 // cp.async ring in shared memory (16-byte copies, two row groups deep) and
-// moves the fp32 state with 256-bit streaming accesses; the unfused
-// primitives are 128-bit grid-stride loops sized to the SM count.
+// moves the fp32 state with 256-bit streaming accesses.  Two other variants
+// compute the same step bit for bit: k_step_fused (rows loaded straight into
+// registers; the kernel for rows read in place from host memory) and
+// k_step_fused_tma (a producer warp's cp.async.bulk copies of rows and state
+// into mbarrier-tracked shared-memory rings).  The unfused primitives are
+// 128-bit grid-stride loops sized to the SM count.
 //
 // Bit-exactness: every fp32 operation is an explicit correctly rounded
 // intrinsic (__fadd_rn/__fmul_rn/__fdiv_rn/__fsqrt_rn), so no multiply-add is
