@@ -617,6 +617,71 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+def run_entry(args) -> None:
+    """One entry point besides the fused step, on the bench workload's shard
+    rows and state (rank --rank, shard view), timed over --steps back-to-back
+    calls with CUDA events:
+      check    zero_check_nonfinite (the in-place pre-check): 2 Nd B/param read;
+      unfused  zero_step_shard_unfused (reduce into the fusion buffer, AdamW
+               from it, cast): 2 Nd + 4 + 28 + 6 = 2 Nd + 38 B/param."""
+    import torch
+
+    import synth
+    from zero_sharded_optimizer_02_gb300 import _abi, build
+    from zero_sharded_optimizer_02_gb300.step import DataParallelStep
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = workload(args)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        dps = DataParallelStep(w.psi, w.nd, [args.rank], w.grad_dtype, w.hparams,
+                               w.loss_scale, w.bucket, dev, gathered="slot",
+                               fused=args.op != "unfused", stream=stream)
+        L = dps.layouts[args.rank]
+        n, pitch = int(L.length), int(L.row_pitch)
+        st = dps.state[args.rank]
+        for row, which in zip(st.bufs[st.cur], ("master", "m", "v")):
+            synth.fill_shard_state(w, args.rank, which, row)
+        grads = torch.empty(w.nd, pitch, dtype=w.torch_grad_dtype, device=dev)
+        synth.fill_shard_rows(w, 0, args.rank, grads)
+    desc = {args.rank: _abi.grads(grads, pitch, 0, w.nd, w.grad_dtype)}
+    torch.cuda.synchronize(dev)
+
+    if args.op == "check":
+        def call():
+            _abi.zero_check_nonfinite(desc[args.rank], 0, n, dps.flag, stream)
+        bpp, launches = 2 * w.nd, 1
+    else:
+        def call():
+            dps.launch(desc)
+            dps.commit(False)
+        bpp = 2 * w.nd + 38
+        launches = 3 * -(-n // w.bucket)
+    for _ in range(args.warmup):
+        call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(args.steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    assert int(dps.flag.item()) == 0
+    ms = e0.elapsed_time(e1) / args.steps
+    gbs = bpp * n / (ms * 1e-3) / 1e9
+    peak = measured_peaks().get("hbm_gbs", 6800.0)
+    name = {"check": "zero_check_nonfinite", "unfused": "zero_step_shard_unfused"}[args.op]
+    print(json.dumps({"op": name, "metric": "params/s", "value": n / (ms * 1e-3),
+                      "unit": "params/s", "ms_per_call": ms,
+                      "config": {"workload": f"{args.config}: {w.title}", "shard_params": n,
+                                 "nd": w.nd, "bucket": w.bucket, "rank": args.rank},
+                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak,
+                                   "unit": "GB/s", "frac": gbs / peak,
+                                   "algorithmic_bytes_per_param": bpp},
+                      "gpu_launches": args.steps * launches}), flush=True)
+
+
 def run_gather(args) -> None:
     """ZeRO-3 on-demand gather: zero_gather_range collecting the whole flat
     fp16 parameter vector of a workload from its Nd pitched shards (the worst
@@ -736,7 +801,8 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["step", "gather", "checkpoint"], default="step",
+    ap.add_argument("--op", choices=["step", "gather", "checkpoint", "check", "unfused"],
+                    default="step",
                     help="step (the benchmark line) or a measurement of another entry point")
     ap.add_argument("--config", default="c4", choices=["c0", "c1", "c2", "c3", "c4"])
     ap.add_argument("--rank", type=int, default=0, help="first data-parallel rank to run")
@@ -768,6 +834,8 @@ def main():
         os.environ["ZERO_FUSED_VARIANT"] = args.variant
     if args.impl == "reference":
         run_reference(args)
+    elif args.op in ("check", "unfused"):
+        run_entry(args)
     elif args.op == "gather":
         run_gather(args)
     elif args.op == "checkpoint":
