@@ -657,7 +657,7 @@ def run_entry(args) -> None:
             dps.launch(desc)
             dps.commit(False)
         bpp = 2 * w.nd + 38
-        launches = 3 * -(-n // w.bucket)
+        launches = _abi.unfused_launch_count(n, w.bucket, 0)
     for _ in range(args.warmup):
         call()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

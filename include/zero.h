@@ -203,8 +203,8 @@ zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layout_t* L,
 #define ZERO_FUSED_WINDOW_ELEMS 25165824ull
 
 /* The same step unfused, through the constant-size fusion buffer: per bucket,
- * zero_reduce_scatter_bucket into cb, then zero_adam_step_shard from cb, then
- * zero_gather_params_shard.  cb: device fp32 workspace of cb_elems >=
+ * zero_reduce_scatter_bucket into cb (in the fused step's launch windows),
+ * then zero_adam_step_shard from cb, then zero_gather_params_shard.  cb: device fp32 workspace of cb_elems >=
  * min(bucket_elems, L->length) + 4 elements, 16-byte aligned, owned by the
  * caller and overwritten.  Bitwise identical results to zero_step_shard. */
 zero_status_t zero_step_shard_unfused(const zero_grads_t* g, const zero_layout_t* L,

@@ -226,6 +226,9 @@ def test_binding_constants_match_header(z):
     assert z._abi.fused_launch_count(117_187_500, 500_000_000) == 5
     assert z._abi.fused_launch_count(23_437_500, 50_000_000) == 1
     assert z._abi.fused_launch_count(16, 1) == 16 and z._abi.fused_launch_count(0, 8) == 0
+    # unfused: the reduction in the same windows, plus AdamW and cast, per bucket
+    assert z._abi.unfused_launch_count(117_187_500, 500_000_000) == 5 + 2
+    assert z._abi.unfused_launch_count(262_144, 65_536) == 4 * 3
     # a whole 64-shard vector is 64 segments: two gather launches; a layer
     # range inside one shard is one
     assert z._abi.gather_launch_count(1_500_000_000, 64, 0, 1_500_000_000) == 2

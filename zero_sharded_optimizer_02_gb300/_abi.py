@@ -91,23 +91,30 @@ _SIGNATURES = {
 ZERO_FUSED_WINDOW_ELEMS = 25165824
 
 
+def _windows(length: int, phase: int) -> int:
+    """Launch windows of one bucket (the library's split, see zero.h)."""
+    nwin = -(-length // ZERO_FUSED_WINDOW_ELEMS)
+    target = -(-(-(-length // nwin)) // 8) * 8
+    cut, w0, count = target - (phase & 7), 0, 0
+    while w0 < length:
+        w1 = min(cut, length)
+        if length - w1 < 64:
+            w1 = length
+        w0, cut = w1, cut + target
+        count += 1
+    return count
+
+
 def fused_launch_count(n: int, bucket: int, offset: int = 0) -> int:
     """Kernel launches zero_step_shard issues for a shard of n elements whose
     rows start at element `offset` (the same window split as the library)."""
-    count = 0
-    for b0 in range(0, n, bucket):
-        length = min(bucket, n - b0)
-        phase = (offset + b0) & 7
-        nwin = -(-length // ZERO_FUSED_WINDOW_ELEMS)
-        target = -(-(-(-length // nwin)) // 8) * 8
-        cut, w0 = target - phase, 0
-        while w0 < length:
-            w1 = min(cut, length)
-            if length - w1 < 64:
-                w1 = length
-            w0, cut = w1, cut + target
-            count += 1
-    return count
+    return sum(_windows(min(bucket, n - b0), offset + b0) for b0 in range(0, n, bucket))
+
+
+def unfused_launch_count(n: int, bucket: int, offset: int = 0) -> int:
+    """Kernel launches zero_step_shard_unfused issues: per bucket, the
+    reduction in the same launch windows, then the AdamW and cast passes."""
+    return sum(_windows(min(bucket, n - b0), offset + b0) + 2 for b0 in range(0, n, bucket))
 
 
 # Bit of the step flag word set when a step kernel gave up waiting on its own

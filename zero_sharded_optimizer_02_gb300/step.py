@@ -189,10 +189,8 @@ class DataParallelStep:
                                              self.loss_scale, self.h, self.cb, self.cb_elems,
                                              self.flag, self.stream)
             n = int(L.length)
-            if self.fused:
-                launches += _abi.fused_launch_count(n, self.bucket, int(grads[r].offset))
-            else:
-                launches += 3 * (-(-n // self.bucket) if n else 0)
+            count = _abi.fused_launch_count if self.fused else _abi.unfused_launch_count
+            launches += count(n, self.bucket, int(grads[r].offset))
         return launches
 
     def decide(self) -> bool:
