@@ -623,7 +623,9 @@ def run_entry(args) -> None:
     calls with CUDA events:
       check    zero_check_nonfinite (the in-place pre-check): 2 Nd B/param read;
       unfused  zero_step_shard_unfused (reduce into the fusion buffer, AdamW
-               from it, cast): 2 Nd + 4 + 28 + 6 = 2 Nd + 38 B/param."""
+               from it, cast): 2 Nd + 4 + 28 + 6 = 2 Nd + 38 B/param;
+      streamed zero_step_shard_streamed with every ready word already set:
+               2 Nd + 26 B/param."""
     import torch
 
     import synth
@@ -652,6 +654,23 @@ def run_entry(args) -> None:
         def call():
             _abi.zero_check_nonfinite(desc[args.rank], 0, n, dps.flag, stream)
         bpp, launches = 2 * w.nd, 1
+    elif args.op == "streamed":
+        # every bucket's ready word already set: the bucket-ready kernel's own
+        # rate, with the rows resident (the buckets of the end-to-end fed form)
+        sb = max(8, -(-(-(-n // args.e2e_buckets)) // 8) * 8)
+        ready = torch.ones(-(-n // sb), dtype=torch.int32, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        st, Lr = dps.state[args.rank], dps.layouts[args.rank]
+
+        def call():
+            gbuf, goff = dps._gathered_target(args.rank, 1 - dps.gcur)
+            dps.h.step = dps.t + 1
+            _abi.zero_step_shard_streamed(desc[args.rank], Lr, st.states[st.cur],
+                                          st.states[1 - st.cur], gbuf, goff, sb,
+                                          dps.loss_scale, dps.h, ready, 1, 10 ** 10, dps.flag,
+                                          status, stream)
+            dps.commit(False)
+        bpp, launches = 2 * w.nd + 26, 1
     else:
         def call():
             dps.launch(desc)
@@ -668,10 +687,13 @@ def run_entry(args) -> None:
     e1.record(stream)
     torch.cuda.synchronize(dev)
     assert int(dps.flag.item()) == 0
+    if args.op == "streamed":
+        assert int(status.item()) == 0
     ms = e0.elapsed_time(e1) / args.steps
     gbs = bpp * n / (ms * 1e-3) / 1e9
     peak = measured_peaks().get("hbm_gbs", 6800.0)
-    name = {"check": "zero_check_nonfinite", "unfused": "zero_step_shard_unfused"}[args.op]
+    name = {"check": "zero_check_nonfinite", "unfused": "zero_step_shard_unfused",
+            "streamed": "zero_step_shard_streamed"}[args.op]
     print(json.dumps({"op": name, "metric": "params/s", "value": n / (ms * 1e-3),
                       "unit": "params/s", "ms_per_call": ms,
                       "config": {"workload": f"{args.config}: {w.title}", "shard_params": n,
@@ -801,8 +823,8 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["step", "gather", "checkpoint", "check", "unfused"],
-                    default="step",
+    ap.add_argument("--op", choices=["step", "gather", "checkpoint", "check", "unfused",
+                                     "streamed"], default="step",
                     help="step (the benchmark line) or a measurement of another entry point")
     ap.add_argument("--config", default="c4", choices=["c0", "c1", "c2", "c3", "c4"])
     ap.add_argument("--rank", type=int, default=0, help="first data-parallel rank to run")
@@ -834,7 +856,7 @@ def main():
         os.environ["ZERO_FUSED_VARIANT"] = args.variant
     if args.impl == "reference":
         run_reference(args)
-    elif args.op in ("check", "unfused"):
+    elif args.op in ("check", "unfused", "streamed"):
         run_entry(args)
     elif args.op == "gather":
         run_gather(args)
