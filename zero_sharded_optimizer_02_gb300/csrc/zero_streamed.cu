@@ -5,15 +5,23 @@
 // section "ZeRO-DP", Stage 2: gradients are reduce-scattered bucket by bucket
 // during the backward pass.  Here the producer of a bucket -- in one GPU's
 // emulation, a copy stream landing the bucket's Nd contribution slices --
-// writes the bucket's ready word after its data; one persistent kernel walks
-// the shard's buckets in order and, before each, waits for that word.
+// writes the bucket's ready word after its data.  One persistent kernel walks
+// the shard's 8-element vectors grid-stride, each thread in increasing order,
+// and processes a vector once every bucket it touches is known to be ready.
+// There is no barrier per bucket, so a thread never idles at a bucket's end
+// while others finish it: when the buckets are already resident the kernel
+// is one even pass over the shard.
 //
-// Every wait is bounded: thread 0 of each CTA polls the word with an acquire
-// load, sleeping between polls (64 ns, doubling up to about 16 us), for at most
-// timeout_ns of %globaltimer time and an iteration cap.  On expiry it records ZERO_ERR_TIMEOUT in the
-// status word and the CTA returns without touching that bucket or later ones;
-// the context stays usable.  The kernel never waits on another kernel: only on
-// a word written by a copy engine or the host.
+// Readiness is cached per CTA in shared memory ("buckets [0, upto) are
+// ready").  A thread that needs a later bucket elects itself poller (one per
+// CTA at a time) and polls the ready words in bucket order with acquire loads,
+// sleeping between polls (64 ns, doubling up to about 16 us), for at most
+// timeout_ns of %globaltimer time a bucket and an iteration cap; the other
+// threads sleep on the shared cache, bounded the same way while it makes no
+// progress.  On expiry ZERO_ERR_TIMEOUT is recorded in the status word, the
+// CTA's threads stop before touching a bucket that is not ready, and the
+// context stays usable.  The kernel never waits on another kernel: only on a
+// word written by a copy engine or the host.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -100,61 +108,143 @@ struct StreamArgs {
     uint32_t* status;      // ZERO_ERR_TIMEOUT is recorded here on expiry
 };
 
+__device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared.u32 %0, [%1];"
+                 : "=r"(v)
+                 : "r"(smem_u32(p))
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_cta(uint32_t* p, uint32_t v)
+{
+    asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+// A CTA's shared readiness cache.
+struct ReadyCache {
+    uint32_t upto;     // buckets [0, upto) are ready
+    uint32_t poller;   // 1 while a thread of the CTA polls the ready words
+    uint32_t abort;    // 1 once a wait ran out
+};
+
+// Waits until buckets [0, need] are known ready.  False if a wait ran out
+// (here or in another thread of the CTA); the status word then holds
+// ZERO_ERR_TIMEOUT.
+__device__ bool wait_buckets(ReadyCache& rc, const StreamArgs& s, uint32_t need)
+{
+    uint64_t t0 = global_ns();
+    uint32_t seen = ld_acquire_cta(&rc.upto);
+    unsigned sleep_ns = 32;
+    for (uint64_t i = 0; i < (1ull << 40); ++i) {
+        const uint32_t u = ld_acquire_cta(&rc.upto);
+        if (u > need)
+            return true;
+        if (ld_acquire_cta(&rc.abort))
+            return false;
+        if (u != seen) {                       // progress: restart the clock
+            seen = u;
+            t0 = global_ns();
+        }
+        if (atomicCAS(&rc.poller, 0u, 1u) == 0u) {
+            // the elected poller: ready words in bucket order, one wait each
+            uint32_t v = ld_acquire_cta(&rc.upto);
+            bool ok = true;
+            while (v <= need) {
+                if (!wait_ready(s.ready + v, s.epoch, s.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                st_release_cta(&rc.upto, ++v);
+            }
+            if (!ok) {
+                atomicCAS(s.status, 0u, (uint32_t)ZERO_ERR_TIMEOUT);
+                st_release_cta(&rc.abort, 1u);
+            }
+            atomicExch(&rc.poller, 0u);
+            if (!ok)
+                return false;
+            continue;
+        }
+        // another thread polls: bounded by the poller's own limit plus margin
+        if (global_ns() - t0 > 2 * s.timeout_ns + 1000000) {
+            atomicCAS(s.status, 0u, (uint32_t)ZERO_ERR_TIMEOUT);
+            st_release_cta(&rc.abort, 1u);
+            return false;
+        }
+        __nanosleep(sleep_ns);
+        if (sleep_ns < 1024)
+            sleep_ns *= 2;
+    }
+    atomicCAS(s.status, 0u, (uint32_t)ZERO_ERR_TIMEOUT);
+    st_release_cta(&rc.abort, 1u);
+    return false;
+}
+
+// Scalar element e of the shard (head or tail): fold with .cg loads, AdamW,
+// cast.  Returns "sum nonfinite".
+template <int DT>
+__device__ __forceinline__ bool streamed_scalar(const FusedArgs& a, uint64_t e)
+{
+    float g = widen1<DT>(ld_grad2_cg(a.g + e));
+    for (uint32_t j = 1; j < a.nd; ++j)
+        g = __fadd_rn(g, widen1<DT>(ld_grad2_cg(a.g + e + (uint64_t)j * a.row_stride)));
+    float p = a.p_in[e], m = a.m_in[e], v = a.v_in[e];
+    adamw1(a.k, __fmul_rn(g, a.k.inv), p, m, v);
+    a.p_out[e] = p;
+    a.m_out[e] = m;
+    a.v_out[e] = v;
+    a.gath[e] = narrow1<DT>(p);
+    return nonfinite(g);
+}
+
 template <int DT, int W, bool V8>
 __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) k_step_streamed(const StreamArgs s)
 {
-    __shared__ int s_ok;
+    __shared__ ReadyCache rc;
+    if (threadIdx.x == 0) {
+        rc.upto = 0;
+        rc.poller = 0;
+        rc.abort = 0;
+    }
+    __syncthreads();
     bool bad = false;
     const uint64_t tid = (uint64_t)blockIdx.x * kStreamThreads + threadIdx.x;
     const uint64_t nthr = (uint64_t)gridDim.x * kStreamThreads;
-    const uint64_t nb = (s.n + s.bucket - 1) / s.bucket;
-    for (uint64_t b = 0; b < nb; ++b) {
-        if (threadIdx.x == 0)
-            s_ok = wait_ready(s.ready + b, s.epoch, s.timeout_ns) ? 1 : 0;
-        __syncthreads();
-        const bool ok = s_ok != 0;
-        __syncthreads();            // s_ok is rewritten in the next round
-        if (!ok) {
-            if (threadIdx.x == 0)
-                atomicCAS(s.status, 0u, (uint32_t)ZERO_ERR_TIMEOUT);
+    const FusedArgs& a = s.a;            // the whole shard; a.sp splits it
+    uint32_t known = 0;                  // buckets [0, known) seen ready by this thread
+    auto ready_for = [&](uint64_t last_elem) {
+        const uint32_t need = (uint32_t)(last_elem / s.bucket);
+        if (need < known)
+            return true;
+        if (!wait_buckets(rc, s, need))
+            return false;
+        known = need + 1;
+        return true;
+    };
+    bool ok = true;
+    // head scalars (bucket 0), then the vectors in order, then the tail
+    const uint64_t nscalar = a.sp.nscalar();
+    const bool head_scalar = tid < nscalar && tid < a.sp.head;
+    if (head_scalar) {
+        ok = ready_for(tid);
+        if (ok)
+            bad |= streamed_scalar<DT>(a, tid);
+    }
+    for (uint64_t q = tid; ok && q < a.sp.nvec; q += nthr) {
+        const uint64_t e = a.sp.head + 8 * q;
+        if (!(ok = ready_for(e + 7)))
             break;
-        }
-        const uint64_t b0 = b * s.bucket;
-        const uint64_t len = s.n - b0 < s.bucket ? s.n - b0 : s.bucket;
-        Split sp;
-        sp.len = len;
-        const uint64_t head = (8 - ((s.phase + b0) & 7)) & 7;
-        sp.head = head < len ? head : len;
-        sp.nvec = (len - sp.head) / 8;
-        FusedArgs a = s.a;
-        a.g += b0;
-        a.p_in += b0;
-        a.m_in += b0;
-        a.v_in += b0;
-        a.p_out += b0;
-        a.m_out += b0;
-        a.v_out += b0;
-        a.gath += b0;
-        a.sp = sp;
-        if (tid < sp.nscalar()) {
-            const uint64_t e = sp.scalar_elem(tid);
-            float g = widen1<DT>(ld_grad2_cg(a.g + e));
-            for (uint32_t j = 1; j < a.nd; ++j)
-                g = __fadd_rn(g, widen1<DT>(ld_grad2_cg(a.g + e + (uint64_t)j * a.row_stride)));
-            bad |= nonfinite(g);
-            float p = a.p_in[e], m = a.m_in[e], v = a.v_in[e];
-            adamw1(a.k, __fmul_rn(g, a.k.inv), p, m, v);
-            a.p_out[e] = p;
-            a.m_out[e] = m;
-            a.v_out[e] = v;
-            a.gath[e] = narrow1<DT>(p);
-        }
-        for (uint64_t q = tid; q < sp.nvec; q += nthr) {
-            const uint64_t e = sp.head + 8 * q;
-            float acc[8];
-            fold8_cg<DT>(a.g + e, a.row_stride, a.nd, acc);
-            bad |= fused_epilogue<DT, W, V8>(a, e, acc);
-        }
+        float acc[8];
+        fold8_cg<DT>(a.g + e, a.row_stride, a.nd, acc);
+        bad |= fused_epilogue<DT, W, V8>(a, e, acc);
+    }
+    if (ok && tid < nscalar && !head_scalar) {
+        const uint64_t e = a.sp.scalar_elem(tid);
+        if (ready_for(e))
+            bad |= streamed_scalar<DT>(a, e);
     }
     flag_if_any(bad, s.a.flag);
 }
@@ -227,7 +317,13 @@ extern "C" zero_status_t zero_step_shard_streamed(
     s.a.g = static_cast<const uint16_t*>(gr.base) + g->offset;
     s.a.row_stride = g->row_stride;
     s.a.nd = g->nd;
-    s.a.sp = Split{0, 0, 0};
+    {   // the whole shard: scalar head up to the first 16-byte aligned row
+        // element (none, as offset is a multiple of 8), vectors, scalar tail
+        const uint64_t head = (8 - (g->offset & 7)) & 7;
+        s.a.sp.len = n;
+        s.a.sp.head = head < n ? head : n;
+        s.a.sp.nvec = (n - s.a.sp.head) / 8;
+    }
     s.a.p_in = in->master;
     s.a.m_in = in->m;
     s.a.v_in = in->v;
