@@ -259,17 +259,19 @@ zero_status_t zero_check_nonfinite(const zero_grads_t* g, uint64_t begin, uint64
 
 /* The fused step started bucket by bucket as gradients arrive ("ZeRO-DP",
  * Stage 2: gradients are reduce-scattered in buckets during the backward
- * pass).  One persistent launch walks the shard's buckets in order; before
- * bucket b (elements [b*bucket_elems, ...) of the shard) each CTA waits until
- * d_ready[b] >= epoch (wrap-around comparison).  The producer of bucket b
+ * pass).  The shard runs as the fused step's launch windows (at most
+ * ZERO_FUSED_WINDOW_ELEMS elements each), and each launch processes a vector
+ * of 8 elements only once d_ready[b] >= epoch (wrap-around comparison) for
+ * every bucket b it touches (bucket b: elements [b*bucket_elems, ...) of the
+ * shard); buckets are awaited in order.  The producer of bucket b
  * writes d_ready[b] after the bucket's contributions are in place -- e.g. a
  * cudaMemcpyAsync of the word on the copy stream that copied the data.  The
  * ready words must be written by a copy engine or the host, never by a kernel
  * that would have to run concurrently with this one.
  * Each wait is bounded by timeout_ns of GPU time (%globaltimer) and an
  * iteration cap; on expiry the kernel stores ZERO_ERR_TIMEOUT into *d_status
- * (if it is still 0), leaves that bucket and the later ones unwritten, and
- * returns: the caller reads *d_status after the stream work completes.
+ * (if it is still 0), touches no element of a bucket that was not seen ready,
+ * and returns: the caller reads *d_status after the stream work completes.
  * timeout_ns must be in [1, ZERO_MAX_WAIT_NS] (ZERO_ERR_INVALID_ARG otherwise).
  * Other arguments, alignment and results as zero_step_shard (bitwise equal). */
 #define ZERO_MAX_WAIT_NS 60000000000ull

@@ -10,7 +10,8 @@ from ._abi import (  # noqa: F401
     ZERO_ERR_TIMEOUT, ZERO_ERR_UNSUPPORTED, ZERO_F16, ZERO_FUSED_WINDOW_ELEMS,
     ZERO_GATHER_SEGMENTS_PER_LAUNCH, ZERO_OK, ZERO_STATIC_CB_ELEMS, ZERO_STATIC_CB_MAX_BUCKET,
     AdamW, CkptHeader, Grads, Layout, State, ZeroError, adamw, exported_names,
-    fused_launch_count, gather_launch_count, grads, unfused_launch_count, lib, state, zero_adam_step_shard,
+    fused_launch_count, gather_launch_count, grads, streamed_launch_count,
+    unfused_launch_count, lib, state, zero_adam_step_shard,
     zero_check_nonfinite, zero_checkpoint_load, zero_checkpoint_read_header,
     zero_checkpoint_save, zero_comm_volume_elems, zero_feed_buckets, zero_gather_params_shard,
     zero_gather_range, zero_model_state_bytes, zero_model_state_bytes_mp,

@@ -111,6 +111,12 @@ def fused_launch_count(n: int, bucket: int, offset: int = 0) -> int:
     return sum(_windows(min(bucket, n - b0), offset + b0) for b0 in range(0, n, bucket))
 
 
+def streamed_launch_count(n: int, offset: int = 0) -> int:
+    """Kernel launches zero_step_shard_streamed issues: the launch windows of
+    the whole shard, whatever the bucket size."""
+    return _windows(n, offset) if n else 0
+
+
 def unfused_launch_count(n: int, bucket: int, offset: int = 0) -> int:
     """Kernel launches zero_step_shard_unfused issues: per bucket, the
     reduction in the same launch windows, then the AdamW and cast passes."""

@@ -446,6 +446,30 @@ __device__ __forceinline__ bool fused_epilogue_loaded(const FusedArgs& a, uint64
     return bad;
 }
 
+// Calls fn(w0, w1) for the fewest equal launch windows of at most
+// max_window elements (a multiple of 8) covering [0, len) of a bucket whose
+// rows' element 0 has phase `phase` (elements past a 16-byte boundary): every
+// cut falls on an 8-element boundary of the rows, and a remainder of under
+// 64 elements joins the last window.  Stops at the first status other than
+// ZERO_OK.
+template <typename F>
+zero_status_t for_each_window(uint64_t phase, uint64_t len, uint64_t max_window, F&& fn)
+{
+    const uint64_t nwin = (len + max_window - 1) / max_window;
+    const uint64_t target = ((len + nwin - 1) / nwin + 7) / 8 * 8;
+    uint64_t cut = target - (phase & 7);
+    for (uint64_t w0 = 0; w0 < len; cut += target) {
+        uint64_t w1 = cut < len ? cut : len;
+        if (len - w1 < 64)
+            w1 = len;
+        const zero_status_t st = fn(w0, w1);
+        if (st != ZERO_OK)
+            return st;
+        w0 = w1;
+    }
+    return ZERO_OK;
+}
+
 // True if every state pointer of the fused step is 32-byte aligned (the
 // vectors of every window then are too: they start at multiples of 8
 // elements).

@@ -641,29 +641,6 @@ Split split_window(uint64_t phase, uint64_t len)
     return s;
 }
 
-// Calls fn(w0, w1) for the fewest equal launch windows of at most kWindow
-// elements covering [0, len) of a bucket whose rows' element 0 has phase
-// `phase` (elements past a 16-byte boundary): every cut falls on an
-// 8-element boundary of the rows, and a remainder of under 64 elements joins
-// the last window.  Stops at the first status other than ZERO_OK.
-template <typename F>
-zero_status_t for_each_window(uint64_t phase, uint64_t len, F&& fn)
-{
-    const uint64_t nwin = (len + kWindow - 1) / kWindow;
-    const uint64_t target = ((len + nwin - 1) / nwin + 7) / 8 * 8;
-    uint64_t cut = target - (phase & 7);
-    for (uint64_t w0 = 0; w0 < len; cut += target) {
-        uint64_t w1 = cut < len ? cut : len;
-        if (len - w1 < 64)
-            w1 = len;
-        const zero_status_t st = fn(w0, w1);
-        if (st != ZERO_OK)
-            return st;
-        w0 = w1;
-    }
-    return ZERO_OK;
-}
-
 bool mul_overflows(uint64_t a, uint64_t b) { return a != 0 && b > UINT64_MAX / a; }
 
 // Validates a gradient descriptor for elements [begin, begin + n) of the shard.
@@ -1012,7 +989,7 @@ extern "C" zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layou
     const bool v8 = state_v8_ok(sp);
     for (uint64_t b0 = 0; b0 < n; b0 += bucket_elems) {
         const uint64_t len = n - b0 < bucket_elems ? n - b0 : bucket_elems;
-        st = for_each_window(g->offset + b0, len, [&](uint64_t w0, uint64_t w1) {
+        st = for_each_window(g->offset + b0, len, kWindow, [&](uint64_t w0, uint64_t w1) {
             const uint64_t e0 = b0 + w0;
             FusedArgs a{rows + e0, g->row_stride, g->nd, split_window(g->offset + e0, w1 - w0),
                         in->master + e0, in->m + e0, in->v + e0, out->master + e0,
@@ -1067,7 +1044,7 @@ extern "C" zero_status_t zero_step_shard_unfused(const zero_grads_t* g, const ze
         // phase and the optimizer pass runs on float4s.
         float* cbb = cb + (b0 & 3);
         // the reduction in launch windows, like the fused step
-        st = for_each_window(g->offset + b0, len, [&](uint64_t w0, uint64_t w1) {
+        st = for_each_window(g->offset + b0, len, kWindow, [&](uint64_t w0, uint64_t w1) {
             ReduceArgs r{rows + b0 + w0, g->row_stride, g->nd,
                          split_window(g->offset + b0 + w0, w1 - w0), k.inv, cbb + w0,
                          d_nonfinite};

@@ -37,7 +37,12 @@ constexpr int kStreamCtasPerSm = 2;
 // go through L2 (.cg) instead of the non-coherent path.
 __device__ __forceinline__ uint4 ld_grad16_cg(const uint16_t* p)
 {
-    return __ldcg(reinterpret_cast<const uint4*>(p));
+    uint4 r;
+    asm volatile("ld.global.cg.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p)
+                 : "memory");
+    return r;
 }
 
 __device__ __forceinline__ uint16_t ld_grad2_cg(const uint16_t* p)
@@ -98,11 +103,10 @@ __device__ __forceinline__ void fold8_cg(const uint16_t* gp, uint64_t row_stride
 }
 
 struct StreamArgs {
-    FusedArgs a;           // the whole shard: pointers at shard element 0
-    uint64_t n;            // shard length
+    FusedArgs a;           // one launch window: pointers at its first element, a.sp its split
+    uint64_t e0;           // shard element of the window's element 0
     uint64_t bucket;       // bucket size (elements)
-    uint64_t phase;        // gradient element phase of shard element 0 (offset % 8)
-    const uint32_t* ready; // ready word of each bucket
+    const uint32_t* ready; // ready word of each bucket of the shard
     uint32_t epoch;
     uint64_t timeout_ns;
     uint32_t* status;      // ZERO_ERR_TIMEOUT is recorded here on expiry
@@ -204,8 +208,9 @@ template <int DT, int W, bool V8>
 __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) k_step_streamed(const StreamArgs s)
 {
     __shared__ ReadyCache rc;
+    const uint32_t first_bucket = (uint32_t)(s.e0 / s.bucket);
     if (threadIdx.x == 0) {
-        rc.upto = 0;
+        rc.upto = first_bucket;          // earlier buckets belong to earlier windows
         rc.poller = 0;
         rc.abort = 0;
     }
@@ -213,10 +218,10 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) k_step_strea
     bool bad = false;
     const uint64_t tid = (uint64_t)blockIdx.x * kStreamThreads + threadIdx.x;
     const uint64_t nthr = (uint64_t)gridDim.x * kStreamThreads;
-    const FusedArgs& a = s.a;            // the whole shard; a.sp splits it
-    uint32_t known = 0;                  // buckets [0, known) seen ready by this thread
+    const FusedArgs& a = s.a;            // the window; a.sp splits it
+    uint32_t known = first_bucket;       // buckets below `known` seen ready by this thread
     auto ready_for = [&](uint64_t last_elem) {
-        const uint32_t need = (uint32_t)(last_elem / s.bucket);
+        const uint32_t need = (uint32_t)((s.e0 + last_elem) / s.bucket);
         if (need < known)
             return true;
         if (!wait_buckets(rc, s, need))
@@ -225,7 +230,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) k_step_strea
         return true;
     };
     bool ok = true;
-    // head scalars (bucket 0), then the vectors in order, then the tail
+    // head scalars, then the vectors in order, then the tail
     const uint64_t nscalar = a.sp.nscalar();
     const bool head_scalar = tid < nscalar && tid < a.sp.head;
     if (head_scalar) {
@@ -313,42 +318,53 @@ extern "C" zero_status_t zero_step_shard_streamed(
     const zero_status_t rs = resolve_grads(g, &gr);
     if (rs != ZERO_OK)
         return rs;
-    StreamArgs s;
-    s.a.g = static_cast<const uint16_t*>(gr.base) + g->offset;
-    s.a.row_stride = g->row_stride;
-    s.a.nd = g->nd;
-    {   // the whole shard: scalar head up to the first 16-byte aligned row
-        // element (none, as offset is a multiple of 8), vectors, scalar tail
-        const uint64_t head = (8 - (g->offset & 7)) & 7;
-        s.a.sp.len = n;
-        s.a.sp.head = head < n ? head : n;
-        s.a.sp.nvec = (n - s.a.sp.head) / 8;
-    }
-    s.a.p_in = in->master;
-    s.a.m_in = in->m;
-    s.a.v_in = in->v;
-    s.a.p_out = out->master;
-    s.a.m_out = out->m;
-    s.a.v_out = out->v;
-    s.a.gath = static_cast<uint16_t*>(gathered) + gathered_offset_elems;
-    s.a.k = make_scalars(h, g->nd, loss_scale);
-    s.a.flag = d_nonfinite;
-    s.n = n;
-    s.bucket = bucket_elems;
-    s.phase = g->offset & 7;
-    s.ready = d_ready;
-    s.epoch = epoch;
-    s.timeout_ns = timeout_ns;
-    s.status = d_status;
-    // Every bucket's first vector starts at a shard element b0 + head that is
-    // a multiple of 8 (offset is), so one store width fits all buckets.
-    const uint64_t head0 = (8 - (s.phase & 7)) & 7;
-    const uintptr_t a0 = (uintptr_t)(s.a.gath + head0);
+    StreamArgs base;
+    base.a.g = static_cast<const uint16_t*>(gr.base) + g->offset;
+    base.a.row_stride = g->row_stride;
+    base.a.nd = g->nd;
+    base.a.p_in = in->master;
+    base.a.m_in = in->m;
+    base.a.v_in = in->v;
+    base.a.p_out = out->master;
+    base.a.m_out = out->m;
+    base.a.v_out = out->v;
+    base.a.gath = static_cast<uint16_t*>(gathered) + gathered_offset_elems;
+    base.a.k = make_scalars(h, g->nd, loss_scale);
+    base.a.flag = d_nonfinite;
+    base.bucket = bucket_elems;
+    base.ready = d_ready;
+    base.epoch = epoch;
+    base.timeout_ns = timeout_ns;
+    base.status = d_status;
+    // Windows start at multiples of 8 shard elements (offset is one), so
+    // every vector of every window has the gathered phase of element 0 and
+    // one store width fits all.
+    const uintptr_t a0 = (uintptr_t)base.a.gath;
     const int width = (a0 & 15) == 0 ? 16 : (a0 & 7) == 0 ? 8 : (a0 & 3) == 0 ? 4 : 2;
-    const uint64_t want = (n / 8 + kStreamThreads - 1) / kStreamThreads;
+    const float* const sp[6] = {in->master, in->m, in->v, out->master, out->m, out->v};
+    const bool v8 = state_v8_ok(sp);
     const uint64_t cap = (uint64_t)sms_streamed() * kStreamCtasPerSm;
-    const unsigned grid = (unsigned)(want == 0 ? 1 : (want < cap ? want : cap));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // The shard runs as the fused step's launch windows: kernel boundaries
+    // keep the SMs at the same place in the rows.
+    return for_each_window(g->offset, n, ZERO_FUSED_WINDOW_ELEMS, [&](uint64_t w0, uint64_t w1) {
+        StreamArgs s = base;
+        s.e0 = w0;
+        s.a.g += w0;
+        s.a.p_in += w0;
+        s.a.m_in += w0;
+        s.a.v_in += w0;
+        s.a.p_out += w0;
+        s.a.m_out += w0;
+        s.a.v_out += w0;
+        s.a.gath += w0;
+        const uint64_t len = w1 - w0;
+        const uint64_t head = (8 - ((g->offset + w0) & 7)) & 7;
+        s.a.sp.len = len;
+        s.a.sp.head = head < len ? head : len;
+        s.a.sp.nvec = (len - s.a.sp.head) / 8;
+        const uint64_t want = (len / 8 + kStreamThreads - 1) / kStreamThreads;
+        const unsigned grid = (unsigned)(want == 0 ? 1 : (want < cap ? want : cap));
 #define ZERO_STREAM_LAUNCH(DT, V8)                                                          \
     switch (width) {                                                                        \
     case 16: k_step_streamed<DT, 16, V8><<<grid, kStreamThreads, 0, st>>>(s); break;        \
@@ -356,23 +372,22 @@ extern "C" zero_status_t zero_step_shard_streamed(
     case 4: k_step_streamed<DT, 4, V8><<<grid, kStreamThreads, 0, st>>>(s); break;          \
     default: k_step_streamed<DT, 2, V8><<<grid, kStreamThreads, 0, st>>>(s); break;         \
     }
-    const float* const sp[6] = {in->master, in->m, in->v, out->master, out->m, out->v};
-    const bool v8 = state_v8_ok(sp);
-    if (g->dtype == ZERO_F16) {
-        if (v8) {
-            ZERO_STREAM_LAUNCH(ZERO_F16, true)
+        if (g->dtype == ZERO_F16) {
+            if (v8) {
+                ZERO_STREAM_LAUNCH(ZERO_F16, true)
+            } else {
+                ZERO_STREAM_LAUNCH(ZERO_F16, false)
+            }
         } else {
-            ZERO_STREAM_LAUNCH(ZERO_F16, false)
+            if (v8) {
+                ZERO_STREAM_LAUNCH(ZERO_BF16, true)
+            } else {
+                ZERO_STREAM_LAUNCH(ZERO_BF16, false)
+            }
         }
-    } else {
-        if (v8) {
-            ZERO_STREAM_LAUNCH(ZERO_BF16, true)
-        } else {
-            ZERO_STREAM_LAUNCH(ZERO_BF16, false)
-        }
-    }
 #undef ZERO_STREAM_LAUNCH
-    return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ERR_CUDA;
+        return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ERR_CUDA;
+    });
 }
 
 extern "C" zero_status_t zero_feed_buckets(const void* host, uint64_t host_row_stride,
