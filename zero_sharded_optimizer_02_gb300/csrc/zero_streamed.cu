@@ -37,12 +37,7 @@ constexpr int kStreamCtasPerSm = 2;
 // go through L2 (.cg) instead of the non-coherent path.
 __device__ __forceinline__ uint4 ld_grad16_cg(const uint16_t* p)
 {
-    uint4 r;
-    asm volatile("ld.global.cg.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p)
-                 : "memory");
-    return r;
+    return __ldcg(reinterpret_cast<const uint4*>(p));
 }
 
 __device__ __forceinline__ uint16_t ld_grad2_cg(const uint16_t* p)
@@ -219,14 +214,20 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) k_step_strea
     const uint64_t tid = (uint64_t)blockIdx.x * kStreamThreads + threadIdx.x;
     const uint64_t nthr = (uint64_t)gridDim.x * kStreamThreads;
     const FusedArgs& a = s.a;            // the window; a.sp splits it
-    uint32_t known = first_bucket;       // buckets below `known` seen ready by this thread
+    // buckets below `known` are seen ready by this thread: window elements
+    // below `ready_end` (kept so that the common case costs one compare)
+    uint32_t known = first_bucket;
+    uint64_t ready_end = 0;
     auto ready_for = [&](uint64_t last_elem) {
-        const uint32_t need = (uint32_t)((s.e0 + last_elem) / s.bucket);
-        if (need < known)
+        if (last_elem < ready_end)
             return true;
-        if (!wait_buckets(rc, s, need))
-            return false;
-        known = need + 1;
+        const uint32_t need = (uint32_t)((s.e0 + last_elem) / s.bucket);
+        if (need >= known) {
+            if (!wait_buckets(rc, s, need))
+                return false;
+            known = need + 1;
+        }
+        ready_end = (uint64_t)known * s.bucket - s.e0;
         return true;
     };
     bool ok = true;
