@@ -624,8 +624,8 @@ def run_entry(args) -> None:
       check    zero_check_nonfinite (the in-place pre-check): 2 Nd B/param read;
       unfused  zero_step_shard_unfused (reduce into the fusion buffer, AdamW
                from it, cast): 2 Nd + 4 + 28 + 6 = 2 Nd + 38 B/param;
-      streamed zero_step_shard_streamed with every ready word already set:
-               2 Nd + 26 B/param."""
+      streamed zero_step_shard_streamed with every ready word already set
+               (the waits pass at once): 2 Nd + 26 B/param."""
     import torch
 
     import synth
@@ -670,7 +670,7 @@ def run_entry(args) -> None:
                                           dps.loss_scale, dps.h, ready, 1, 10 ** 10, dps.flag,
                                           status, stream)
             dps.commit(False)
-        bpp, launches = 2 * w.nd + 26, _abi.streamed_launch_count(n, 0)
+        bpp, launches = 2 * w.nd + 26, _abi.streamed_launch_count(n, sb, 0)
     else:
         def call():
             dps.launch(desc)

@@ -259,11 +259,12 @@ zero_status_t zero_check_nonfinite(const zero_grads_t* g, uint64_t begin, uint64
 
 /* The fused step started bucket by bucket as gradients arrive ("ZeRO-DP",
  * Stage 2: gradients are reduce-scattered in buckets during the backward
- * pass).  The shard runs as the fused step's launch windows (at most
- * ZERO_FUSED_WINDOW_ELEMS elements each), and each launch processes a vector
- * of 8 elements only once d_ready[b] >= epoch (wrap-around comparison) for
- * every bucket b it touches (bucket b: elements [b*bucket_elems, ...) of the
- * shard); buckets are awaited in order.  The producer of bucket b
+ * pass).  For each bucket b in order (elements [b*bucket_elems, ...) of the
+ * shard), a one-thread kernel waits until d_ready[b] >= epoch (wrap-around
+ * comparison), then the fused step's launches for the bucket follow on the
+ * same stream (as zero_step_shard: launch windows of at most
+ * ZERO_FUSED_WINDOW_ELEMS elements, the same kernel variant).  The producer
+ * of bucket b
  * writes d_ready[b] after the bucket's contributions are in place -- e.g. a
  * cudaMemcpyAsync of the word on the copy stream that copied the data.  The
  * ready words must be written by a copy engine or the host, never by a kernel

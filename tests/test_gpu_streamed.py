@@ -4,11 +4,11 @@
 section "ZeRO-DP", Stage 2: gradients are reduce-scattered bucket by bucket
 during backward, so the optimizer can start on a bucket once it is complete.
 A copy stream lands each bucket's contributions and then writes its ready
-word; the persistent step kernel, launched first on another stream, waits for
-each word (bounded) and processes the bucket.  Results must equal the fused
+word; on the compute stream a one-thread kernel waits for each word
+(bounded) before the bucket's step launches.  Results must equal the fused
 step bit for bit.  A ready word that nothing writes makes the bounded wait
-run out: the kernel reports ZERO_ERR_TIMEOUT in its status word, leaves the
-late buckets untouched, and the context stays usable.
+run out: ZERO_ERR_TIMEOUT lands in the status word, the late buckets stay
+untouched, and the context stays usable.
 """
 import dataclasses
 

@@ -111,10 +111,10 @@ def fused_launch_count(n: int, bucket: int, offset: int = 0) -> int:
     return sum(_windows(min(bucket, n - b0), offset + b0) for b0 in range(0, n, bucket))
 
 
-def streamed_launch_count(n: int, offset: int = 0) -> int:
-    """Kernel launches zero_step_shard_streamed issues: the launch windows of
-    the whole shard, whatever the bucket size."""
-    return _windows(n, offset) if n else 0
+def streamed_launch_count(n: int, bucket: int, offset: int = 0) -> int:
+    """Kernel launches zero_step_shard_streamed issues: per bucket, one wait
+    and the fused step's launch windows."""
+    return sum(1 + _windows(min(bucket, n - b0), offset + b0) for b0 in range(0, n, bucket))
 
 
 def unfused_launch_count(n: int, bucket: int, offset: int = 0) -> int:

@@ -334,7 +334,14 @@ struct FusedArgs {
     uint16_t* gath;        // gathered element of window element 0
     StepScalars k;
     uint32_t* flag;
+    const uint32_t* gate;  // if non-null and nonzero at launch, the launch does nothing
 };
+
+// True if the launch is gated off (a bucket wait before it ran out).
+__device__ __forceinline__ bool gated(const FusedArgs& a)
+{
+    return a.gate && *static_cast<const volatile uint32_t*>(a.gate) != 0;
+}
 
 // Scalar element e of the window (head or tail): fold, AdamW, cast.
 template <int DT>

@@ -40,4 +40,17 @@ StepScalars make_scalars(const zero_adamw_t* h, uint32_t nd, double loss_scale);
 // host memory.
 zero_status_t resolve_grads(const zero_grads_t* g, zero_grads_t* out, bool* in_host = nullptr);
 
+// Launches the fused step over elements [b0, b0 + len) of a shard -- one
+// bucket -- as the fewest equal launch windows of at most
+// ZERO_FUSED_WINDOW_ELEMS elements.  rows: the rows at shard element 0, at
+// the address the device reads them (resolve_grads); gath: the gathered slot
+// of shard element 0.  The variant follows ZERO_FUSED_VARIANT (the register
+// kernel for host_rows).  gate: if non-null, every launch reads it first and
+// does nothing if it is nonzero.  Returns ZERO_ERR_CUDA if a launch failed.
+zero_status_t launch_fused_bucket(const uint16_t* rows, const zero_grads_t* g,
+                                  const zero_state_t* in, const zero_state_t* out,
+                                  uint16_t* gath, uint64_t b0, uint64_t len,
+                                  const StepScalars& k, bool host_rows, uint32_t* d_nonfinite,
+                                  const uint32_t* gate, void* stream);
+
 }  // namespace zero

@@ -151,6 +151,8 @@ constexpr uint64_t kTmaDrainNs = 1000ull * 1000 * 1000;
 template <int DT, int W, bool V8>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_step_fused(const FusedArgs a)
 {
+    if (gated(a))
+        return;
     bool bad = false;
     const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
     const uint64_t nthr = (uint64_t)gridDim.x * kThreads;
@@ -177,6 +179,8 @@ template <int DT, int W, bool V8>
 __global__ void __launch_bounds__(kRingThreads, 1) k_step_fused_ring(const FusedArgs a)
 {
     extern __shared__ uint4 ring[];
+    if (gated(a))
+        return;
     bool bad = false;
     const int t = threadIdx.x;
     const uint64_t tid = (uint64_t)blockIdx.x * kRingThreads + t;
@@ -306,6 +310,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_step_fused_tma(const FusedAr
     const float* slots =                                              // [slot][array][consumer][8]
         reinterpret_cast<const float*>(tma_smem + kTmaStages * kTmaStageBytes);
     uint64_t* bars = reinterpret_cast<uint64_t*>(tma_smem + kTmaBarOffset);
+    if (gated(a))                       // uniform: every thread returns before any barrier
+        return;
     const uint32_t full0 = smem_u32(bars);                                    // + 8 s
     const uint32_t empty0 = smem_u32(bars + kTmaStages);                      // + 8 s
     const uint32_t sfull0 = smem_u32(bars + 2 * kTmaStages);                  // + 8 slot
@@ -866,6 +872,31 @@ zero_status_t check_step_common(const zero_grads_t* g, const zero_layout_t* L,
 }
 
 }  // namespace
+
+zero_status_t launch_fused_bucket(const uint16_t* rows, const zero_grads_t* g,
+                                  const zero_state_t* in, const zero_state_t* out,
+                                  uint16_t* gath, uint64_t b0, uint64_t len,
+                                  const StepScalars& k, bool host_rows, uint32_t* d_nonfinite,
+                                  const uint32_t* gate, void* stream)
+{
+    const int variant = fused_variant(host_rows);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const float* const sp[6] = {in->master, in->m, in->v, out->master, out->m, out->v};
+    const bool v8 = state_v8_ok(sp);
+    return for_each_window(g->offset + b0, len, kWindow, [&](uint64_t w0, uint64_t w1) {
+        const uint64_t e0 = b0 + w0;
+        FusedArgs a{rows + e0, g->row_stride, g->nd, split_window(g->offset + e0, w1 - w0),
+                    in->master + e0, in->m + e0, in->v + e0, out->master + e0, out->m + e0,
+                    out->v + e0, gath + e0, k, d_nonfinite, gate};
+        const int width = store_width(gath + e0 + a.sp.head);
+        if (g->dtype == ZERO_F16)
+            launch_fused_dt<ZERO_F16>(a, width, v8, variant, s);
+        else
+            launch_fused_dt<ZERO_BF16>(a, width, v8, variant, s);
+        return launch_status();
+    });
+}
+
 }  // namespace zero
 
 using namespace zero;
@@ -980,27 +1011,13 @@ extern "C" zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layou
     st = resolve_grads(g, &gr, &host_rows);
     if (st != ZERO_OK)
         return st;
-    const int variant = fused_variant(host_rows);
     const StepScalars k = make_scalars(h, g->nd, loss_scale);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     const uint16_t* rows = static_cast<const uint16_t*>(gr.base) + g->offset;
     uint16_t* gath = static_cast<uint16_t*>(gathered) + gathered_offset_elems;
-    const float* const sp[6] = {in->master, in->m, in->v, out->master, out->m, out->v};
-    const bool v8 = state_v8_ok(sp);
     for (uint64_t b0 = 0; b0 < n; b0 += bucket_elems) {
         const uint64_t len = n - b0 < bucket_elems ? n - b0 : bucket_elems;
-        st = for_each_window(g->offset + b0, len, kWindow, [&](uint64_t w0, uint64_t w1) {
-            const uint64_t e0 = b0 + w0;
-            FusedArgs a{rows + e0, g->row_stride, g->nd, split_window(g->offset + e0, w1 - w0),
-                        in->master + e0, in->m + e0, in->v + e0, out->master + e0,
-                        out->m + e0, out->v + e0, gath + e0, k, d_nonfinite};
-            const int width = store_width(gath + e0 + a.sp.head);
-            if (g->dtype == ZERO_F16)
-                launch_fused_dt<ZERO_F16>(a, width, v8, variant, s);
-            else
-                launch_fused_dt<ZERO_BF16>(a, width, v8, variant, s);
-            return launch_status();
-        });
+        st = launch_fused_bucket(rows, g, in, out, gath, b0, len, k, host_rows, d_nonfinite,
+                                 nullptr, stream);
         if (st != ZERO_OK)
             return st;
         if (len < bucket_elems)
