@@ -670,7 +670,7 @@ def run_entry(args) -> None:
                                           dps.loss_scale, dps.h, ready, 1, 10 ** 10, dps.flag,
                                           status, stream)
             dps.commit(False)
-        bpp, launches = 2 * w.nd + 26, _abi.streamed_launch_count(n, sb, 0)
+        bpp, launches = 2 * w.nd + 26, _abi.streamed_launch_count(n, sb, w.nd, 0)
     else:
         def call():
             dps.launch(desc)

@@ -259,10 +259,12 @@ zero_status_t zero_check_nonfinite(const zero_grads_t* g, uint64_t begin, uint64
 
 /* The fused step started bucket by bucket as gradients arrive ("ZeRO-DP",
  * Stage 2: gradients are reduce-scattered in buckets during the backward
- * pass).  For each bucket b in order (elements [b*bucket_elems, ...) of the
- * shard), a one-thread kernel waits until d_ready[b] >= epoch (wrap-around
- * comparison), then the fused step's launches for the bucket follow on the
- * same stream (as zero_step_shard: launch windows of at most
+ * pass).  Bucket b is elements [b*bucket_elems, ...) of the shard.
+ * Consecutive buckets form launch groups of at least ZERO_STREAM_GROUP_BYTES
+ * of step traffic ((2*nd + 26) bytes per element); for each group in order a
+ * one-thread kernel waits until d_ready[b] >= epoch (wrap-around comparison)
+ * for each of its buckets, then the fused step's launches for the group follow
+ * on the same stream (as zero_step_shard: launch windows of at most
  * ZERO_FUSED_WINDOW_ELEMS elements, the same kernel variant).  The producer
  * of bucket b
  * writes d_ready[b] after the bucket's contributions are in place -- e.g. a
@@ -276,6 +278,7 @@ zero_status_t zero_check_nonfinite(const zero_grads_t* g, uint64_t begin, uint64
  * timeout_ns must be in [1, ZERO_MAX_WAIT_NS] (ZERO_ERR_INVALID_ARG otherwise).
  * Other arguments, alignment and results as zero_step_shard (bitwise equal). */
 #define ZERO_MAX_WAIT_NS 60000000000ull
+#define ZERO_STREAM_GROUP_BYTES 500000000ull
 zero_status_t zero_step_shard_streamed(const zero_grads_t* g, const zero_layout_t* L,
                                        const zero_state_t* in, const zero_state_t* out,
                                        void* gathered, uint64_t gathered_offset_elems,

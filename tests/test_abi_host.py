@@ -213,7 +213,7 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
 def test_binding_constants_match_header(z):
     text = open(os.path.join(ROOT, "include", "zero.h")).read()
     for name in ("ZERO_FUSED_WINDOW_ELEMS", "ZERO_STATIC_CB_ELEMS",
-                 "ZERO_GATHER_SEGMENTS_PER_LAUNCH"):
+                 "ZERO_GATHER_SEGMENTS_PER_LAUNCH", "ZERO_STREAM_GROUP_BYTES"):
         m = re.search(rf"#define {name} (\d+)ull", text)
         assert m and int(m.group(1)) == getattr(z._abi, name), name
     m = re.search(r"#define ZERO_STEP_FLAG_WAIT_TIMEOUT (0x[0-9A-Fa-f]+)u", text)
@@ -229,6 +229,15 @@ def test_binding_constants_match_header(z):
     # unfused: the reduction in the same windows, plus AdamW and cast, per bucket
     assert z._abi.unfused_launch_count(117_187_500, 500_000_000) == 5 + 2
     assert z._abi.unfused_launch_count(262_144, 65_536) == 4 * 3
+    # bucket-ready groups: 7.3M-element buckets at Nd = 64 (1.1 GB each) stand
+    # alone; 1.46M-element ones group by 3 (225 MB each); the groups tile the shard
+    g4 = z._abi.stream_groups(117_187_500, 7_324_224, 64)
+    g3 = z._abi.stream_groups(23_437_500, 1_464_848, 64)
+    assert len(g4) == 16 and [x[1] for x in g3[:-1]] == [3 * 1_464_848] * 5
+    for gs, n in ((g4, 117_187_500), (g3, 23_437_500)):
+        assert gs[0][0] == 0 and sum(x[1] for x in gs) == n
+        assert all(a[0] + a[1] == b[0] for a, b in zip(gs, gs[1:]))
+    assert z._abi.streamed_launch_count(117_187_500, 7_324_224, 64) == 16 * 2
     # a whole 64-shard vector is 64 segments: two gather launches; a layer
     # range inside one shard is one
     assert z._abi.gather_launch_count(1_500_000_000, 64, 0, 1_500_000_000) == 2

@@ -111,10 +111,30 @@ def fused_launch_count(n: int, bucket: int, offset: int = 0) -> int:
     return sum(_windows(min(bucket, n - b0), offset + b0) for b0 in range(0, n, bucket))
 
 
-def streamed_launch_count(n: int, bucket: int, offset: int = 0) -> int:
-    """Kernel launches zero_step_shard_streamed issues: per bucket, one wait
-    and the fused step's launch windows."""
-    return sum(1 + _windows(min(bucket, n - b0), offset + b0) for b0 in range(0, n, bucket))
+# Least step traffic of a launch group of zero_step_shard_streamed (zero.h).
+ZERO_STREAM_GROUP_BYTES = 500000000
+
+
+def stream_groups(n: int, bucket: int, nd: int) -> list:
+    """The launch groups of zero_step_shard_streamed: (first element, length)
+    of each run of consecutive buckets with at least ZERO_STREAM_GROUP_BYTES
+    of step traffic (the last group may have less)."""
+    min_group = ZERO_STREAM_GROUP_BYTES // (2 * nd + 26) + 1
+    nb = -(-n // bucket)
+    groups, b = [], 0
+    while b < nb:
+        g0, b_end = b * bucket, b + 1
+        while b_end < nb and b_end * bucket - g0 < min_group:
+            b_end += 1
+        groups.append((g0, min(b_end * bucket, n) - g0))
+        b = b_end
+    return groups
+
+
+def streamed_launch_count(n: int, bucket: int, nd: int, offset: int = 0) -> int:
+    """Kernel launches zero_step_shard_streamed issues: per launch group, one
+    wait and the fused step's launch windows."""
+    return sum(1 + _windows(glen, offset + g0) for g0, glen in stream_groups(n, bucket, nd))
 
 
 def unfused_launch_count(n: int, bucket: int, offset: int = 0) -> int:

@@ -58,15 +58,19 @@ __device__ bool wait_ready(const uint32_t* word, uint32_t epoch, uint64_t timeou
     return (int32_t)(ld_acquire(word) - epoch) >= 0;
 }
 
-// One bucket's wait: a single thread polls the ready word (bounded).  If an
-// earlier wait of the call ran out (status nonzero), it does not wait again.
-__global__ void k_wait_ready(const uint32_t* word, uint32_t epoch, uint64_t timeout_ns,
-                             uint32_t* status)
+// One launch group's wait: a single thread polls the ready words of `count`
+// consecutive buckets in order (each wait bounded).  If an earlier wait of
+// the call ran out (status nonzero), it does not wait again.
+__global__ void k_wait_ready(const uint32_t* words, uint32_t count, uint32_t epoch,
+                             uint64_t timeout_ns, uint32_t* status)
 {
     if (*static_cast<volatile uint32_t*>(status) != 0)
         return;
-    if (!wait_ready(word, epoch, timeout_ns))
-        atomicCAS(status, 0u, (uint32_t)ZERO_ERR_TIMEOUT);
+    for (uint32_t i = 0; i < count; ++i)
+        if (!wait_ready(words + i, epoch, timeout_ns)) {
+            atomicCAS(status, 0u, (uint32_t)ZERO_ERR_TIMEOUT);
+            return;
+        }
 }
 
 bool is_aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
@@ -128,17 +132,27 @@ extern "C" zero_status_t zero_step_shard_streamed(
     const uint16_t* rows = static_cast<const uint16_t*>(gr.base) + g->offset;
     uint16_t* gath = static_cast<uint16_t*>(gathered) + gathered_offset_elems;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    for (uint64_t b0 = 0, b = 0; b0 < n; b0 += bucket_elems, ++b) {
-        const uint64_t len = n - b0 < bucket_elems ? n - b0 : bucket_elems;
-        k_wait_ready<<<1, 1, 0, st>>>(d_ready + b, epoch, timeout_ns, d_status);
+    // Consecutive buckets form launch groups of at least
+    // ZERO_STREAM_GROUP_BYTES of step traffic, so that each group's launches
+    // outweigh their fixed cost; a group starts once all its buckets landed.
+    const uint64_t min_group = ZERO_STREAM_GROUP_BYTES / (2ull * g->nd + 26) + 1;
+    const uint64_t nb = (n + bucket_elems - 1) / bucket_elems;
+    for (uint64_t b = 0; b < nb;) {
+        const uint64_t g0 = b * bucket_elems;
+        uint64_t b_end = b;
+        do {
+            ++b_end;
+        } while (b_end < nb && b_end * bucket_elems - g0 < min_group);
+        const uint64_t glen = (b_end * bucket_elems < n ? b_end * bucket_elems : n) - g0;
+        k_wait_ready<<<1, 1, 0, st>>>(d_ready + b, (uint32_t)(b_end - b), epoch, timeout_ns,
+                                      d_status);
         if (cudaGetLastError() != cudaSuccess)
             return ZERO_ERR_CUDA;
-        const zero_status_t ls = launch_fused_bucket(rows, g, in, out, gath, b0, len, k,
+        const zero_status_t ls = launch_fused_bucket(rows, g, in, out, gath, g0, glen, k,
                                                      host_rows, d_nonfinite, d_status, stream);
         if (ls != ZERO_OK)
             return ls;
-        if (len < bucket_elems)
-            break;
+        b = b_end;
     }
     return ZERO_OK;
 }

@@ -250,7 +250,8 @@ class DataParallelStep:
                                self._ready, self._epoch_host, copy_stream)
         self._feed_done = torch.cuda.Event()
         self._feed_done.record(copy_stream)
-        return _abi.streamed_launch_count(n, stream_bucket, int(dev_grads.offset))
+        return _abi.streamed_launch_count(n, stream_bucket, int(dev_grads.nd),
+                                          int(dev_grads.offset))
 
     def host_fed_status(self) -> int:
         """ZERO_OK, or ZERO_ERR_TIMEOUT if a bucket never arrived (read after
