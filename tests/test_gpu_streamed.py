@@ -51,10 +51,16 @@ def _fused_reference(w, dps, rank, g, bucket):
     return out, gath
 
 
+@pytest.mark.parametrize("group_bytes", [None, "0"])
 @pytest.mark.parametrize("psi,nd,rank,dt,bucket", [(400_003, 8, 3, "bf16", 7_000),
                                                    (250_000, 64, 1, "f16", 1_001),
                                                    (90_001, 5, 4, "f16", 90_001)])
-def test_streamed_matches_fused(psi, nd, rank, dt, bucket):
+def test_streamed_matches_fused(psi, nd, rank, dt, bucket, group_bytes, monkeypatch):
+    # default launch groups (here one group of all buckets), and one group a bucket
+    if group_bytes is None:
+        monkeypatch.delenv("ZERO_STREAM_GROUP_BYTES", raising=False)
+    else:
+        monkeypatch.setenv("ZERO_STREAM_GROUP_BYTES", group_bytes)
     w, dps, rows, g = _setup(psi, nd, rank, dt)
     out_ref, gath_ref = _fused_reference(w, dps, rank, g, bucket)
     L = dps.layouts[rank]
@@ -88,7 +94,8 @@ def test_streamed_matches_fused(psi, nd, rank, dt, bucket):
     assert np.array_equal(u16(gath[b:b + n]), u16(gath_ref[b:b + n]))
 
 
-def test_wait_that_nothing_satisfies_times_out():
+def test_wait_that_nothing_satisfies_times_out(monkeypatch):
+    monkeypatch.setenv("ZERO_STREAM_GROUP_BYTES", "0")     # every bucket its own group
     psi, nd, rank, bucket = 300_000, 4, 0, 10_000
     w, dps, rows, g = _setup(psi, nd, rank, "bf16")
     out_ref, _ = _fused_reference(w, dps, rank, g, bucket)
@@ -168,3 +175,29 @@ def test_feeder_rejects_short_rows():
     with pytest.raises(z.ZeroError) as e:
         z.zero_feed_buckets(host, 10, g, 500, 128, ready, ep, None)
     assert e.value.status == z.ZERO_ERR_INVALID_ARG
+
+
+def test_a_group_waits_for_all_its_buckets(monkeypatch):
+    """With the default grouping the 8 small buckets form one launch group:
+    one bucket that never lands keeps the whole group untouched."""
+    monkeypatch.delenv("ZERO_STREAM_GROUP_BYTES", raising=False)
+    psi, nd, rank, bucket = 300_000, 4, 0, 10_000
+    w, dps, rows, g = _setup(psi, nd, rank, "bf16")
+    L = dps.layouts[rank]
+    n = int(L.length)
+    assert len(z._abi.stream_groups(n, bucket, nd)) == 1
+    ready = torch.ones(-(-n // bucket), dtype=torch.int32, device=DEV)
+    ready[-1] = 0                                   # the last bucket never arrives
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    st = dps.state[rank]
+    out = torch.full_like(st.bufs[0], -1.0)
+    gath = torch.zeros_like(dps.gathered[0])
+    h = z.adamw(w.hparams["lr"], 0.9, 0.999, 1e-8, 0.01, 1)
+    torch.cuda.synchronize()
+    z.zero_step_shard_streamed(g, L, st.states[st.cur], z.state(*out), gath, L.begin, bucket,
+                               w.loss_scale, h, ready, 1, 20_000_000, flag, status, None)
+    torch.cuda.synchronize()
+    assert int(status.item()) == z.ZERO_ERR_TIMEOUT
+    assert bool((out[:, :n] == -1.0).all()), "a bucket of an incomplete group was touched"
+

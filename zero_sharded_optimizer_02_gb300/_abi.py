@@ -119,7 +119,9 @@ def stream_groups(n: int, bucket: int, nd: int) -> list:
     """The launch groups of zero_step_shard_streamed: (first element, length)
     of each run of consecutive buckets with at least ZERO_STREAM_GROUP_BYTES
     of step traffic (the last group may have less)."""
-    min_group = ZERO_STREAM_GROUP_BYTES // (2 * nd + 26) + 1
+    env = os.environ.get("ZERO_STREAM_GROUP_BYTES", "")
+    group_bytes = int(env) if env.isdigit() else ZERO_STREAM_GROUP_BYTES
+    min_group = group_bytes // (2 * nd + 26) + 1
     nb = -(-n // bucket)
     groups, b = [], 0
     while b < nb:

@@ -21,6 +21,7 @@
 // written by a copy engine or the host.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "zero_device.cuh"
 
@@ -133,9 +134,17 @@ extern "C" zero_status_t zero_step_shard_streamed(
     uint16_t* gath = static_cast<uint16_t*>(gathered) + gathered_offset_elems;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // Consecutive buckets form launch groups of at least
-    // ZERO_STREAM_GROUP_BYTES of step traffic, so that each group's launches
-    // outweigh their fixed cost; a group starts once all its buckets landed.
-    const uint64_t min_group = ZERO_STREAM_GROUP_BYTES / (2ull * g->nd + 26) + 1;
+    // ZERO_STREAM_GROUP_BYTES of step traffic (or the environment variable of
+    // that name, read at each call), so that each group's launches outweigh
+    // their fixed cost; a group starts once all its buckets landed.
+    uint64_t group_bytes = ZERO_STREAM_GROUP_BYTES;
+    if (const char* e = getenv("ZERO_STREAM_GROUP_BYTES")) {
+        char* end = nullptr;
+        const unsigned long long v = strtoull(e, &end, 10);
+        if (end != e && *end == '\0')
+            group_bytes = v;
+    }
+    const uint64_t min_group = group_bytes / (2ull * g->nd + 26) + 1;
     const uint64_t nb = (n + bucket_elems - 1) / bucket_elems;
     for (uint64_t b = 0; b < nb;) {
         const uint64_t g0 = b * bucket_elems;
