@@ -319,92 +319,106 @@ def run_gpu(args) -> None:
     #    sequential form (copy everything, then step) is timed beside it. -----
     e2e = None
     if args.e2e_steps > 0:
-        host_grads = torch.empty(grads.shape, dtype=grads.dtype, pin_memory=True)
-        host_grads.copy_(grads)
-        host_params = torch.empty(n, dtype=grads.dtype, pin_memory=True)
-        copy_stream = torch.cuda.Stream(dev)
-        stream_bucket = max(8, -(-(-(-n // args.e2e_buckets)) // 8) * 8)
-        slot0 = int(L.begin) if args.gathered == "full" else 0   # the rank's parameters
+        # the step's gradients in page-locked host memory (each rank its own);
+        # every rank must have them, or no rank runs the end-to-end leg
+        pin_gb = (grads.numel() + n) * grads.element_size() / 1e9
+        try:
+            host_grads = torch.empty(grads.shape, dtype=grads.dtype, pin_memory=True)
+            host_grads.copy_(grads)
+            host_params = torch.empty(n, dtype=grads.dtype, pin_memory=True)
+            pin_error = ""
+        except RuntimeError as err:
+            host_grads = host_params = None
+            pin_error = str(err).splitlines()[0][:160] if str(err) else type(err).__name__
+        pinned_everywhere = -max_over_ranks(-float(not pin_error), group, dev) > 0.5
+        if not pinned_everywhere:
+            e2e = {"unavailable": f"could not pin {pin_gb:.1f} GB of host memory on every rank"
+                                  + (f" ({pin_error})" if pin_error else "")}
+            host_grads = host_params = None
+        else:
+            copy_stream = torch.cuda.Stream(dev)
+            stream_bucket = max(8, -(-(-(-n // args.e2e_buckets)) // 8) * 8)
+            slot0 = int(L.begin) if args.gathered == "full" else 0   # the rank's parameters
 
-        gview = dps.gathered_view(dp_rank)
+            gview = dps.gathered_view(dp_rank)
 
-        def read_back():
-            with torch.cuda.stream(stream):
-                host_params.copy_(gview[slot0:slot0 + n], non_blocking=True)
-            stream.synchronize()
+            def read_back():
+                with torch.cuda.stream(stream):
+                    host_params.copy_(gview[slot0:slot0 + n], non_blocking=True)
+                stream.synchronize()
 
-        def host_fed():
-            dps.launch_host_fed(dp_rank, host_grads, desc[dp_rank], stream_bucket, copy_stream)
-            dps.commit(dps.decide())
-            read_back()
+            def host_fed():
+                dps.launch_host_fed(dp_rank, host_grads, desc[dp_rank], stream_bucket, copy_stream)
+                dps.commit(dps.decide())
+                read_back()
 
-        def sequential():
-            with torch.cuda.stream(stream):
-                grads.copy_(host_grads, non_blocking=True)
-            dps.step(desc)
-            read_back()
+            def sequential():
+                with torch.cuda.stream(stream):
+                    grads.copy_(host_grads, non_blocking=True)
+                dps.step(desc)
+                read_back()
 
-        host_desc = {dp_rank: _abi.grads(host_grads, row_stride, 0, w.nd, w.grad_dtype)}
+            host_desc = {dp_rank: _abi.grads(host_grads, row_stride, 0, w.nd, w.grad_dtype)}
 
-        def zero_copy():      # the fused kernels read the gradients in host memory
-            dps.step(host_desc)
-            read_back()
+            def zero_copy():      # the fused kernels read the gradients in host memory
+                dps.step(host_desc)
+                read_back()
 
-        def copies_alone():   # the host link alone: the same bytes, no step
-            with torch.cuda.stream(stream):
-                grads.copy_(host_grads, non_blocking=True)
-            read_back()
+            def copies_alone():   # the host link alone: the same bytes, no step
+                with torch.cuda.stream(stream):
+                    grads.copy_(host_grads, non_blocking=True)
+                read_back()
 
-        # The three forms run interleaved, one of each per iteration, so that
-        # they see the same host-memory conditions (the host is shared); the
-        # first iteration is untimed.  Each is timed on the host around the
-        # whole call, its final synchronisation included.
-        forms = {"fed": host_fed, "sequential": sequential, "zero_copy": zero_copy,
-                 "copies": copies_alone}
-        times = {k: [] for k in forms}
-        for it in range(args.e2e_steps + 1):
-            for k, fn in forms.items():
-                if world > 1:
-                    dist.barrier()
-                torch.cuda.synchronize(dev)
-                t0 = time.perf_counter()
-                fn()
-                if it:
-                    times[k].append((time.perf_counter() - t0) * 1e3)
-        assert dps.host_fed_status() == 0, "a bucket never arrived"
-        mean = {k: max_over_ranks(statistics.fmean(v), group, dev) for k, v in times.items()}
-        best = {k: max_over_ranks(min(v), group, dev) for k, v in times.items()}
-        grad_bytes = w.nd * n * host_grads.element_size()
-        nbk = -(-n // stream_bucket)
+            # The three forms run interleaved, one of each per iteration, so that
+            # they see the same host-memory conditions (the host is shared); the
+            # first iteration is untimed.  Each is timed on the host around the
+            # whole call, its final synchronisation included.
+            forms = {"fed": host_fed, "sequential": sequential, "zero_copy": zero_copy,
+                     "copies": copies_alone}
+            times = {k: [] for k in forms}
+            for it in range(args.e2e_steps + 1):
+                for k, fn in forms.items():
+                    if world > 1:
+                        dist.barrier()
+                    torch.cuda.synchronize(dev)
+                    t0 = time.perf_counter()
+                    fn()
+                    if it:
+                        times[k].append((time.perf_counter() - t0) * 1e3)
+            assert dps.host_fed_status() == 0, "a bucket never arrived"
+            mean = {k: max_over_ranks(statistics.fmean(v), group, dev) for k, v in times.items()}
+            best = {k: max_over_ranks(min(v), group, dev) for k, v in times.items()}
+            grad_bytes = w.nd * n * host_grads.element_size()
+            nbk = -(-n // stream_bucket)
 
-        def form(k, path, h2d):
-            return {"ms_per_step": mean[k], "ms_per_step_min": best[k],
-                    "value": world * n / (mean[k] * 1e-3), "path": path,
-                    "h2d_bytes_per_step": h2d}
-        # The headline is the zero-copy form: the kernels read the step's
-        # gradients in place in pinned host memory, so the same bytes cross
-        # the host link every step without a device copy; it runs steadily
-        # where the copy engines' time varies with the shared host.
-        e2e = {"value": world * n / (mean["zero_copy"] * 1e-3), "unit": UNIT,
-               "h2d_bytes_per_step": grad_bytes,
-               "d2h_bytes_per_step": n * host_params.element_size() + 4,
-               "ms_per_step": mean["zero_copy"], "ms_per_step_min": best["zero_copy"],
-               "steps": args.e2e_steps,
-               "path": "zero_step_shard reading the Nd gradient rows in place in pinned host "
-                       "memory (zero-copy over the host link), then the flag and the new "
-                       "parameters device-to-host",
-               "other_forms": {
-                   "fed": form("fed", f"zero_feed_buckets (DMA, {nbk} transfer buckets) + "
-                                      "zero_step_shard_streamed", grad_bytes + 4 * nbk),
-                   "sequential": form("sequential", "one DMA copy of the gradients, then "
-                                                    "zero_step_shard", grad_bytes),
-                   "copies_alone": form("copies", "the DMA copies alone, no step",
-                                        grads.numel() * grads.element_size())},
-               "ms_per_iteration": {k: [round(x, 3) for x in v] for k, v in times.items()},
-               "link": {"bound_ms": best["copies"],
-                        "bound": "the fastest iteration of the DMA copies alone",
-                        "frac": best["copies"] / mean["zero_copy"]}}
-        del host_grads, host_params
+            def form(k, path, h2d):
+                return {"ms_per_step": mean[k], "ms_per_step_min": best[k],
+                        "value": world * n / (mean[k] * 1e-3), "path": path,
+                        "h2d_bytes_per_step": h2d}
+            # The headline is the zero-copy form: the kernels read the step's
+            # gradients in place in pinned host memory, so the same bytes cross
+            # the host link every step without a device copy; it runs steadily
+            # where the copy engines' time varies with the shared host.
+            e2e = {"value": world * n / (mean["zero_copy"] * 1e-3), "unit": UNIT,
+                   "h2d_bytes_per_step": grad_bytes,
+                   "d2h_bytes_per_step": n * host_params.element_size() + 4,
+                   "ms_per_step": mean["zero_copy"], "ms_per_step_min": best["zero_copy"],
+                   "steps": args.e2e_steps,
+                   "path": "zero_step_shard reading the Nd gradient rows in place in pinned host "
+                           "memory (zero-copy over the host link), then the flag and the new "
+                           "parameters device-to-host",
+                   "other_forms": {
+                       "fed": form("fed", f"zero_feed_buckets (DMA, {nbk} transfer buckets) + "
+                                          "zero_step_shard_streamed", grad_bytes + 4 * nbk),
+                       "sequential": form("sequential", "one DMA copy of the gradients, then "
+                                                        "zero_step_shard", grad_bytes),
+                       "copies_alone": form("copies", "the DMA copies alone, no step",
+                                            grads.numel() * grads.element_size())},
+                   "ms_per_iteration": {k: [round(x, 3) for x in v] for k, v in times.items()},
+                   "link": {"bound_ms": best["copies"],
+                            "bound": "the fastest iteration of the DMA copies alone",
+                            "frac": best["copies"] / mean["zero_copy"]}}
+            del host_grads, host_params
 
     if rank != 0:
         if world > 1:
