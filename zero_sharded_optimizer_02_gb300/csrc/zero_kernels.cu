@@ -143,6 +143,8 @@ static_assert(kTmaConsumers % 32 == 0 && kTmaStages <= 32, "TMA pipeline shape")
 static_assert(kTmaBytes <= 227 * 1024, "TMA rings exceed shared memory");
 static_assert(kTmaStageBytes < (1u << 20) && kTmaStateSlotBytes < (1u << 20),
               "a slot exceeds an mbarrier phase");
+// Longest wait on a pipeline barrier before the kernel gives up (a healthy
+// wait lasts microseconds), and on each in-flight copy after giving up.
 constexpr uint64_t kTmaWaitNs = 10ull * 1000 * 1000 * 1000;
 constexpr uint64_t kTmaDrainNs = 1000ull * 1000 * 1000;
 
