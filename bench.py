@@ -107,6 +107,8 @@ def workload(args):
     w = synth.WORKLOADS[args.config]
     if args.psi:
         w = dataclasses.replace(w, psi=args.psi, plant=None)
+    if args.nd:
+        w = dataclasses.replace(w, nd=args.nd, plant=None)
     if args.bucket:
         w = dataclasses.replace(w, bucket=args.bucket)
     if args.grad_dtype and args.grad_dtype != w.grad_dtype:
@@ -438,7 +440,8 @@ def run_gpu(args) -> None:
     peak = peaks.get("hbm_gbs")
     peak_src = "measured" if peak else "fallback"
     peak = peak or 6800.0
-    traffic_pp = None if (args.psi or args.grad_dtype or args.row_pad or args.bucket) else \
+    traffic_pp = None if (args.psi or args.nd or args.grad_dtype or args.row_pad or
+                          args.bucket) else \
         recorded_traffic(args.config)
     line = {
         "metric": METRIC,
@@ -454,7 +457,8 @@ def run_gpu(args) -> None:
         "dtype": "f32",
         "data": "synthetic (seeded counter-based generator; no dataset or weights)",
         "config": {"workload": f"{args.config}: {w.title}" + (
-                       " (overridden)" if (args.psi or args.grad_dtype or args.bucket) else ""),
+                       " (overridden)" if (args.psi or args.nd or args.grad_dtype or args.bucket)
+                       else ""),
                    "psi": w.psi, "nd": w.nd,
                    "rank": dp_rank, "shard_params": n, "grad_dtype": w.grad_dtype,
                    "bucket": w.bucket, "loss_scale": w.loss_scale,
@@ -849,6 +853,7 @@ def main():
                          "r*S of the flat Nd*S buffer (odd ranks then start off the 16-byte "
                          "boundary when S mod 8 != 0)")
     ap.add_argument("--psi", type=int, default=0, help="override the parameter count")
+    ap.add_argument("--nd", type=int, default=0, help="override the data-parallel degree")
     ap.add_argument("--bucket", type=int, default=0, help="override the bucket size")
     ap.add_argument("--grad-dtype", choices=["f16", "bf16"], default=None,
                     help="override the gradient dtype")
