@@ -39,16 +39,19 @@ def variant(request, monkeypatch):
     return request.param
 
 
+@pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("variant", VARIANTS, indirect=True)
-def test_c0_matches_oracle(variant):
+def test_c0_matches_oracle(variant, fused):
+    """Fused, and unfused (whose reduction follows the variant: the ring's
+    reduction mode, or the register kernel)."""
     w = synth.WORKLOADS["c0"]
-    dps = make_group(w)
+    dps = make_group(w, fused=fused)
     _, hist = oracle_trajectory(w, np.arange(w.psi), w.steps)
     buf = None
     for k in range(w.steps):
         buf, desc = full_rows(w, dps, k, buf)
         assert not dps.step(desc)
-        check_against_oracle(w, dps, hist[k], f"{variant} c0 step {k}")
+        check_against_oracle(w, dps, hist[k], f"{variant} fused={fused} c0 step {k}")
 
 
 @pytest.mark.parametrize("psi,nd,dt,bucket", EDGE_CASES)

@@ -335,6 +335,7 @@ struct FusedArgs {
     StepScalars k;
     uint32_t* flag;
     const uint32_t* gate;  // if non-null and nonzero at launch, the launch does nothing
+    float* cb;             // reduction-only launches: cb[e] = sum * k.inv (null: check only)
 };
 
 // True if the launch is gated off (a bucket wait before it ran out).

@@ -177,7 +177,49 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_step_fused(const Fused
 // reads are contiguous.  Only the issuing thread reads its slots, so
 // cp.async.wait_group needs no block barrier.  Rows are still folded in
 // rank order.
-template <int DT, int W, bool V8>
+// Epilogue modes of the ring kernel: the whole step, or the reduction alone
+// (K1: scaled sums into the fusion buffer; K5: the nonfinite check).
+constexpr int kModeStep = 0;
+constexpr int kModeReduce = 1;
+constexpr int kModeCheck = 2;
+
+// Reduction-only epilogue of 8 sums at window element e: the nonfinite test,
+// and for K1 the scaled sums into cb (VEC: cb + e is 16-byte aligned).
+template <int MODE, bool VEC>
+__device__ __forceinline__ bool reduce_epilogue(const FusedArgs& a, uint64_t e,
+                                                const float (&s)[8])
+{
+    bool bad = false;
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        bad |= nonfinite(s[i]);
+        x[i] = __fmul_rn(s[i], a.k.inv);
+    }
+    if (MODE == kModeReduce) {
+        if (VEC) {
+            __stcg(reinterpret_cast<float4*>(a.cb + e), make_float4(x[0], x[1], x[2], x[3]));
+            __stcg(reinterpret_cast<float4*>(a.cb + e) + 1, make_float4(x[4], x[5], x[6], x[7]));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                __stcg(a.cb + e + i, x[i]);
+        }
+    }
+    return bad;
+}
+
+// Scalar element e of a reduction-only launch.
+template <int DT, int MODE>
+__device__ __forceinline__ bool reduce_scalar(const FusedArgs& a, uint64_t e)
+{
+    const float s = fold1<DT>(a.g + e, a.row_stride, a.nd);
+    if (MODE == kModeReduce)
+        a.cb[e] = __fmul_rn(s, a.k.inv);
+    return nonfinite(s);
+}
+
+template <int DT, int W, bool V8, int MODE = kModeStep>
 __global__ void __launch_bounds__(kRingThreads, 1) k_step_fused_ring(const FusedArgs a)
 {
     extern __shared__ uint4 ring[];
@@ -187,8 +229,12 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_step_fused_ring(const Fused
     const int t = threadIdx.x;
     const uint64_t tid = (uint64_t)blockIdx.x * kRingThreads + t;
     const uint64_t nthr = (uint64_t)gridDim.x * kRingThreads;
-    if (tid < a.sp.nscalar())
-        bad |= fused_scalar<DT>(a, a.sp.scalar_elem(tid));
+    if (tid < a.sp.nscalar()) {
+        if (MODE == kModeStep)
+            bad |= fused_scalar<DT>(a, a.sp.scalar_elem(tid));
+        else
+            bad |= reduce_scalar<DT, MODE>(a, a.sp.scalar_elem(tid));
+    }
 
     const uint32_t groups = (a.nd + kRingRows - 1) / kRingRows;   // groups per vector
     const uint16_t* base = a.g + a.sp.head;
@@ -221,7 +267,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_step_fused_ring(const Fused
     uint32_t gc = 0;
     float acc[8];
     float sp[8], sm[8], sv[8];     // the current vector's state (prefetch mode)
-    constexpr bool kPrefetch = V8 && ZERO_STATE_PREFETCH;
+    constexpr bool kPrefetch = MODE == kModeStep && V8 && ZERO_STATE_PREFETCH;
     for (uint64_t qc = tid; qc < a.sp.nvec;) {
         issue();
         cp_async_wait<kRingDepth - 1>();     // the oldest group has landed
@@ -245,7 +291,9 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_step_fused_ring(const Fused
         slot_c = slot_c + 1 == kRingDepth ? 0 : slot_c + 1;
         if (++gc == groups) {
             gc = 0;
-            if (kPrefetch)
+            if (MODE != kModeStep)
+                bad |= reduce_epilogue<MODE, W == 16>(a, a.sp.head + 8 * qc, acc);
+            else if (kPrefetch)
                 bad |= fused_epilogue_loaded<DT, W>(a, a.sp.head + 8 * qc, acc, sp, sm, sv);
             else
                 bad |= fused_epilogue<DT, W, V8>(a, a.sp.head + 8 * qc, acc);
@@ -796,17 +844,52 @@ void launch_fused_dt(const FusedArgs& a, int width, bool v8, int variant, cudaSt
         launch_fused_v<DT, false>(a, width, variant, s);
 }
 
-void launch_reduce(const ReduceArgs& a, int dtype, cudaStream_t s)
+template <int DT, bool VEC, int MODE>
+void launch_reduce_ring(const FusedArgs& a, cudaStream_t s)
 {
-    const unsigned grid = grid_for(a.sp.nvec > a.sp.nscalar() ? a.sp.nvec : a.sp.nscalar());
-    const bool vec = a.cb == nullptr || aligned(a.cb + a.sp.head, 16);
-    if (dtype == ZERO_F16) {
-        if (vec) k_reduce<ZERO_F16, true><<<grid, kThreads, 0, s>>>(a);
-        else k_reduce<ZERO_F16, false><<<grid, kThreads, 0, s>>>(a);
-    } else {
-        if (vec) k_reduce<ZERO_BF16, true><<<grid, kThreads, 0, s>>>(a);
-        else k_reduce<ZERO_BF16, false><<<grid, kThreads, 0, s>>>(a);
+    static std::atomic<uint64_t> opted{0};
+    smem_opt_in(k_step_fused_ring<DT, VEC ? 16 : 4, false, MODE>, kRingBytes, opted);
+    const uint64_t work = a.sp.nvec > a.sp.nscalar() ? a.sp.nvec : a.sp.nscalar();
+    const uint64_t want = (work + kRingThreads - 1) / kRingThreads;
+    const uint64_t cap = (uint64_t)sm_count();
+    const unsigned grid = (unsigned)(want < cap ? (want ? want : 1) : cap);
+    k_step_fused_ring<DT, VEC ? 16 : 4, false, MODE><<<grid, kRingThreads, kRingBytes, s>>>(a);
+}
+
+// K1 (a.cb != nullptr) or K5 over one window: the ring kernel's reduction
+// modes, or the register kernel k_reduce for the register variant.
+void launch_reduce(const ReduceArgs& r, int dtype, int variant, cudaStream_t s)
+{
+    const bool vec = r.cb == nullptr || aligned(r.cb + r.sp.head, 16);
+    if (variant == 0) {
+        const unsigned grid = grid_for(r.sp.nvec > r.sp.nscalar() ? r.sp.nvec : r.sp.nscalar());
+        if (dtype == ZERO_F16) {
+            if (vec) k_reduce<ZERO_F16, true><<<grid, kThreads, 0, s>>>(r);
+            else k_reduce<ZERO_F16, false><<<grid, kThreads, 0, s>>>(r);
+        } else {
+            if (vec) k_reduce<ZERO_BF16, true><<<grid, kThreads, 0, s>>>(r);
+            else k_reduce<ZERO_BF16, false><<<grid, kThreads, 0, s>>>(r);
+        }
+        return;
     }
+    FusedArgs a{};
+    a.g = r.g;
+    a.row_stride = r.row_stride;
+    a.nd = r.nd;
+    a.sp = r.sp;
+    a.k.inv = r.inv;
+    a.flag = r.flag;
+    a.cb = r.cb;
+#define ZERO_REDUCE_RING(DT)                                                         \
+    if (r.cb && vec) launch_reduce_ring<DT, true, kModeReduce>(a, s);                 \
+    else if (r.cb) launch_reduce_ring<DT, false, kModeReduce>(a, s);                  \
+    else launch_reduce_ring<DT, true, kModeCheck>(a, s);
+    if (dtype == ZERO_F16) {
+        ZERO_REDUCE_RING(ZERO_F16)
+    } else {
+        ZERO_REDUCE_RING(ZERO_BF16)
+    }
+#undef ZERO_REDUCE_RING
 }
 
 void launch_adam(const float* grad, const zero_state_t* in, const zero_state_t* out, uint64_t n,
@@ -921,15 +1004,21 @@ extern "C" zero_status_t zero_reduce_scatter_bucket(const zero_grads_t* g, uint6
         return ZERO_ERR_ALIGNMENT;
     if (bucket_len == 0)
         return ZERO_OK;
+    bool host_rows = false;
     zero_grads_t gr;   // the rows at the address the device reads them
-    st = resolve_grads(g, &gr);
+    st = resolve_grads(g, &gr, &host_rows);
     if (st != ZERO_OK)
         return st;
+    const int variant = fused_variant(host_rows);
     const uint16_t* first = static_cast<const uint16_t*>(gr.base) + g->offset + bucket_begin;
-    ReduceArgs a{first, g->row_stride, g->nd, split_window(g->offset + bucket_begin, bucket_len),
-                 inv_scale, cb_out, d_nonfinite};
-    launch_reduce(a, g->dtype, static_cast<cudaStream_t>(stream));
-    return launch_status();
+    return for_each_window(g->offset + bucket_begin, bucket_len, kWindow,
+                           [&](uint64_t w0, uint64_t w1) {
+        ReduceArgs a{first + w0, g->row_stride, g->nd,
+                     split_window(g->offset + bucket_begin + w0, w1 - w0), inv_scale, cb_out + w0,
+                     d_nonfinite};
+        launch_reduce(a, g->dtype, variant, static_cast<cudaStream_t>(stream));
+        return launch_status();
+    });
 }
 
 extern "C" zero_status_t zero_check_nonfinite(const zero_grads_t* g, uint64_t begin, uint64_t n,
@@ -944,15 +1033,19 @@ extern "C" zero_status_t zero_check_nonfinite(const zero_grads_t* g, uint64_t be
         return ZERO_ERR_ALIGNMENT;
     if (n == 0)
         return ZERO_OK;
+    bool host_rows = false;
     zero_grads_t gr;   // the rows at the address the device reads them
-    st = resolve_grads(g, &gr);
+    st = resolve_grads(g, &gr, &host_rows);
     if (st != ZERO_OK)
         return st;
+    const int variant = fused_variant(host_rows);
     const uint16_t* first = static_cast<const uint16_t*>(gr.base) + g->offset + begin;
-    ReduceArgs a{first, g->row_stride, g->nd, split_window(g->offset + begin, n), 1.0f, nullptr,
-                 d_nonfinite};
-    launch_reduce(a, g->dtype, static_cast<cudaStream_t>(stream));
-    return launch_status();
+    return for_each_window(g->offset + begin, n, kWindow, [&](uint64_t w0, uint64_t w1) {
+        ReduceArgs a{first + w0, g->row_stride, g->nd, split_window(g->offset + begin + w0, w1 - w0),
+                     1.0f, nullptr, d_nonfinite};
+        launch_reduce(a, g->dtype, variant, static_cast<cudaStream_t>(stream));
+        return launch_status();
+    });
 }
 
 extern "C" zero_status_t zero_adam_step_shard(const float* grad, const zero_state_t* in,
@@ -1048,10 +1141,12 @@ extern "C" zero_status_t zero_step_shard_unfused(const zero_grads_t* g, const ze
         return ZERO_ERR_ALIGNMENT;
     if (n == 0)
         return ZERO_OK;
+    bool host_rows = false;
     zero_grads_t gr;   // the rows at the address the device reads them
-    st = resolve_grads(g, &gr);
+    st = resolve_grads(g, &gr, &host_rows);
     if (st != ZERO_OK)
         return st;
+    const int variant = fused_variant(host_rows);
     const StepScalars k = make_scalars(h, g->nd, loss_scale);
     const StepScalars k_adam_only = make_scalars(h, 1, 1.0);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -1067,7 +1162,7 @@ extern "C" zero_status_t zero_step_shard_unfused(const zero_grads_t* g, const ze
             ReduceArgs r{rows + b0 + w0, g->row_stride, g->nd,
                          split_window(g->offset + b0 + w0, w1 - w0), k.inv, cbb + w0,
                          d_nonfinite};
-            launch_reduce(r, g->dtype, s);
+            launch_reduce(r, g->dtype, variant, s);
             return launch_status();
         });
         if (st != ZERO_OK)
