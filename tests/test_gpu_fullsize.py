@@ -6,7 +6,8 @@ hold at any size (padding untouched, skip decisions, step count).
 Workloads: GPT-2-small-sized ZeRO-2 shard (psi = 124,439,808, Nd = 8, bf16,
 10 steps); padding and overflow (psi = 350,000,017, Nd = 16, fp16 x 1024,
 all 16 ranks, +inf planted at step 5); GPT-2 1.5B shard view (Nd = 64, fp16,
-20 steps); 7.5B shard view (Nd = 64, bf16, bucket 5e8, 20 steps).
+20 steps); 7.5B shard view (Nd = 64, bf16, bucket 5e8, 20 steps); the
+end-to-end forms (rows in pinned host memory) on the 1.5B shard view.
 """
 import gc
 
@@ -16,6 +17,7 @@ import torch
 
 import oracle
 import synth
+import zero_sharded_optimizer_02_gb300 as z
 from gpu_util import (assert_params_close, assert_state_close, f32, full_rows, make_group,
                       oracle_trajectory, sample_indices, shard_rows, u16)
 
@@ -132,3 +134,41 @@ def test_c2_padding_and_overflow_all_ranks():
         assert not g[w.psi:].view(torch.int16).any()
     last = dps.layouts[w.nd - 1]
     assert int(last.length) == 21_874_987 and w.nd * s - w.psi == 15
+
+
+@pytest.mark.parametrize("form", ["zero_copy", "fed"])
+def test_c3_end_to_end_forms_sampled(form):
+    """The benchmark's end-to-end forms on the GPT-2 1.5B shard view (Nd = 64
+    fp16 rows, 3 GB): the rows stay in pinned host memory and are either read
+    in place by the step (zero-copy) or landed bucket by bucket by the feeder
+    while the bucket-ready step consumes them (16 buckets).  Two steps,
+    checked on sampled elements against the oracle."""
+    w = synth.WORKLOADS["c3"]
+    rank = 0
+    dps = make_group(w, ranks=[rank], gathered="slot")
+    idx = sample_indices(w.psi, w.nd, [rank], 2048, seed=33)
+    _, hist = oracle_trajectory(w, idx, 2)
+    buf, desc = shard_rows(w, dps, rank, 0)
+    host = torch.empty(buf.shape, dtype=buf.dtype, pin_memory=True)
+    host.copy_(buf)
+    pitch = int(dps.layouts[rank].row_pitch)
+    n = int(dps.layouts[rank].length)
+    copy = torch.cuda.Stream()
+    bucket = -(-(-(-n // 16)) // 8) * 8
+    if form == "fed":
+        buf.zero_()                       # the device rows fill as the buckets land
+    for k in range(2):
+        if form == "zero_copy":
+            assert not dps.step({rank: z.grads(host, pitch, 0, w.nd, w.grad_dtype)})
+        else:
+            dps.launch_host_fed(rank, host, desc[rank], bucket, copy)
+            assert not dps.decide()
+            dps.commit(False)
+            assert dps.host_fed_status() == 0
+        p, m, v, params, t = hist[k]
+        (gp, gm, gv), _ = _sampled_state(dps, idx, with_params=False)
+        assert_state_close(gp, p, 1e-12, f"{form} master step {k}")
+        assert_state_close(gm, m, 1e-20, f"{form} m step {k}")
+        assert_state_close(gv, v, 1e-20, f"{form} v step {k}")
+        assert_params_close(_slot_params(dps, rank, idx), params, f"{form} params step {k}")
+        assert dps.t == t
