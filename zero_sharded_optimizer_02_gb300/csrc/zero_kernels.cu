@@ -223,6 +223,11 @@ template <int DT, int W, bool V8, int MODE = kModeStep>
 __global__ void __launch_bounds__(kRingThreads, 1) k_step_fused_ring(const FusedArgs a)
 {
     extern __shared__ uint4 ring[];
+    // Programmatic dependent launch (when the launch allows it): wait for the
+    // previous grid in the stream to complete and its writes to be visible,
+    // then let the next grid be scheduled.  No-ops on a plain launch.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (gated(a))
         return;
     bool bad = false;
@@ -800,6 +805,39 @@ void smem_opt_in(F* fn, size_t bytes, std::atomic<uint64_t>& done)
         done.fetch_or(bit, std::memory_order_relaxed);
 }
 
+// Programmatic dependent launch of the ring kernel (on unless ZERO_PDL=0 in
+// the environment, read at each call): the next launch in the stream is
+// scheduled while this one's last CTAs drain, and waits in the kernel (not
+// at the launch) for its predecessor's results.  Consecutive windows and
+// steps lose their launch gap: +2% on the 7.5B shard's 5-launch step.
+bool pdl_enabled()
+{
+    const char* v = getenv("ZERO_PDL");
+    return !(v && v[0] == '0' && v[1] == '\0');
+}
+
+template <int DT, int W, bool V8, int MODE>
+void launch_ring(unsigned grid, const FusedArgs& a, cudaStream_t s)
+{
+    static std::atomic<uint64_t> opted{0};
+    smem_opt_in(k_step_fused_ring<DT, W, V8, MODE>, kRingBytes, opted);
+    if (pdl_enabled()) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kRingThreads);
+        cfg.dynamicSmemBytes = kRingBytes;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaLaunchKernelEx(&cfg, k_step_fused_ring<DT, W, V8, MODE>, a);
+    } else {
+        k_step_fused_ring<DT, W, V8, MODE><<<grid, kRingThreads, kRingBytes, s>>>(a);
+    }
+}
+
 template <int DT, int W, bool V8>
 void launch_fused_w(const FusedArgs& a, int variant, cudaStream_t s)
 {
@@ -813,12 +851,10 @@ void launch_fused_w(const FusedArgs& a, int variant, cudaStream_t s)
         k_step_fused_tma<DT, W, V8><<<grid, kTmaThreads, kTmaBytes, s>>>(a);
     } else if (variant == 1) {
         // one resident CTA per SM; the ring needs the opt-in shared memory size
-        static std::atomic<uint64_t> opted{0};
-        smem_opt_in(k_step_fused_ring<DT, W, V8>, kRingBytes, opted);
         const uint64_t want = (work + kRingThreads - 1) / kRingThreads;
         const uint64_t cap = (uint64_t)sm_count();
         const unsigned grid = (unsigned)(want < cap ? (want ? want : 1) : cap);
-        k_step_fused_ring<DT, W, V8><<<grid, kRingThreads, kRingBytes, s>>>(a);
+        launch_ring<DT, W, V8, kModeStep>(grid, a, s);
     } else {
         k_step_fused<DT, W, V8><<<grid_for(work), kThreads, 0, s>>>(a);
     }
@@ -847,13 +883,11 @@ void launch_fused_dt(const FusedArgs& a, int width, bool v8, int variant, cudaSt
 template <int DT, bool VEC, int MODE>
 void launch_reduce_ring(const FusedArgs& a, cudaStream_t s)
 {
-    static std::atomic<uint64_t> opted{0};
-    smem_opt_in(k_step_fused_ring<DT, VEC ? 16 : 4, false, MODE>, kRingBytes, opted);
     const uint64_t work = a.sp.nvec > a.sp.nscalar() ? a.sp.nvec : a.sp.nscalar();
     const uint64_t want = (work + kRingThreads - 1) / kRingThreads;
     const uint64_t cap = (uint64_t)sm_count();
     const unsigned grid = (unsigned)(want < cap ? (want ? want : 1) : cap);
-    k_step_fused_ring<DT, VEC ? 16 : 4, false, MODE><<<grid, kRingThreads, kRingBytes, s>>>(a);
+    launch_ring<DT, VEC ? 16 : 4, false, MODE>(grid, a, s);
 }
 
 // K1 (a.cb != nullptr) or K5 over one window: the ring kernel's reduction
