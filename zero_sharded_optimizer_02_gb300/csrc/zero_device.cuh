@@ -338,6 +338,16 @@ struct FusedArgs {
     float* cb;             // reduction-only launches: cb[e] = sum * k.inv (null: check only)
 };
 
+// First instructions of every step kernel: under a programmatic dependent
+// launch, wait until the previous grid in the stream has completed and its
+// writes are visible, then let the next grid be scheduled.  No-ops on a
+// plain launch.
+__device__ __forceinline__ void pdl_entry()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // True if the launch is gated off (a bucket wait before it ran out).
 __device__ __forceinline__ bool gated(const FusedArgs& a)
 {

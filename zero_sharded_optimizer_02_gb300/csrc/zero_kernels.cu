@@ -29,6 +29,7 @@
 #include <string.h>
 
 #include <atomic>
+#include <utility>
 
 #include "zero_device.cuh"
 
@@ -153,6 +154,7 @@ constexpr uint64_t kTmaDrainNs = 1000ull * 1000 * 1000;
 template <int DT, int W, bool V8>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_step_fused(const FusedArgs a)
 {
+    pdl_entry();
     if (gated(a))
         return;
     bool bad = false;
@@ -223,11 +225,7 @@ template <int DT, int W, bool V8, int MODE = kModeStep>
 __global__ void __launch_bounds__(kRingThreads, 1) k_step_fused_ring(const FusedArgs a)
 {
     extern __shared__ uint4 ring[];
-    // Programmatic dependent launch (when the launch allows it): wait for the
-    // previous grid in the stream to complete and its writes to be visible,
-    // then let the next grid be scheduled.  No-ops on a plain launch.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_entry();
     if (gated(a))
         return;
     bool bad = false;
@@ -365,6 +363,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_step_fused_tma(const FusedAr
     const float* slots =                                              // [slot][array][consumer][8]
         reinterpret_cast<const float*>(tma_smem + kTmaStages * kTmaStageBytes);
     uint64_t* bars = reinterpret_cast<uint64_t*>(tma_smem + kTmaBarOffset);
+    pdl_entry();
     if (gated(a))                       // uniform: every thread returns before any barrier
         return;
     const uint32_t full0 = smem_u32(bars);                                    // + 8 s
@@ -537,6 +536,7 @@ struct ReduceArgs {
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_reduce(const ReduceArgs a)
 {
+    pdl_entry();
     bool bad = false;
     const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
     const uint64_t nthr = (uint64_t)gridDim.x * kThreads;
@@ -589,6 +589,7 @@ struct AdamArgs {
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads, kCtasPerSmLight) k_adam(const AdamArgs a)
 {
+    pdl_entry();
     const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
     const uint64_t nthr = (uint64_t)gridDim.x * kThreads;
     if (!VEC) {
@@ -638,6 +639,7 @@ struct CastArgs {
 template <int DT, int W>
 __global__ void __launch_bounds__(kThreads, kCtasPerSmLight) k_cast(const CastArgs a)
 {
+    pdl_entry();
     const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
     const uint64_t nthr = (uint64_t)gridDim.x * kThreads;
     const uint64_t nscalar = a.n - 8 * a.nvec;
@@ -816,26 +818,36 @@ bool pdl_enabled()
     return !(v && v[0] == '0' && v[1] == '\0');
 }
 
-template <int DT, int W, bool V8, int MODE>
-void launch_ring(unsigned grid, const FusedArgs& a, cudaStream_t s)
+// Launches `kern` as a programmatic dependent launch when enabled (every
+// step kernel starts with pdl_entry), else as a plain launch.
+template <typename... KArgs, typename... Args>
+void launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+              Args&&... args)
 {
-    static std::atomic<uint64_t> opted{0};
-    smem_opt_in(k_step_fused_ring<DT, W, V8, MODE>, kRingBytes, opted);
     if (pdl_enabled()) {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(grid);
-        cfg.blockDim = dim3(kRingThreads);
-        cfg.dynamicSmemBytes = kRingBytes;
+        cfg.gridDim = grid;
+        cfg.blockDim = block;
+        cfg.dynamicSmemBytes = smem;
         cfg.stream = s;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        cudaLaunchKernelEx(&cfg, k_step_fused_ring<DT, W, V8, MODE>, a);
+        cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
     } else {
-        k_step_fused_ring<DT, W, V8, MODE><<<grid, kRingThreads, kRingBytes, s>>>(a);
+        kern<<<grid, block, smem, s>>>(std::forward<Args>(args)...);
     }
+}
+
+template <int DT, int W, bool V8, int MODE>
+void launch_ring(unsigned grid, const FusedArgs& a, cudaStream_t s)
+{
+    static std::atomic<uint64_t> opted{0};
+    smem_opt_in(k_step_fused_ring<DT, W, V8, MODE>, kRingBytes, opted);
+    launch_k(k_step_fused_ring<DT, W, V8, MODE>, dim3(grid), dim3(kRingThreads), kRingBytes, s,
+             a);
 }
 
 template <int DT, int W, bool V8>
@@ -848,7 +860,7 @@ void launch_fused_w(const FusedArgs& a, int variant, cudaStream_t s)
         const uint64_t tiles = (a.sp.nvec + kTmaConsumers - 1) / kTmaConsumers;
         const uint64_t cap = (uint64_t)sm_count();
         const unsigned grid = (unsigned)(tiles < cap ? (tiles ? tiles : 1) : cap);
-        k_step_fused_tma<DT, W, V8><<<grid, kTmaThreads, kTmaBytes, s>>>(a);
+        launch_k(k_step_fused_tma<DT, W, V8>, dim3(grid), dim3(kTmaThreads), kTmaBytes, s, a);
     } else if (variant == 1) {
         // one resident CTA per SM; the ring needs the opt-in shared memory size
         const uint64_t want = (work + kRingThreads - 1) / kRingThreads;
@@ -856,7 +868,7 @@ void launch_fused_w(const FusedArgs& a, int variant, cudaStream_t s)
         const unsigned grid = (unsigned)(want < cap ? (want ? want : 1) : cap);
         launch_ring<DT, W, V8, kModeStep>(grid, a, s);
     } else {
-        k_step_fused<DT, W, V8><<<grid_for(work), kThreads, 0, s>>>(a);
+        launch_k(k_step_fused<DT, W, V8>, dim3(grid_for(work)), dim3(kThreads), 0, s, a);
     }
 }
 
@@ -898,11 +910,11 @@ void launch_reduce(const ReduceArgs& r, int dtype, int variant, cudaStream_t s)
     if (variant == 0) {
         const unsigned grid = grid_for(r.sp.nvec > r.sp.nscalar() ? r.sp.nvec : r.sp.nscalar());
         if (dtype == ZERO_F16) {
-            if (vec) k_reduce<ZERO_F16, true><<<grid, kThreads, 0, s>>>(r);
-            else k_reduce<ZERO_F16, false><<<grid, kThreads, 0, s>>>(r);
+            if (vec) launch_k(k_reduce<ZERO_F16, true>, dim3(grid), dim3(kThreads), 0, s, r);
+            else launch_k(k_reduce<ZERO_F16, false>, dim3(grid), dim3(kThreads), 0, s, r);
         } else {
-            if (vec) k_reduce<ZERO_BF16, true><<<grid, kThreads, 0, s>>>(r);
-            else k_reduce<ZERO_BF16, false><<<grid, kThreads, 0, s>>>(r);
+            if (vec) launch_k(k_reduce<ZERO_BF16, true>, dim3(grid), dim3(kThreads), 0, s, r);
+            else launch_k(k_reduce<ZERO_BF16, false>, dim3(grid), dim3(kThreads), 0, s, r);
         }
         return;
     }
@@ -940,9 +952,10 @@ void launch_adam(const float* grad, const zero_state_t* in, const zero_state_t* 
         a.head = head < n ? head : n;
         a.nvec = (n - a.head) / 4;
         const uint64_t ns = n - 4 * a.nvec;
-        k_adam<true><<<grid_for(a.nvec > ns ? a.nvec : ns, kCtasPerSmLight), kThreads, 0, s>>>(a);
+        launch_k(k_adam<true>, dim3(grid_for(a.nvec > ns ? a.nvec : ns, kCtasPerSmLight)),
+                 dim3(kThreads), 0, s, a);
     } else {
-        k_adam<false><<<grid_for(n, kCtasPerSmLight), kThreads, 0, s>>>(a);
+        launch_k(k_adam<false>, dim3(grid_for(n, kCtasPerSmLight)), dim3(kThreads), 0, s, a);
     }
 }
 
@@ -955,12 +968,12 @@ void launch_cast(const float* master, uint64_t n, uint16_t* gath, int dtype, cud
     const uint64_t ns = n - 8 * a.nvec;
     const unsigned grid = grid_for(a.nvec > ns ? a.nvec : ns, kCtasPerSmLight);
     const int w = store_width(gath + a.head);
-#define ZERO_CAST_CASE(DT)                                                   \
-    switch (w) {                                                             \
-    case 16: k_cast<DT, 16><<<grid, kThreads, 0, s>>>(a); break;             \
-    case 8: k_cast<DT, 8><<<grid, kThreads, 0, s>>>(a); break;               \
-    case 4: k_cast<DT, 4><<<grid, kThreads, 0, s>>>(a); break;               \
-    default: k_cast<DT, 2><<<grid, kThreads, 0, s>>>(a); break;              \
+#define ZERO_CAST_CASE(DT)                                                                      \
+    switch (w) {                                                                                \
+    case 16: launch_k(k_cast<DT, 16>, dim3(grid), dim3(kThreads), 0, s, a); break;              \
+    case 8: launch_k(k_cast<DT, 8>, dim3(grid), dim3(kThreads), 0, s, a); break;                \
+    case 4: launch_k(k_cast<DT, 4>, dim3(grid), dim3(kThreads), 0, s, a); break;                \
+    default: launch_k(k_cast<DT, 2>, dim3(grid), dim3(kThreads), 0, s, a); break;               \
     }
     if (dtype == ZERO_F16) {
         ZERO_CAST_CASE(ZERO_F16)
