@@ -260,10 +260,11 @@ zero_status_t zero_check_nonfinite(const zero_grads_t* g, uint64_t begin, uint64
 /* The fused step started bucket by bucket as gradients arrive ("ZeRO-DP",
  * Stage 2: gradients are reduce-scattered in buckets during the backward
  * pass).  Bucket b is elements [b*bucket_elems, ...) of the shard.
- * Consecutive buckets form launch groups of at least ZERO_STREAM_GROUP_BYTES
- * of step traffic ((2*nd + 26) bytes per element; the environment variable
- * ZERO_STREAM_GROUP_BYTES, read at each call, overrides it: 0 makes every
- * bucket its own group); for each group in order a
+ * Consecutive buckets form launch groups: as many groups as the shard's step
+ * traffic ((2*nd + 26) bytes per element) holds ZERO_STREAM_GROUP_BYTES, at
+ * least one, with the buckets dealt as evenly as possible (the environment
+ * variable ZERO_STREAM_GROUP_BYTES, read at each call, overrides the size: 0
+ * makes every bucket its own group); for each group in order a
  * one-thread kernel waits until d_ready[b] >= epoch (wrap-around comparison)
  * for each of its buckets, then the fused step's launches for the group follow
  * on the same stream (as zero_step_shard: launch windows of at most

@@ -116,19 +116,22 @@ ZERO_STREAM_GROUP_BYTES = 500000000
 
 
 def stream_groups(n: int, bucket: int, nd: int) -> list:
-    """The launch groups of zero_step_shard_streamed: (first element, length)
-    of each run of consecutive buckets with at least ZERO_STREAM_GROUP_BYTES
-    of step traffic (the last group may have less)."""
+    """The launch groups of zero_step_shard_streamed, as (first element,
+    length): as many groups as the shard's step traffic holds
+    ZERO_STREAM_GROUP_BYTES (0: one group a bucket), the buckets dealt as
+    evenly as possible."""
     env = os.environ.get("ZERO_STREAM_GROUP_BYTES", "")
     group_bytes = int(env) if env.isdigit() else ZERO_STREAM_GROUP_BYTES
-    min_group = group_bytes // (2 * nd + 26) + 1
     nb = -(-n // bucket)
+    if nb == 0:
+        return []
+    ngroups = n * (2 * nd + 26) // group_bytes if group_bytes else nb
+    ngroups = min(max(ngroups, 1), nb)
+    base, extra = divmod(nb, ngroups)
     groups, b = [], 0
-    while b < nb:
-        g0, b_end = b * bucket, b + 1
-        while b_end < nb and b_end * bucket - g0 < min_group:
-            b_end += 1
-        groups.append((g0, min(b_end * bucket, n) - g0))
+    for grp in range(ngroups):
+        b_end = b + base + (1 if grp < extra else 0)
+        groups.append((b * bucket, min(b_end * bucket, n) - b * bucket))
         b = b_end
     return groups
 

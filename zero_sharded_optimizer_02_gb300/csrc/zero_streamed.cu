@@ -133,10 +133,11 @@ extern "C" zero_status_t zero_step_shard_streamed(
     const uint16_t* rows = static_cast<const uint16_t*>(gr.base) + g->offset;
     uint16_t* gath = static_cast<uint16_t*>(gathered) + gathered_offset_elems;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // Consecutive buckets form launch groups of at least
-    // ZERO_STREAM_GROUP_BYTES of step traffic (or the environment variable of
-    // that name, read at each call), so that each group's launches outweigh
-    // their fixed cost; a group starts once all its buckets landed.
+    // Consecutive buckets form launch groups: as many groups as the shard's
+    // step traffic holds ZERO_STREAM_GROUP_BYTES (the environment variable of
+    // that name, read at each call, overrides it; 0: one group a bucket), the
+    // buckets dealt as evenly as possible, so that each group's launches
+    // outweigh their fixed cost.  A group starts once all its buckets landed.
     uint64_t group_bytes = ZERO_STREAM_GROUP_BYTES;
     if (const char* e = getenv("ZERO_STREAM_GROUP_BYTES")) {
         char* end = nullptr;
@@ -144,14 +145,14 @@ extern "C" zero_status_t zero_step_shard_streamed(
         if (end != e && *end == '\0')
             group_bytes = v;
     }
-    const uint64_t min_group = group_bytes / (2ull * g->nd + 26) + 1;
     const uint64_t nb = (n + bucket_elems - 1) / bucket_elems;
-    for (uint64_t b = 0; b < nb;) {
+    const uint64_t traffic = n * (2ull * g->nd + 26);
+    uint64_t ngroups = group_bytes ? traffic / group_bytes : nb;
+    ngroups = ngroups < 1 ? 1 : (ngroups > nb ? nb : ngroups);
+    const uint64_t base = nb / ngroups, extra = nb % ngroups;   // buckets per group
+    for (uint64_t grp = 0, b = 0; grp < ngroups; ++grp) {
         const uint64_t g0 = b * bucket_elems;
-        uint64_t b_end = b;
-        do {
-            ++b_end;
-        } while (b_end < nb && b_end * bucket_elems - g0 < min_group);
+        const uint64_t b_end = b + base + (grp < extra ? 1 : 0);
         const uint64_t glen = (b_end * bucket_elems < n ? b_end * bucket_elems : n) - g0;
         k_wait_ready<<<1, 1, 0, st>>>(d_ready + b, (uint32_t)(b_end - b), epoch, timeout_ns,
                                       d_status);
