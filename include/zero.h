@@ -179,7 +179,10 @@ zero_status_t zero_gather_params_shard(const float* master, uint64_t n, void* ga
  * The kernel is the cp.async-ring variant unless the environment variable
  * ZERO_FUSED_VARIANT, read at each call, names another ("registers", "ring"
  * or "tma": bulk copies and mbarriers); rows in host memory always use the
- * register variant.  All variants give bitwise the same results.
+ * register variant.  All variants give bitwise the same results.  Launches
+ * are programmatic dependent launches (each kernel waits in-kernel for its
+ * predecessor in the stream, so consecutive launches lose their gap) unless
+ * the environment variable ZERO_PDL is "0".
  * The new state goes to `out` and the cast parameters to
  * gathered[gathered_offset_elems + i].  *d_nonfinite |= 1 if any reduced sum
  * is nonfinite; the step is then to be skipped on every shard: with out != in
