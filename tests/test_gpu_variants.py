@@ -111,3 +111,20 @@ def test_two_launch_windows_agree_across_variants(monkeypatch):
             del dps, buf, desc
             torch.cuda.empty_cache()
         assert out["registers"] == out["ring"] == out["tma"], w.psi
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_plain_and_programmatic_launches_agree(fused, monkeypatch):
+    """Every step kernel runs as a programmatic dependent launch by default;
+    ZERO_PDL=0 launches them plainly.  Both give the oracle's result (the
+    4-rank workload, 3 steps: consecutive launches of the same stream)."""
+    w = synth.WORKLOADS["c0"]
+    _, hist = oracle_trajectory(w, np.arange(w.psi), w.steps)
+    for pdl in ("0", "1"):
+        monkeypatch.setenv("ZERO_PDL", pdl)
+        dps = make_group(w, fused=fused)
+        buf = None
+        for k in range(w.steps):
+            buf, desc = full_rows(w, dps, k, buf)
+            assert not dps.step(desc)
+            check_against_oracle(w, dps, hist[k], f"ZERO_PDL={pdl} fused={fused} step {k}")
