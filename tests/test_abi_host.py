@@ -247,3 +247,48 @@ def test_binding_constants_match_header(z):
     assert z._abi.gather_launch_count(1000, 10, 95, 10) == 1
     assert z._abi.gather_launch_count(1000, 10, 0, 0) == 0
     assert z._abi.gather_launch_count(1000, 1000, 0, 1000) == 21
+
+
+def _window_cuts(length: int, phase: int):
+    """The launch windows of one bucket, restated from zero.h's description:
+    the fewest equal windows of at most ZERO_FUSED_WINDOW_ELEMS elements,
+    cut on 8-element row boundaries, a remainder under 64 joining the last."""
+    W = z_abi().ZERO_FUSED_WINDOW_ELEMS
+    nwin = -(-length // W)
+    target = -(-(-(-length // nwin)) // 8) * 8
+    cuts, w0, cut = [], 0, target - (phase & 7)
+    while w0 < length:
+        w1 = min(cut, length)
+        if length - w1 < 64:
+            w1 = length
+        cuts.append((w0, w1))
+        w0, cut = w1, cut + target
+    return cuts
+
+
+def z_abi():
+    from zero_sharded_optimizer_02_gb300 import _abi
+    return _abi
+
+
+def test_launch_windows_properties():
+    import random
+    rng = random.Random(7)
+    W = z_abi().ZERO_FUSED_WINDOW_ELEMS
+    cases = [(117_187_500, 0), (23_437_500, 4), (25_165_824, 0), (25_165_825, 3),
+             (50_331_648 + 63, 5), (64, 7), (1, 0)]
+    cases += [(rng.randrange(1, 400_000_000), rng.randrange(8)) for _ in range(300)]
+    for length, phase in cases:
+        cuts = _window_cuts(length, phase)
+        # they tile the bucket in order
+        assert cuts[0][0] == 0 and cuts[-1][1] == length
+        assert all(a[1] == b[0] for a, b in zip(cuts, cuts[1:]))
+        # every inner cut falls on a 16-byte boundary of the rows
+        assert all((phase + c[0]) % 8 == 0 for c in cuts[1:])
+        # the fewest windows (a remainder under 64 may join the last one), each
+        # at most one window plus such a remainder
+        nwin = -(-length // W)
+        assert len(cuts) in (nwin, max(nwin - 1, 1))
+        assert all(c[1] - c[0] <= W + 63 for c in cuts)
+        # and the binding's launch count is exactly this split
+        assert z_abi()._windows(length, phase) == len(cuts)
