@@ -12,7 +12,7 @@
 // longer changes, and only the waits run while a bucket is in flight.
 //
 // Every wait is bounded: the waiting thread polls the word with an acquire
-// load, sleeping between polls (64 ns, doubling up to about 16 us), for at
+// load, sleeping between polls (64 ns, doubling up to about 1 us), for at
 // most timeout_ns of %globaltimer time and an iteration cap.  On expiry it
 // records ZERO_ERR_TIMEOUT in the status word; every later wait and step
 // launch of the call reads the status word first and does nothing, so no
