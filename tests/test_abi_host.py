@@ -292,3 +292,30 @@ def test_launch_windows_properties():
         assert all(c[1] - c[0] <= W + 63 for c in cuts)
         # and the binding's launch count is exactly this split
         assert z_abi()._windows(length, phase) == len(cuts)
+
+
+def test_header_is_plain_c_and_host_calls_work_from_c(z, tmp_path):
+    """include/zero.h compiles as C99 with warnings as errors, and a C program
+    linked against libzero.so gets the same layout and accounting as the
+    binding (host-only calls: no GPU needed)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    lib_dir = os.path.dirname(z._abi.LIB_PATH)
+    exe = str(tmp_path / "abi_check")
+    subprocess.check_call([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                           "-I", os.path.join(ROOT, "include"),
+                           os.path.join(ROOT, "tests", "c", "abi_check.c"), "-o", exe,
+                           "-L", lib_dir, "-lzero", f"-Wl,-rpath,{lib_dir}"])
+    out = subprocess.check_output([exe], text=True).splitlines()
+    L = z.zero_partition_layout(350_000_017, 16, 15, 8)
+    assert out[0] == (f"layout {L.shard_elems} {L.begin} {L.length} {L.padded_elems} "
+                      f"{L.row_pitch}")
+    for stage in range(4):
+        expect = z.zero_model_state_bytes(7_500_000_000, 64, stage, 12)
+        assert out[1 + stage] == f"bytes {stage} {expect}"
+    assert out[5] == f"invalid {z.ZERO_ERR_INVALID_ARG}"
+    assert out[6] == f"status {z.zero_status_string(z.ZERO_ERR_TIMEOUT)}"
+    assert out[7] == f"window {z._abi.ZERO_FUSED_WINDOW_ELEMS}"
