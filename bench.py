@@ -36,7 +36,7 @@ sys.path.insert(0, ROOT)
 METRIC = "ZeRO shard step: params updated/s and HBM GB/s vs GB300 peak (1 GPU)"
 UNIT = "params/s"
 KERNEL_SRCS = [os.path.join(ROOT, "zero_sharded_optimizer_02_gb300", "csrc", f)
-               for f in ("zero_kernels.cu", "zero_device.cuh")]
+               for f in ("zero_ring.cuh", "zero_device.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k_step_fused_traffic.txt")
 NOMINAL_HBM_GBS = 7900.0
 
@@ -64,7 +64,9 @@ def kernel_name() -> str:
 
 def kernel_source_hash() -> str:
     """Hash of the code (comments and whitespace removed) of the sources the
-    fused kernel is compiled from: any change of the kernel's code changes it."""
+    default fused kernel is compiled from (its header and the shared device
+    helpers): any change of the kernel's code changes it; host launch code
+    does not."""
     import re
     h = hashlib.sha256()
     for path in KERNEL_SRCS:
