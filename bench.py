@@ -422,6 +422,9 @@ def run_gpu(args) -> None:
                    "link": {"bound_ms": best["copies"],
                             "bound": "the fastest iteration of the DMA copies alone",
                             "frac": best["copies"] / mean["zero_copy"]}}
+            if best["copies"] > mean["zero_copy"]:
+                e2e["link"]["note"] = ("the copy engines ran slower than the kernels' own "
+                                       "reads of host memory in this run: not a bound")
             del host_grads, host_params
 
     if rank != 0:
