@@ -39,6 +39,7 @@ KERNEL_SRCS = [os.path.join(ROOT, "zero_sharded_optimizer_02_gb300", "csrc", f)
                for f in ("zero_ring.cuh", "zero_device.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "k_step_fused_traffic.txt")
 NOMINAL_HBM_GBS = 7900.0
+L2_BYTES = 129e6
 
 
 def measured_peaks() -> dict:
@@ -472,8 +473,10 @@ def run_gpu(args) -> None:
                        f" (slot at element {int(L.begin)}, 16-byte phase "
                        f"{(int(L.begin) * 2) % 16} B)" if args.gathered == "full" else
                        " (the rank's own S-element buffer)"),
-                   "l2": f"inputs larger than L2 ({bytes_per_param * n / 1e9:.1f} GB per step),"
-                         " no flush",
+                   "l2": (f"inputs larger than L2 ({bytes_per_param * n / 1e9:.1f} GB per step),"
+                          " no flush" if bytes_per_param * n > L2_BYTES else
+                          f"inputs L2-resident ({bytes_per_param * n / 1e6:.1f} MB per step, "
+                          "L2 129 MB), no flush: a latency figure, not a bandwidth one"),
                    "parallelism": f"zero-dp{w.nd} emulated, {world} process(es)"},
         "gbs": bytes_per_param * n / (ms_per_step * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
