@@ -365,9 +365,22 @@ def run_gpu(args) -> None:
 
             host_desc = {dp_rank: _abi.grads(host_grads, row_stride, 0, w.nd, w.grad_dtype)}
 
-            def zero_copy():      # the fused kernels read the gradients in host memory
+            def zero_copy_read_back():   # the kernels read the gradients in host memory
                 dps.step(host_desc)
                 read_back()
+
+            # the same step with its gathered slot in pinned host memory: the
+            # kernels also write the new parameters in place over the host
+            # link, so they are on the host when the step's flag is read
+            dps_h = DataParallelStep(w.psi, w.nd, [dp_rank], w.grad_dtype, w.hparams,
+                                     w.loss_scale, w.bucket, dev, gathered="slot", fused=True,
+                                     process_group=group, stream=stream, gathered_on_host=True)
+            with torch.cuda.stream(stream):
+                dps_h.state[dp_rank].bufs[0].copy_(dps.state[dp_rank].bufs[dps.state[dp_rank].cur])
+            dps_h.t = dps.t
+
+            def zero_copy():
+                dps_h.step(host_desc)
 
             def copies_alone():   # the host link alone: the same bytes, no step
                 with torch.cuda.stream(stream):
@@ -379,7 +392,7 @@ def run_gpu(args) -> None:
             # first iteration is untimed.  Each is timed on the host around the
             # whole call, its final synchronisation included.
             forms = {"fed": host_fed, "sequential": sequential, "zero_copy": zero_copy,
-                     "copies": copies_alone}
+                     "zero_copy_read_back": zero_copy_read_back, "copies": copies_alone}
             times = {k: [] for k in forms}
             for it in range(args.e2e_steps + 1):
                 for k, fn in forms.items():
@@ -401,22 +414,27 @@ def run_gpu(args) -> None:
                         "value": world * n / (mean[k] * 1e-3), "path": path,
                         "h2d_bytes_per_step": h2d}
             # The headline is the zero-copy form: the kernels read the step's
-            # gradients in place in pinned host memory, so the same bytes cross
-            # the host link every step without a device copy; it runs steadily
-            # where the copy engines' time varies with the shared host.
+            # gradients, and write its parameters, in place in pinned host
+            # memory, so the same bytes cross the host link every step without
+            # a device copy; it runs steadily where the copy engines' time
+            # varies with the shared host.
             e2e = {"value": world * n / (mean["zero_copy"] * 1e-3), "unit": UNIT,
                    "h2d_bytes_per_step": grad_bytes,
                    "d2h_bytes_per_step": n * host_params.element_size() + 4,
                    "ms_per_step": mean["zero_copy"], "ms_per_step_min": best["zero_copy"],
                    "steps": args.e2e_steps,
-                   "path": "zero_step_shard reading the Nd gradient rows in place in pinned host "
-                           "memory (zero-copy over the host link), then the flag and the new "
-                           "parameters device-to-host",
+                   "path": "zero_step_shard reading the Nd gradient rows, and writing the new "
+                           "parameters, in place in pinned host memory (zero-copy both ways over "
+                           "the host link), then the flag device-to-host",
                    "other_forms": {
                        "fed": form("fed", f"zero_feed_buckets (DMA, {nbk} transfer buckets) + "
                                           "zero_step_shard_streamed", grad_bytes + 4 * nbk),
                        "sequential": form("sequential", "one DMA copy of the gradients, then "
                                                         "zero_step_shard", grad_bytes),
+                       "zero_copy_read_back": form(
+                           "zero_copy_read_back", "zero_step_shard reading the rows in place in "
+                           "host memory into device parameters, then a DMA copy of them",
+                           grad_bytes),
                        "copies_alone": form("copies", "the DMA copies alone, no step",
                                             grads.numel() * grads.element_size())},
                    "ms_per_iteration": {k: [round(x, 3) for x in v] for k, v in times.items()},
@@ -426,7 +444,7 @@ def run_gpu(args) -> None:
             if best["copies"] > mean["zero_copy"]:
                 e2e["link"]["note"] = ("the copy engines ran slower than the kernels' own "
                                        "reads of host memory in this run: not a bound")
-            del host_grads, host_params
+            del host_grads, host_params, dps_h
 
     if rank != 0:
         if world > 1:

@@ -22,6 +22,12 @@
  *   - Pointers named d_* or documented "device" must be device memory of the
  *     current CUDA device; structs passed by pointer are host memory and are
  *     read before the call returns.
+ *   - Gradient rows (zero_grads_t.base) and gathered parameter buffers may
+ *     also be page-locked host memory registered with CUDA (cudaHostAlloc,
+ *     cudaHostRegister): the kernels then read the rows, or write the cast
+ *     parameters, in place over the host link at the memory's device mapping
+ *     (zero-copy).  Any other host pointer, pageable memory included, is
+ *     ZERO_ERR_INVALID_ARG before anything is launched.
  *   - Errors: every call validates its arguments on the host first and returns
  *     a zero_status_t without launching anything if they are invalid.  Kernel
  *     work is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
@@ -158,8 +164,8 @@ zero_status_t zero_adam_step_shard(const float* grad, const zero_state_t* in,
 /* Cast of a shard's fp32 master weights into its slot of the gathered
  * parameter buffer (the local part of the Stage-1 all-gather):
  *     gathered[slot_offset_elems + i] = round_to_nearest_even(master[i]).
- * master: device fp32[n], 4-byte aligned; gathered: device, 2-byte aligned
- * (any slot phase; the store width follows it). */
+ * master: device fp32[n], 4-byte aligned; gathered: device or page-locked
+ * host memory, 2-byte aligned (any slot phase; the store width follows it). */
 zero_status_t zero_gather_params_shard(const float* master, uint64_t n, void* gathered,
                                        uint64_t slot_offset_elems, zero_dtype_t dtype,
                                        void* stream);
@@ -184,7 +190,7 @@ zero_status_t zero_gather_params_shard(const float* master, uint64_t n, void* ga
  * predecessor in the stream, so consecutive launches lose their gap) unless
  * the environment variable ZERO_PDL is "0".
  * The new state goes to `out` and the cast parameters to
- * gathered[gathered_offset_elems + i].  *d_nonfinite |= 1 if any reduced sum
+ * gathered[gathered_offset_elems + i] (device or page-locked host memory).  *d_nonfinite |= 1 if any reduced sum
  * is nonfinite; the step is then to be skipped on every shard: with out != in
  * the caller simply keeps `in` (and its previous gathered buffer).  With
  * out == in the update happens in place and cannot be rolled back: run

@@ -57,13 +57,14 @@ def assert_params_close(got: np.ndarray, ref: np.ndarray, what: str):
 # -- workloads on the device -------------------------------------------------
 
 def make_group(w: synth.Workload, ranks=None, fused=True, bucket=None, gathered="full",
-               psi=None, nd=None):
+               psi=None, nd=None, gathered_on_host=False):
     """A DataParallelStep over `ranks` with the workload's initial state."""
     psi = psi or w.psi
     nd = nd or w.nd
     ranks = list(range(nd)) if ranks is None else list(ranks)
     dps = DataParallelStep(psi, nd, ranks, w.grad_dtype, w.hparams, w.loss_scale,
-                           bucket or w.bucket, DEV, gathered=gathered, fused=fused)
+                           bucket or w.bucket, DEV, gathered=gathered, fused=fused,
+                           gathered_on_host=gathered_on_host)
     for r in ranks:
         st = dps.state[r]
         buf = st.bufs[st.cur]

@@ -79,8 +79,9 @@ def _bench_driver(w, rank):
 
 def _slot_params(dps, rank, idx):
     s = int(dps.layouts[rank].shard_elems)
-    local = torch.from_numpy(idx - rank * s).to(dps.device)
-    return u16(dps.gathered_view(rank)[local])
+    slot = dps.gathered_view(rank)
+    local = torch.from_numpy(idx - rank * s).to(slot.device)
+    return u16(slot[local])
 
 
 @pytest.mark.parametrize("key,rank,bench_cfg", [("c1", 0, False), ("c1", 5, False),
@@ -136,16 +137,20 @@ def test_c2_padding_and_overflow_all_ranks():
     assert int(last.length) == 21_874_987 and w.nd * s - w.psi == 15
 
 
-@pytest.mark.parametrize("form", ["zero_copy", "fed"])
+@pytest.mark.parametrize("form", ["zero_copy", "zero_copy_device_params", "fed"])
 def test_c3_end_to_end_forms_sampled(form):
     """The benchmark's end-to-end forms on the GPT-2 1.5B shard view (Nd = 64
     fp16 rows, 3 GB): the rows stay in pinned host memory and are either read
-    in place by the step (zero-copy) or landed bucket by bucket by the feeder
-    while the bucket-ready step consumes them (16 buckets).  Two steps,
-    checked on sampled elements against the oracle."""
+    in place by the step (zero-copy, with the new parameters written in place
+    to pinned host memory or to device memory) or landed bucket by bucket by
+    the feeder while the bucket-ready step consumes them (16 buckets).  Two
+    steps, checked on sampled elements against the oracle."""
     w = synth.WORKLOADS["c3"]
     rank = 0
-    dps = make_group(w, ranks=[rank], gathered="slot")
+    dps = make_group(w, ranks=[rank], gathered="slot", gathered_on_host=form == "zero_copy")
+    if form == "zero_copy":
+        assert dps.gathered_view(rank).device.type == "cpu"
+        assert dps.gathered_view(rank).is_pinned()
     idx = sample_indices(w.psi, w.nd, [rank], 2048, seed=33)
     _, hist = oracle_trajectory(w, idx, 2)
     buf, desc = shard_rows(w, dps, rank, 0)
@@ -158,7 +163,7 @@ def test_c3_end_to_end_forms_sampled(form):
     if form == "fed":
         buf.zero_()                       # the device rows fill as the buckets land
     for k in range(2):
-        if form == "zero_copy":
+        if form.startswith("zero_copy"):
             assert not dps.step({rank: z.grads(host, pitch, 0, w.nd, w.grad_dtype)})
         else:
             dps.launch_host_fed(rank, host, desc[rank], bucket, copy)

@@ -1,11 +1,12 @@
-"""Gradient contributions read in place from page-locked host memory.
+"""Gradient contributions read, and cast parameters written, in place in
+page-locked host memory.
 
-On a Grace-Blackwell node the GPU reads page-locked host memory over the
-host link at the link's bandwidth, so a rank's step can take its Nd
-contributions straight from host memory without a device copy of them.  The
-results must be those of the same contributions in device memory, and a
-pointer the GPU cannot read (pageable host memory) must be refused before
-anything is launched.
+On a Grace-Blackwell node the GPU reads and writes page-locked host memory
+over the host link at the link's bandwidth, so a rank's step can take its Nd
+contributions straight from host memory, and return its new parameters
+there, without device copies of either.  The results must be those of the
+same step in device memory, and a pointer the GPU cannot use (pageable host
+memory) must be refused before anything is launched.
 """
 import dataclasses
 
@@ -133,4 +134,119 @@ def test_pageable_host_rows_are_refused():
     torch.cuda.synchronize()
     assert int(dps.flag.item()) == 0
     for a, b in zip(before, dps.state[1].tensors("cur")):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("path", ["ring", "registers", "tma", "unfused"])
+def test_host_params_equal_device_params(path, monkeypatch):
+    """Every rank's cast parameters written into one flat gathered buffer in
+    pinned host memory (16 ranks, S mod 8 = 3: every slot phase; buckets of
+    7), contributions in device or host memory: the same state and
+    parameters, bit for bit, as with the buffer in device memory."""
+    w = dataclasses.replace(synth.WORKLOADS["c1"], psi=70_001, nd=16, grad_dtype="f16",
+                            loss_scale=1024.0, plant=None)
+    if path != "unfused":
+        monkeypatch.setenv("ZERO_FUSED_VARIANT", path)
+    out = {}
+    for params_on_host in (False, True):
+        for rows_on_host in (False, True):
+            dps = make_group(w, fused=path != "unfused", bucket=7,
+                             gathered_on_host=params_on_host)
+            assert dps.gathered_view().is_pinned() == params_on_host
+            pitch = int(dps.layouts[0].row_pitch)
+            buf = None
+            for k in range(2):
+                buf, desc = full_rows(w, dps, k, buf)
+                if rows_on_host:
+                    host = _pinned_copy(buf)
+                    desc = {r: z.grads(host, w.nd * pitch, r * pitch, w.nd, w.grad_dtype)
+                            for r in dps.ranks}
+                assert not dps.step(desc)
+            got = [a.tobytes() for a in flat_state(dps)] + \
+                [u16(dps.gathered_view()).tobytes()]
+            out[params_on_host, rows_on_host] = got
+    first = out[False, False]
+    for key, got in out.items():
+        assert got == first, key
+
+
+def test_host_params_streamed_and_cast():
+    """The bucket-ready step and the standalone cast write a pinned host slot
+    at an odd element phase: the bytes of the device-memory results, and the
+    guard elements on either side untouched."""
+    w = dataclasses.replace(synth.WORKLOADS["c1"], psi=8 * 30_001 + 3, nd=8, plant=None)
+    rank = 5
+    dps = make_group(w, ranks=[rank], gathered="slot")
+    buf, desc = shard_rows(w, dps, rank, 0)
+    L = dps.layouts[rank]
+    n = int(L.length)
+    st = dps.state[rank]
+    h = z.adamw(w.hparams["lr"], 0.9, 0.999, 1e-8, 0.01, 1)
+    bucket = 6_001
+    ready = torch.ones(-(-n // bucket), dtype=torch.int32, device=DEV)
+    results = []
+    for on_host in (False, True):
+        slot = torch.full((n + 10,), 0x5A5A, dtype=torch.int16,
+                          **({"pin_memory": True} if on_host else {"device": DEV}))
+        flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        s_out = z.state(*(torch.empty(n, dtype=torch.float32, device=DEV) for _ in range(3)))
+        z.zero_step_shard_streamed(desc[rank], L, st.states[st.cur], s_out, slot, 3, bucket,
+                                   w.loss_scale, h, ready, 1, 10 ** 9, flag, status)
+        torch.cuda.synchronize()
+        assert int(flag.item()) == 0 and int(status.item()) == 0
+        cast = torch.full((n + 10,), 0x5A5A, dtype=torch.int16,
+                          **({"pin_memory": True} if on_host else {"device": DEV}))
+        master = dps.state[rank].tensors("cur")[0]
+        z.zero_gather_params_shard(master, n, cast, 5, w.grad_dtype)
+        torch.cuda.synchronize()
+        results.append((slot.cpu().numpy().tobytes(), cast.cpu().numpy().tobytes()))
+        for t, off in ((slot, 3), (cast, 5)):
+            c = t.cpu()
+            assert (c[:off] == 0x5A5A).all() and (c[off + n:] == 0x5A5A).all()
+    assert results[0] == results[1]
+
+
+def test_pageable_params_are_refused():
+    """A gathered buffer in pageable host memory: every entry point that writes
+    parameters returns ZERO_ERR_INVALID_ARG and launches nothing."""
+    w = synth.WORKLOADS["c0"]
+    rank = 1
+    dps = make_group(w, ranks=[rank], gathered="slot")
+    buf, desc = shard_rows(w, dps, rank, 0)
+    L = dps.layouts[rank]
+    n = int(L.length)
+    st = dps.state[rank]
+    before = [t.clone() for t in st.tensors("cur")]
+    pageable = torch.zeros(n + 8, dtype=TORCH_DT[w.grad_dtype])
+    assert not pageable.is_pinned()
+    s_out = st.states[1 - st.cur]
+    out_before = [t.clone() for t in st.tensors("next")]
+    h = z.adamw(w.hparams["lr"], 0.9, 0.999, 1e-8, 0.01, 1)
+    cb = torch.empty(n + 4, dtype=torch.float32, device=DEV)
+    ready = torch.ones(1, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    calls = [
+        lambda: z.zero_step_shard(desc[rank], L, st.states[st.cur], s_out, pageable, 0, w.bucket,
+                                  w.loss_scale, h, dps.flag),
+        lambda: z.zero_step_shard_unfused(desc[rank], L, st.states[st.cur], s_out, pageable, 0,
+                                          w.bucket, w.loss_scale, h, cb, n + 4, dps.flag),
+        lambda: z.zero_step_shard_unfused_static(desc[rank], L, st.states[st.cur], s_out,
+                                                 pageable, 0, w.bucket, w.loss_scale, h,
+                                                 dps.flag),
+        lambda: z.zero_step_shard_streamed(desc[rank], L, st.states[st.cur], s_out, pageable, 0,
+                                           n, w.loss_scale, h, ready, 1, 10 ** 9, dps.flag,
+                                           status),
+        lambda: z.zero_gather_params_shard(st.tensors("cur")[0], n, pageable, 0, w.grad_dtype),
+    ]
+    for call in calls:
+        with pytest.raises(z.ZeroError) as e:
+            call()
+        assert e.value.status == z.ZERO_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert int(dps.flag.item()) == 0 and int(status.item()) == 0
+    assert not pageable.any()
+    for a, b in zip(before, st.tensors("cur")):
+        assert torch.equal(a, b)
+    for a, b in zip(out_before, st.tensors("next")):
         assert torch.equal(a, b)

@@ -31,13 +31,17 @@ bool adamw_valid(const zero_adamw_t* h);
 // (pass nd = 1, loss_scale = 1 when the gradient is already scaled).
 StepScalars make_scalars(const zero_adamw_t* h, uint32_t nd, double loss_scale);
 
-// The descriptor the kernels read: g with base replaced by the address the
-// device reads it at.  Device and managed memory are read where they are;
-// page-locked host memory registered with CUDA is read in place over the
-// host link (zero-copy) at its device-mapped address; anything else
+// The address the kernels access p at.  Device and managed memory are
+// accessed where they are; page-locked host memory registered with CUDA is
+// accessed in place over the host link (zero-copy) at its device-mapped
+// address, which must share p's place within a 16-byte line; anything else
 // (pageable host memory, unknown pointers) is ZERO_ERR_INVALID_ARG, since the
-// GPU must not touch it.  *in_host (if given) tells whether the rows are in
-// host memory.
+// GPU must not touch it.  *on_host (if given) tells whether p is host memory.
+zero_status_t resolve_ptr(const void* p, void** out, bool* on_host = nullptr);
+
+// The descriptor the kernels read: g with base replaced by the address the
+// device reads it at (resolve_ptr).  *in_host (if given) tells whether the
+// rows are in host memory.
 zero_status_t resolve_grads(const zero_grads_t* g, zero_grads_t* out, bool* in_host = nullptr);
 
 // Launches the fused step over elements [b0, b0 + len) of a shard -- one

@@ -36,13 +36,13 @@
 
 namespace zero {
 
-zero_status_t resolve_grads(const zero_grads_t* g, zero_grads_t* out, bool* in_host)
+zero_status_t resolve_ptr(const void* p, void** out, bool* on_host)
 {
-    *out = *g;
-    if (in_host)
-        *in_host = false;
+    *out = const_cast<void*>(p);
+    if (on_host)
+        *on_host = false;
     cudaPointerAttributes at;
-    if (cudaPointerGetAttributes(&at, g->base) != cudaSuccess) {
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
         (void)cudaGetLastError();
         return ZERO_ERR_INVALID_ARG;
     }
@@ -51,15 +51,26 @@ zero_status_t resolve_grads(const zero_grads_t* g, zero_grads_t* out, bool* in_h
     case cudaMemoryTypeManaged:
         return ZERO_OK;
     case cudaMemoryTypeHost:
-        if (!at.devicePointer || ((uintptr_t)at.devicePointer & 15) != 0)
+        // the mapping keeps the address's place within a 16-byte line, so
+        // every alignment the caller's pointer was checked for still holds
+        if (!at.devicePointer || (((uintptr_t)at.devicePointer ^ (uintptr_t)p) & 15) != 0)
             return ZERO_ERR_INVALID_ARG;
-        out->base = at.devicePointer;
-        if (in_host)
-            *in_host = true;
+        *out = at.devicePointer;
+        if (on_host)
+            *on_host = true;
         return ZERO_OK;
     default:
         return ZERO_ERR_INVALID_ARG;
     }
+}
+
+zero_status_t resolve_grads(const zero_grads_t* g, zero_grads_t* out, bool* in_host)
+{
+    *out = *g;
+    void* base = nullptr;
+    const zero_status_t st = resolve_ptr(g->base, &base, in_host);
+    out->base = base;
+    return st;
 }
 
 namespace {
@@ -972,9 +983,13 @@ extern "C" zero_status_t zero_gather_params_shard(const float* master, uint64_t 
         return ZERO_ERR_INVALID_ARG;
     if (n == 0)
         return ZERO_OK;
-    uint16_t* slot = static_cast<uint16_t*>(gathered) + slot_offset_elems;
-    if (ranges_overlap(slot, master, n * 4))   // conservative: the larger extent
-        return ZERO_ERR_INVALID_ARG;
+    if (ranges_overlap(static_cast<uint16_t*>(gathered) + slot_offset_elems, master, n * 4))
+        return ZERO_ERR_INVALID_ARG;   // conservative: the larger extent
+    void* gdev = nullptr;   // the slot at the address the device writes it
+    const zero_status_t st = resolve_ptr(gathered, &gdev);
+    if (st != ZERO_OK)
+        return st;
+    uint16_t* slot = static_cast<uint16_t*>(gdev) + slot_offset_elems;
     launch_cast(master, n, slot, dtype, static_cast<cudaStream_t>(stream));
     return launch_status();
 }
@@ -998,9 +1013,13 @@ extern "C" zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layou
     st = resolve_grads(g, &gr, &host_rows);
     if (st != ZERO_OK)
         return st;
+    void* gdev = nullptr;   // the gathered buffer at the address the device writes it
+    st = resolve_ptr(gathered, &gdev);
+    if (st != ZERO_OK)
+        return st;
     const StepScalars k = make_scalars(h, g->nd, loss_scale);
     const uint16_t* rows = static_cast<const uint16_t*>(gr.base) + g->offset;
-    uint16_t* gath = static_cast<uint16_t*>(gathered) + gathered_offset_elems;
+    uint16_t* gath = static_cast<uint16_t*>(gdev) + gathered_offset_elems;
     for (uint64_t b0 = 0; b0 < n; b0 += bucket_elems) {
         const uint64_t len = n - b0 < bucket_elems ? n - b0 : bucket_elems;
         st = launch_fused_bucket(rows, g, in, out, gath, b0, len, k, host_rows, d_nonfinite,
@@ -1038,12 +1057,16 @@ extern "C" zero_status_t zero_step_shard_unfused(const zero_grads_t* g, const ze
     st = resolve_grads(g, &gr, &host_rows);
     if (st != ZERO_OK)
         return st;
+    void* gdev = nullptr;   // the gathered buffer at the address the device writes it
+    st = resolve_ptr(gathered, &gdev);
+    if (st != ZERO_OK)
+        return st;
     const int variant = fused_variant(host_rows);
     const StepScalars k = make_scalars(h, g->nd, loss_scale);
     const StepScalars k_adam_only = make_scalars(h, 1, 1.0);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const uint16_t* rows = static_cast<const uint16_t*>(gr.base) + g->offset;
-    uint16_t* gath = static_cast<uint16_t*>(gathered) + gathered_offset_elems;
+    uint16_t* gath = static_cast<uint16_t*>(gdev) + gathered_offset_elems;
     for (uint64_t b0 = 0; b0 < n; b0 += bucket_elems) {
         const uint64_t len = n - b0 < bucket_elems ? n - b0 : bucket_elems;
         // Shift the bucket inside cb so that cb and the state share a 16-byte

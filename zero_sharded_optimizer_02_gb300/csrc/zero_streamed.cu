@@ -126,12 +126,16 @@ extern "C" zero_status_t zero_step_shard_streamed(
         return ZERO_OK;
     bool host_rows = false;
     zero_grads_t gr;   // the rows at the address the device reads them
-    const zero_status_t rs = resolve_grads(g, &gr, &host_rows);
+    zero_status_t rs = resolve_grads(g, &gr, &host_rows);
+    if (rs != ZERO_OK)
+        return rs;
+    void* gdev = nullptr;   // the gathered buffer at the address the device writes it
+    rs = resolve_ptr(gathered, &gdev);
     if (rs != ZERO_OK)
         return rs;
     const StepScalars k = make_scalars(h, g->nd, loss_scale);
     const uint16_t* rows = static_cast<const uint16_t*>(gr.base) + g->offset;
-    uint16_t* gath = static_cast<uint16_t*>(gathered) + gathered_offset_elems;
+    uint16_t* gath = static_cast<uint16_t*>(gdev) + gathered_offset_elems;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // Consecutive buckets form launch groups: as many groups as the shard's
     // step traffic holds ZERO_STREAM_GROUP_BYTES (the environment variable of

@@ -108,11 +108,16 @@ class DataParallelStep:
                  (what zero_gather_range collects a layer from)
     fused        zero_step_shard (default) or zero_step_shard_unfused
     process_group  if given, the skip flag is OR-ed over it every step
+    gathered_on_host  keep the gathered buffers in page-locked host memory:
+                 the kernels write the cast parameters there in place over
+                 the host link, so they reach the host with no copy of
+                 their own
     """
 
     def __init__(self, psi: int, nd: int, ranks, grad_dtype: str, hparams: dict,
                  loss_scale: float, bucket: int, device="cuda", gathered: str = "full",
-                 fused: bool = True, process_group=None, row_align: int = 8, stream=None):
+                 fused: bool = True, process_group=None, row_align: int = 8, stream=None,
+                 gathered_on_host: bool = False):
         self.psi, self.nd, self.ranks = psi, nd, list(ranks)
         self.grad_dtype = grad_dtype
         self.hp = dict(hparams)
@@ -123,21 +128,11 @@ class DataParallelStep:
         self.pg = process_group
         self.layouts = {r: _abi.zero_partition_layout(psi, nd, r, row_align) for r in self.ranks}
         self.state = {r: RankState(self.layouts[r], self.device) for r in self.ranks}
-        s = int(self.layouts[self.ranks[0]].shard_elems)
-        tdt = _TORCH_DTYPES[grad_dtype]
-        self.gathered_mode = gathered
-        if gathered == "full":
-            n = nd * s + 8
-            self.gathered = [torch.zeros(n, dtype=tdt, device=self.device) for _ in range(2)]
-        elif gathered == "pitched":
-            pitch = int(self.layouts[self.ranks[0]].row_pitch)
-            self.gathered = [torch.zeros(nd, max(pitch, 8), dtype=tdt, device=self.device)
-                             for _ in range(2)]
-        elif gathered == "slot":
-            self.gathered = [{r: torch.zeros(max(s, 1) + 8, dtype=tdt, device=self.device)
-                              for r in self.ranks} for _ in range(2)]
-        else:
+        if gathered not in ("full", "pitched", "slot"):
             raise ValueError(gathered)
+        self.gathered_mode = gathered
+        self.gathered_on_host = bool(gathered_on_host)
+        self.gathered = [self._new_gathered() for _ in range(2)]
         self.gcur = 0
         self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
         self.flag = torch.zeros(1, dtype=torch.int32, device=self.device)
@@ -153,6 +148,19 @@ class DataParallelStep:
                             self.hp["weight_decay"], 1)
 
     # -- buffers -------------------------------------------------------------
+
+    def _new_gathered(self):
+        """One gathered buffer set (zeroed) in the configured layout and memory."""
+        tdt = _TORCH_DTYPES[self.grad_dtype]
+        s = int(self.layouts[self.ranks[0]].shard_elems)
+        where = {"dtype": tdt, "device": "cpu", "pin_memory": True} if self.gathered_on_host \
+            else {"dtype": tdt, "device": self.device}
+        if self.gathered_mode == "full":
+            return torch.zeros(self.nd * s + 8, **where)
+        if self.gathered_mode == "pitched":
+            pitch = int(self.layouts[self.ranks[0]].row_pitch)
+            return torch.zeros(self.nd, max(pitch, 8), **where)
+        return {r: torch.zeros(max(s, 1) + 8, **where) for r in self.ranks}
 
     def gathered_view(self, rank=None, which: str = "cur") -> torch.Tensor:
         i = self.gcur if which == "cur" else 1 - self.gcur
@@ -334,10 +342,8 @@ class PipelinedStep(DataParallelStep):
             self.state[r] = RankState(self.layouts[r], self.device, nbuf=nbuf)
             self.state[r].bufs[0].copy_(old.bufs[old.cur])
             self.state[r].states = [_abi.state(b[0], b[1], b[2]) for b in self.state[r].bufs]
-        cur = self.gathered[self.gcur]
-        self.gathered = [cur] + [
-            torch.zeros_like(cur) if self.gathered_mode in ("full", "pitched") else
-            {r: torch.zeros_like(t) for r, t in cur.items()} for _ in range(nbuf - 1)]
+        self.gathered = [self.gathered[self.gcur]] + [self._new_gathered()
+                                                      for _ in range(nbuf - 1)]
         self.gcur = 0
         self.flags = torch.zeros(depth + 1, dtype=torch.int32, device=self.device)
         self.flags_host = torch.zeros(depth + 1, dtype=torch.int32, pin_memory=True)
