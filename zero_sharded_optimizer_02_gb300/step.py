@@ -142,7 +142,7 @@ class DataParallelStep:
         self.cb = None
         self.cb_elems = 0
         if not fused:
-            self.cb_elems = min(self.bucket, s) + 4
+            self.cb_elems = min(self.bucket, int(self.layouts[self.ranks[0]].shard_elems)) + 4
             self.cb = torch.empty(self.cb_elems, dtype=torch.float32, device=self.device)
         self.h = _abi.adamw(self.hp["lr"], self.hp["beta1"], self.hp["beta2"], self.hp["eps"],
                             self.hp["weight_decay"], 1)
