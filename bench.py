@@ -42,6 +42,18 @@ NOMINAL_HBM_GBS = 7900.0
 L2_BYTES = 129e6
 
 
+def host_available_gb():
+    """MemAvailable of this host in GB (None if it cannot be read)."""
+    try:
+        with open("/proc/meminfo") as f:
+            for ln in f:
+                if ln.startswith("MemAvailable:"):
+                    return int(ln.split()[1]) * 1024 / 1e9
+    except (OSError, ValueError, IndexError):
+        pass
+    return None
+
+
 def measured_peaks() -> dict:
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -326,15 +338,26 @@ def run_gpu(args) -> None:
     if args.e2e_steps > 0:
         # the step's gradients in page-locked host memory (each rank its own);
         # every rank must have them, or no rank runs the end-to-end leg
-        pin_gb = (grads.numel() + n) * grads.element_size() / 1e9
-        try:
-            host_grads = torch.empty(grads.shape, dtype=grads.dtype, pin_memory=True)
-            host_grads.copy_(grads)
-            host_params = torch.empty(n, dtype=grads.dtype, pin_memory=True)
-            pin_error = ""
-        except RuntimeError as err:
-            host_grads = host_params = None
-            pin_error = str(err).splitlines()[0][:160] if str(err) else type(err).__name__
+        pin_gb = (grads.numel() + 3 * n) * grads.element_size() / 1e9
+        # every process of this node pins as much at once: leave at least half
+        # of the host's available memory to everything else
+        local_world = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+        avail_gb = host_available_gb()
+        if world > 1:
+            dist.barrier()
+        host_grads = host_params = None
+        if avail_gb is not None and local_world * pin_gb > 0.5 * avail_gb:
+            pin_error = (f"{local_world} x {pin_gb:.1f} GB would exceed half of the host's "
+                         f"{avail_gb:.0f} GB available")
+        else:
+            try:
+                host_grads = torch.empty(grads.shape, dtype=grads.dtype, pin_memory=True)
+                host_grads.copy_(grads)
+                host_params = torch.empty(n, dtype=grads.dtype, pin_memory=True)
+                pin_error = ""
+            except RuntimeError as err:
+                host_grads = host_params = None
+                pin_error = str(err).splitlines()[0][:160] if str(err) else type(err).__name__
         pinned_everywhere = -max_over_ranks(-float(not pin_error), group, dev) > 0.5
         if not pinned_everywhere:
             e2e = {"unavailable": f"could not pin {pin_gb:.1f} GB of host memory on every rank"
