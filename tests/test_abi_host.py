@@ -105,6 +105,26 @@ def test_status_strings(z):
 A = 1 << 20   # 16-byte aligned
 
 
+def test_valid_fake_arguments_reach_the_runtime(z):
+    """The base case of the rejection tests below passes every host-side check
+    and fails only where the library first asks the CUDA runtime about a
+    pointer: ZERO_ERR_CUDA without a device, ZERO_ERR_INVALID_ARG for a
+    pointer the runtime does not know.  So each rejection below comes from
+    its own check, not from that question."""
+    import torch
+    L = z.zero_partition_layout(1000, 4, 1, 8)
+    g = z.grads(A, 4 * 256, 256, 4, "f16")
+    expect = z.ZERO_ERR_INVALID_ARG if torch.cuda.is_available() else z.ZERO_ERR_CUDA
+    with pytest.raises(z.ZeroError) as e:
+        z.zero_step_shard(g, L, _state(z, 2 * A), _state(z, 4 * A), 8 * A, L.begin, 64, 1024.0,
+                          _h(z), 9 * A)
+    assert e.value.status == expect
+    with pytest.raises(z.ZeroError) as e:
+        z.zero_step_shard_streamed(g, L, _state(z, 2 * A), _state(z, 4 * A), 8 * A, L.begin,
+                                   64, 1024.0, _h(z), 10 * A, 1, 10 ** 9, 9 * A, 11 * A)
+    assert e.value.status == expect
+
+
 def _h(z, step=1):
     return z.adamw(1e-4, 0.9, 0.999, 1e-8, 0.01, step)
 
@@ -122,6 +142,10 @@ def _state(z, base):
     ("step_zero", "ZERO_ERR_INVALID_ARG"), ("bad_beta", "ZERO_ERR_INVALID_ARG"),
     ("bad_loss_scale", "ZERO_ERR_INVALID_ARG"), ("odd_gathered", "ZERO_ERR_ALIGNMENT"),
     ("null_flag", "ZERO_ERR_INVALID_ARG"), ("row_overflow", "ZERO_ERR_INVALID_ARG"),
+    ("slot_overlaps_state_in", "ZERO_ERR_INVALID_ARG"),
+    ("slot_overlaps_state_out", "ZERO_ERR_INVALID_ARG"),
+    ("slot_overlaps_rows", "ZERO_ERR_INVALID_ARG"),
+    ("slot_offset_overflow", "ZERO_ERR_INVALID_ARG"),
 ])
 def test_step_shard_rejects(z, case, status):
     L = z.zero_partition_layout(1000, 4, 1, 8)
@@ -160,13 +184,27 @@ def test_step_shard_rejects(z, case, status):
         flag = None
     elif case == "row_overflow":
         g.row_stride = 1 << 62
+    goff = L.begin
+    if case == "slot_overlaps_state_in":          # the slot's last element on master[0]
+        gathered = s_in.master - 2 * (goff + L.length - 1)
+    elif case == "slot_overlaps_state_out":       # the slot starts inside v'
+        gathered = s_out.v + 4 * 100 - 2 * goff
+    elif case == "slot_overlaps_rows":            # the slot lands in the last row
+        gathered = A + 2 * (256 + 3 * 1024 + 10) - 2 * goff
+    elif case == "slot_offset_overflow":
+        goff = 1 << 62
     with pytest.raises(z.ZeroError) as e:
-        z.zero_step_shard(g, L, s_in, s_out, gathered, L.begin, bucket, ls, h, flag)
+        z.zero_step_shard(g, L, s_in, s_out, gathered, goff, bucket, ls, h, flag)
     assert e.value.status == getattr(z, status)
-    # the unfused variant validates the same way, plus its workspace
-    if case in ("misaligned_base", "overlap_state", "bucket_zero"):
+    if case.startswith("slot_"):                 # the bucket-ready step checks the same
         with pytest.raises(z.ZeroError) as e:
-            z.zero_step_shard_unfused(g, L, s_in, s_out, gathered, L.begin, bucket, ls, h,
+            z.zero_step_shard_streamed(g, L, s_in, s_out, gathered, goff, bucket, ls, h,
+                                       10 * A, 1, 10 ** 9, flag, 11 * A)
+        assert e.value.status == getattr(z, status)
+    # the unfused variant validates the same way, plus its workspace
+    if case in ("misaligned_base", "overlap_state", "bucket_zero", "slot_overlaps_rows"):
+        with pytest.raises(z.ZeroError) as e:
+            z.zero_step_shard_unfused(g, L, s_in, s_out, gathered, goff, bucket, ls, h,
                                       10 * A, 1 << 20, flag)
         assert e.value.status == getattr(z, status)
 

@@ -31,12 +31,25 @@ bool adamw_valid(const zero_adamw_t* h);
 // (pass nd = 1, loss_scale = 1 when the gradient is already scaled).
 StepScalars make_scalars(const zero_adamw_t* h, uint32_t nd, double loss_scale);
 
+// Host-side validation shared by every shard-step entry point (nothing is
+// launched on failure): the gradient descriptor for the shard's L->length
+// elements, the in/out state (16-byte aligned; each output its input or
+// disjoint from all of them), the gathered slot (2-byte aligned, no wrap,
+// disjoint from the state and the rows), the flag, bucket size, loss scale
+// and hyperparameters.
+zero_status_t check_step_args(const zero_grads_t* g, const zero_layout_t* L,
+                              const zero_state_t* in, const zero_state_t* out,
+                              const void* gathered, uint64_t gathered_offset_elems,
+                              uint64_t bucket_elems, double loss_scale, const zero_adamw_t* h,
+                              const uint32_t* flag);
+
 // The address the kernels access p at.  Device and managed memory are
 // accessed where they are; page-locked host memory registered with CUDA is
 // accessed in place over the host link (zero-copy) at its device-mapped
 // address, which must share p's place within a 16-byte line; anything else
 // (pageable host memory, unknown pointers) is ZERO_ERR_INVALID_ARG, since the
-// GPU must not touch it.  *on_host (if given) tells whether p is host memory.
+// GPU must not touch it; ZERO_ERR_CUDA if the runtime cannot answer (no
+// device or driver).  *on_host (if given) tells whether p is host memory.
 zero_status_t resolve_ptr(const void* p, void** out, bool* on_host = nullptr);
 
 // The descriptor the kernels read: g with base replaced by the address the

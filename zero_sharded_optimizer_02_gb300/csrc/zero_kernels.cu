@@ -42,9 +42,12 @@ zero_status_t resolve_ptr(const void* p, void** out, bool* on_host)
     if (on_host)
         *on_host = false;
     cudaPointerAttributes at;
-    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    const cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
         (void)cudaGetLastError();
-        return ZERO_ERR_INVALID_ARG;
+        // a pointer CUDA does not know is the caller's error; no device or
+        // driver is the runtime's
+        return e == cudaErrorInvalidValue ? ZERO_ERR_INVALID_ARG : ZERO_ERR_CUDA;
     }
     switch (at.type) {
     case cudaMemoryTypeDevice:
@@ -841,25 +844,53 @@ void launch_cast(const float* master, uint64_t n, uint16_t* gath, int dtype, cud
 
 bool loss_scale_valid(double ls) { return ls > 0.0 && ls <= 1.0e300; }
 
-zero_status_t check_step_common(const zero_grads_t* g, const zero_layout_t* L,
-                                const zero_state_t* in, const zero_state_t* out,
-                                const void* gathered, uint64_t bucket_elems, double loss_scale,
-                                const zero_adamw_t* h, const uint32_t* flag)
+// [a, a + abytes) and [b, b + bbytes) share a byte (spans already checked
+// not to wrap).
+bool spans_overlap(const void* a, uint64_t abytes, const void* b, uint64_t bbytes)
+{
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + bbytes && y < x + abytes;
+}
+
+}  // namespace
+
+zero_status_t check_step_args(const zero_grads_t* g, const zero_layout_t* L,
+                              const zero_state_t* in, const zero_state_t* out,
+                              const void* gathered, uint64_t gathered_offset_elems,
+                              uint64_t bucket_elems, double loss_scale, const zero_adamw_t* h,
+                              const uint32_t* flag)
 {
     if (!L || !gathered || !flag || bucket_elems == 0 || !loss_scale_valid(loss_scale) ||
         !adamw_valid(h))
         return ZERO_ERR_INVALID_ARG;
     if (L->nd == 0 || L->length > L->shard_elems)
         return ZERO_ERR_INVALID_ARG;
-    zero_status_t st = check_grads(g, 0, L->length);
+    const uint64_t n = L->length;
+    zero_status_t st = check_grads(g, 0, n);
     if (st != ZERO_OK)
         return st;
     if (!aligned(gathered, 2) || !aligned(flag, 4))
         return ZERO_ERR_ALIGNMENT;
-    return check_state(in, out, L->length, 16);
+    st = check_state(in, out, n, 16);
+    if (st != ZERO_OK)
+        return st;
+    // the gathered slot [gathered + offset, ... + n) must not wrap the
+    // address space, and must share no byte with the state or the rows
+    const uint64_t lim = 1ull << 61;
+    if (gathered_offset_elems > lim || n > lim - gathered_offset_elems ||
+        (uintptr_t)gathered > UINTPTR_MAX - 2 * (gathered_offset_elems + n))
+        return ZERO_ERR_INVALID_ARG;
+    const uint16_t* slot = static_cast<const uint16_t*>(gathered) + gathered_offset_elems;
+    const float* st6[6] = {in->master, in->m, in->v, out->master, out->m, out->v};
+    for (const float* p : st6)
+        if (spans_overlap(slot, 2 * n, p, 4 * n))
+            return ZERO_ERR_INVALID_ARG;
+    const uint16_t* rows = static_cast<const uint16_t*>(g->base) + g->offset;
+    const uint64_t row_span = (uint64_t)(g->nd - 1) * g->row_stride + n;
+    if (n && spans_overlap(slot, 2 * n, rows, 2 * row_span))
+        return ZERO_ERR_INVALID_ARG;
+    return ZERO_OK;
 }
-
-}  // namespace
 
 zero_status_t launch_fused_bucket(const uint16_t* rows, const zero_grads_t* g,
                                   const zero_state_t* in, const zero_state_t* out,
@@ -875,7 +906,7 @@ zero_status_t launch_fused_bucket(const uint16_t* rows, const zero_grads_t* g,
         const uint64_t e0 = b0 + w0;
         FusedArgs a{rows + e0, g->row_stride, g->nd, split_window(g->offset + e0, w1 - w0),
                     in->master + e0, in->m + e0, in->v + e0, out->master + e0, out->m + e0,
-                    out->v + e0, gath + e0, k, d_nonfinite, gate};
+                    out->v + e0, gath + e0, k, d_nonfinite, gate, nullptr};
         const int width = store_width(gath + e0 + a.sp.head);
         if (g->dtype == ZERO_F16)
             launch_fused_dt<ZERO_F16>(a, width, v8, variant, s);
@@ -1001,8 +1032,8 @@ extern "C" zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layou
                                          const zero_adamw_t* h, uint32_t* d_nonfinite,
                                          void* stream)
 {
-    zero_status_t st = check_step_common(g, L, in, out, gathered, bucket_elems, loss_scale, h,
-                                         d_nonfinite);
+    zero_status_t st = check_step_args(g, L, in, out, gathered, gathered_offset_elems,
+                                       bucket_elems, loss_scale, h, d_nonfinite);
     if (st != ZERO_OK)
         return st;
     const uint64_t n = L->length;
@@ -1040,8 +1071,8 @@ extern "C" zero_status_t zero_step_shard_unfused(const zero_grads_t* g, const ze
                                                  uint64_t cb_elems, uint32_t* d_nonfinite,
                                                  void* stream)
 {
-    zero_status_t st = check_step_common(g, L, in, out, gathered, bucket_elems, loss_scale, h,
-                                         d_nonfinite);
+    zero_status_t st = check_step_args(g, L, in, out, gathered, gathered_offset_elems,
+                                       bucket_elems, loss_scale, h, d_nonfinite);
     if (st != ZERO_OK)
         return st;
     const uint64_t n = L->length;
@@ -1149,8 +1180,8 @@ extern "C" zero_status_t zero_step_shard_unfused_static(const zero_grads_t* g,
     const uint64_t used = bucket_elems < L->length ? bucket_elems : L->length;
     if (used > ZERO_STATIC_CB_MAX_BUCKET)
         return ZERO_ERR_INVALID_ARG;   // the bucket does not fit the static fusion buffer
-    zero_status_t st = check_step_common(g, L, in, out, gathered, bucket_elems, loss_scale, h,
-                                         d_nonfinite);
+    zero_status_t st = check_step_args(g, L, in, out, gathered, gathered_offset_elems,
+                                       bucket_elems, loss_scale, h, d_nonfinite);
     if (st != ZERO_OK)
         return st;
     float* cb = nullptr;

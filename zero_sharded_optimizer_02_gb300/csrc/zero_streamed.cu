@@ -76,12 +76,6 @@ __global__ void k_wait_ready(const uint32_t* words, uint32_t count, uint32_t epo
 
 bool is_aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
-bool overlap(const void* a, const void* b, uint64_t bytes)
-{
-    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
-    return x < y + bytes && y < x + bytes;
-}
-
 }  // namespace
 }  // namespace zero
 
@@ -94,39 +88,22 @@ extern "C" zero_status_t zero_step_shard_streamed(
     uint32_t epoch, uint64_t timeout_ns, uint32_t* d_nonfinite, uint32_t* d_status,
     void* stream)
 {
-    if (!g || !L || !in || !out || !gathered || !h || !d_ready || !d_nonfinite || !d_status ||
-        bucket_elems == 0 || !(loss_scale > 0.0 && loss_scale <= 1.0e300) || !adamw_valid(h))
+    zero_status_t rs = check_step_args(g, L, in, out, gathered, gathered_offset_elems,
+                                       bucket_elems, loss_scale, h, d_nonfinite);
+    if (rs != ZERO_OK)
+        return rs;
+    if (!d_ready || !d_status)
         return ZERO_ERR_INVALID_ARG;
     if (timeout_ns == 0 || timeout_ns > ZERO_MAX_WAIT_NS)
         return ZERO_ERR_INVALID_ARG;   // every device wait must stay bounded
-    if (!g->base || g->nd == 0 || (g->dtype != ZERO_F16 && g->dtype != ZERO_BF16) ||
-        L->length > L->shard_elems)
-        return ZERO_ERR_INVALID_ARG;
-    if (!is_aligned(g->base, 16) || (g->row_stride & 7) || (g->offset & 7) ||
-        !is_aligned(gathered, 2) || !is_aligned(d_ready, 4) || !is_aligned(d_nonfinite, 4) ||
-        !is_aligned(d_status, 4))
+    if (!is_aligned(d_ready, 4) || !is_aligned(d_status, 4))
         return ZERO_ERR_ALIGNMENT;
-    const float* ins[3] = {in->master, in->m, in->v};
-    float* outs[3] = {out->master, out->m, out->v};
     const uint64_t n = L->length;
-    const uint64_t lim = 1ull << 61;   // element indices stay far from overflow
-    if (n > lim || g->offset > lim - n ||
-        (g->nd > 1 && g->row_stride > (lim - g->offset - n) / (g->nd - 1)))
-        return ZERO_ERR_INVALID_ARG;
-    for (int i = 0; i < 3; ++i) {
-        if (!ins[i] || !outs[i])
-            return ZERO_ERR_INVALID_ARG;
-        if (!is_aligned(ins[i], 16) || !is_aligned(outs[i], 16))
-            return ZERO_ERR_ALIGNMENT;
-        for (int j = 0; j < 3; ++j)
-            if (!(i == j && outs[i] == ins[j]) && overlap(outs[i], ins[j], n * 4))
-                return ZERO_ERR_INVALID_ARG;
-    }
     if (n == 0)
         return ZERO_OK;
     bool host_rows = false;
     zero_grads_t gr;   // the rows at the address the device reads them
-    zero_status_t rs = resolve_grads(g, &gr, &host_rows);
+    rs = resolve_grads(g, &gr, &host_rows);
     if (rs != ZERO_OK)
         return rs;
     void* gdev = nullptr;   // the gathered buffer at the address the device writes it
