@@ -68,8 +68,11 @@ def test_gpu_arm_line():
     e = d["e2e"]
     assert e["value"] > 0 and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 8 * n * 2 and e["d2h_bytes_per_step"] == 2 * n + 4
-    assert 0 < e["link"]["frac"] <= 1.5
-    assert set(e["other_forms"]) == {"fed", "sequential", "copies_alone"}
+    # the copy engines' rate varies by box; a copy slower than the zero-copy
+    # step is flagged as no bound
+    assert e["link"]["frac"] > 0
+    assert ("note" in e["link"]) == (e["link"]["frac"] > 1)
+    assert set(e["other_forms"]) == {"fed", "sequential", "zero_copy_read_back", "copies_alone"}
     assert all(len(v) == 1 for v in e["ms_per_iteration"].values())
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] == 4 and cb["value"] > 0
