@@ -542,7 +542,7 @@ def run_gpu(args) -> None:
         "clocks": clocks,
         "wall_s_timed": wall1 - wall0,
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:      # the host-core baseline: N = 1 only
         line["cpu_baseline"] = cpu_baseline(w, dp_rank, args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -105,3 +105,4 @@ def test_gpu_arm_two_processes():
     assert d["config"]["rank"] == 0 and d["skipped_steps"] == 0
     assert d["gpu_launches"] == 2 * 6          # both processes' launches
     assert d["e2e"]["value"] > 0
+    assert "cpu_baseline" not in d             # the host-core baseline is timed at N = 1 only
