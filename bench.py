@@ -375,9 +375,18 @@ def run_gpu(args) -> None:
                     host_params.copy_(gview[slot0:slot0 + n], non_blocking=True)
                 stream.synchronize()
 
+            fed_timeouts = []
+
             def host_fed():
                 dps.launch_host_fed(dp_rank, host_grads, desc[dp_rank], stream_bucket, copy_stream)
-                dps.commit(dps.decide())
+                try:
+                    skipped = dps.decide()
+                except _abi.ZeroError as err:     # a bucket never arrived within the wait
+                    if err.status != _abi.ZERO_ERR_TIMEOUT:
+                        raise
+                    fed_timeouts.append(1)
+                    return
+                dps.commit(skipped)
                 read_back()
 
             def sequential():
@@ -426,7 +435,6 @@ def run_gpu(args) -> None:
                     fn()
                     if it:
                         times[k].append((time.perf_counter() - t0) * 1e3)
-            assert dps.host_fed_status() == 0, "a bucket never arrived"
             mean = {k: max_over_ranks(statistics.fmean(v), group, dev) for k, v in times.items()}
             best = {k: max_over_ranks(min(v), group, dev) for k, v in times.items()}
             grad_bytes = w.nd * n * host_grads.element_size()
@@ -451,7 +459,11 @@ def run_gpu(args) -> None:
                            "the host link), then the flag device-to-host",
                    "other_forms": {
                        "fed": form("fed", f"zero_feed_buckets (DMA, {nbk} transfer buckets) + "
-                                          "zero_step_shard_streamed", grad_bytes + 4 * nbk),
+                                          "zero_step_shard_streamed", grad_bytes + 4 * nbk)
+                       if not fed_timeouts else
+                       {"unavailable": f"a bucket-ready wait expired (ZERO_ERR_TIMEOUT) in "
+                                       f"{len(fed_timeouts)} of {args.e2e_steps + 1} iterations; "
+                                       f"its times are not a measurement"},
                        "sequential": form("sequential", "one DMA copy of the gradients, then "
                                                         "zero_step_shard", grad_bytes),
                        "zero_copy_read_back": form(

@@ -202,12 +202,33 @@ class DataParallelStep:
         return launches
 
     def decide(self) -> bool:
-        """Read the nonfinite flag (OR-ed over the process group if any)."""
+        """Read the nonfinite flag (OR-ed over the process group if any).
+
+        After a host-fed step whose bucket wait expired, raises ZeroError
+        (ZERO_ERR_TIMEOUT) instead: that step is neither committed nor
+        skipped, the committed state is untouched, and the status and flag
+        words are cleared so the next step can run."""
         with torch.cuda.stream(self.stream):
             self.flag_host.copy_(self.flag, non_blocking=True)
         self.stream.synchronize()
-        bad = _abi.check_step_flag(self.flag_host[0])
-        return global_skip(bad, self.pg, self.device)
+        word = int(self.flag_host[0])
+        status = _abi.ZERO_OK
+        if getattr(self, "_fed_pending", False):
+            self._fed_pending = False
+            status = int(self._status.item())
+        expired = status != _abi.ZERO_OK or bool(word & _abi.ZERO_STEP_FLAG_WAIT_TIMEOUT)
+        # every rank takes part in the decision before any rank raises
+        skip = global_skip(word != 0 or expired, self.pg, self.device)
+        if expired:
+            with torch.cuda.stream(self.stream):
+                self.flag.zero_()
+                if status != _abi.ZERO_OK:
+                    self._status.zero_()
+            self.stream.synchronize()
+            raise _abi.ZeroError(_abi.ZERO_ERR_TIMEOUT,
+                                 "bucket-ready step (a bucket never arrived)"
+                                 if status != _abi.ZERO_OK else "step kernel")
+        return skip
 
     def commit(self, skipped: bool) -> None:
         self.skipped_steps.append(skipped)
@@ -229,7 +250,9 @@ class DataParallelStep:
         each bucket's contributions on ``copy_stream`` and marks it ready, so
         the optimizer overlaps the transfer.  ``host_rows`` is [nd, m] pinned
         (contributor j's shard at row j); ``dev_grads`` the Grads descriptor of
-        the device rows they land in.  Returns the kernel launches issued."""
+        the device rows they land in.  Returns the kernel launches issued.
+        If a bucket's wait (timeout_ns) expires, decide() raises ZeroError
+        (ZERO_ERR_TIMEOUT) for this step."""
         L = self.layouts[rank]
         n = int(L.length)
         nb = -(-n // stream_bucket) if n else 0
@@ -258,6 +281,7 @@ class DataParallelStep:
                                self._ready, self._epoch_host, copy_stream)
         self._feed_done = torch.cuda.Event()
         self._feed_done.record(copy_stream)
+        self._fed_pending = True
         return _abi.streamed_launch_count(n, stream_bucket, int(dev_grads.nd),
                                           int(dev_grads.offset))
 
@@ -408,8 +432,21 @@ class PipelinedStep(DataParallelStep):
     def _decide_oldest(self) -> bool:
         out_buf, t, slot, ev, grads = self.pending.pop(0)
         ev.synchronize()
-        bad = _abi.check_step_flag(int(self._flags_np[slot]))
-        skipped = global_skip(bad, self.pg, self.device)
+        word = int(self._flags_np[slot])
+        # every rank takes part in the decision before any rank raises
+        skipped = global_skip(word != 0, self.pg, self.device)
+        if word & _abi.ZERO_STEP_FLAG_WAIT_TIMEOUT:
+            # a kernel's pipeline wait expired: the committed state stays, and
+            # the speculative steps built on this one are dropped (their
+            # kernels finish first in stream order; their flags are cleared)
+            with torch.cuda.stream(self.stream):
+                for s in [slot] + [p[2] for p in self.pending]:
+                    self.flags[s:s + 1].zero_()
+            for p in self.pending:
+                p[3].synchronize()
+            self.pending = []
+            self.stream.synchronize()
+            raise _abi.ZeroError(_abi.ZERO_ERR_TIMEOUT, "step kernel")
         self.skipped_steps.append(skipped)
         if not skipped:
             for r in self.ranks:
