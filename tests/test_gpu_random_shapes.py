@@ -2,7 +2,8 @@
 
 Each case draws a flat size, a data-parallel degree, a bucket size, a
 gradient type, the ranks held and the path (fused with each kernel variant,
-unfused, bucket-ready), runs two steps on the GPU with every rank's whole
+unfused, bucket-ready, or fused with the rows and the gathered parameters in
+pinned host memory), runs two steps on the GPU with every rank's whole
 gradient resident, and compares every element of state and parameters with
 the oracle's unsharded step.  The draws favour the awkward: sizes not
 multiple of 8, shards that are short or empty, buckets of 1 to a few
@@ -21,7 +22,7 @@ from gpu_util import DEV, check_against_oracle, full_rows, make_group, oracle_tr
 
 pytestmark = pytest.mark.gpu
 
-PATHS = ["ring", "registers", "tma", "unfused", "streamed"]
+PATHS = ["ring", "registers", "tma", "unfused", "streamed", "host"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -79,11 +80,18 @@ def test_random_shape(seed, monkeypatch):
         monkeypatch.setenv("ZERO_FUSED_VARIANT", path)
     if path == "streamed":
         monkeypatch.setenv("ZERO_STREAM_GROUP_BYTES", "0")
-    dps = make_group(w, fused=path != "unfused", bucket=bucket, psi=psi, nd=nd)
+    dps = make_group(w, fused=path != "unfused", bucket=bucket, psi=psi, nd=nd,
+                     gathered_on_host=path == "host")
     _, hist = oracle_trajectory(w, np.arange(psi), 2, psi=psi, nd=nd)
     buf = None
     for k in range(2):
         buf, desc = full_rows(w, dps, k, buf)
+        if path == "host":
+            host = torch.empty(buf.shape, dtype=buf.dtype, pin_memory=True)
+            host.copy_(buf)
+            pitch = int(dps.layouts[0].row_pitch)
+            desc = {r: z.grads(host, nd * pitch, r * pitch, nd, w.grad_dtype)
+                    for r in dps.ranks}
         if path == "streamed":
             skipped = _streamed_step(w, dps, buf, bucket)
         else:
