@@ -1,4 +1,4 @@
-"""Multi-process host logic on the CPU: two gloo ranks (world size 2).
+"""Multi-process host logic on the CPU: gloo ranks (world sizes 2 and 4).
 
 Covers what the multi-process benchmark and driver rely on: the global skip
 decision (a one-word OR over the group), the max-over-ranks timing, the
@@ -54,9 +54,9 @@ def _checks(rank: int, world: int):
     assert max_over_ranks(rank + 1.5, g) == world - 1 + 1.5
     assert sum_over_ranks(rank + 5, g) == sum(r + 5 for r in range(world))
     assert data_parallel_rank(0, rank, 64) == rank
-    assert data_parallel_rank(62, rank, 64) == 62 + rank
+    assert data_parallel_rank(64 - world, rank, 64) == 64 - world + rank
     with pytest.raises(ValueError):
-        data_parallel_rank(63, 1, 64)
+        data_parallel_rank(65 - world, world - 1, 64)
 
     # one ZeRO-DP step, Nd = world, rank r owns shard r
     w = dataclasses.replace(synth.WORKLOADS["c0"], psi=1001, nd=world, bucket=64)
@@ -107,12 +107,13 @@ def _checks(rank: int, world: int):
         assert np.array_equal(v1.view(np.uint32), rv[begin:begin + n].view(np.uint32))
 
 
-def test_two_gloo_ranks():
+@pytest.mark.parametrize("world", [2, 4])
+def test_gloo_ranks(world):
     from zero_sharded_optimizer_02_gb300 import build
     build.build()
     import oracle
     oracle.build()
-    mp.spawn(_worker, args=(2, _free_port()), nprocs=2, join=True)
+    mp.spawn(_worker, args=(world, _free_port()), nprocs=world, join=True)
 
 
 def _worker_leaves(rank: int, world: int, port: int, result_path: str):
