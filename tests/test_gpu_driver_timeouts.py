@@ -44,8 +44,16 @@ def test_host_fed_wait_expiry_raises_and_keeps_the_state():
     rows, desc = shard_rows(w, dps, rank, 0)
     host = rows.cpu().pin_memory()
     rows.zero_()
-    before = [t.clone() for t in dps.state[rank].tensors()]
     copy, blocker = torch.cuda.Stream(DEV), torch.cuda.Stream(DEV)
+    # one ordinary host-fed step first: it also loads every kernel the step
+    # uses, since loading a kernel on first launch can wait for the kernels
+    # already running (the sleeping one below) and delay the wait kernel
+    dps.launch_host_fed(rank, host, desc[rank], bucket, copy)
+    assert not dps.decide()
+    dps.commit(False)
+    before = [t.clone() for t in dps.state[rank].tensors()]
+    torch.cuda._sleep(1000)
+    torch.cuda.synchronize()
     with torch.cuda.stream(blocker):
         torch.cuda._sleep(200_000_000)          # ~0.1 s; the copies queue behind it
     held = torch.cuda.Event()
@@ -56,17 +64,18 @@ def test_host_fed_wait_expiry_raises_and_keeps_the_state():
         dps.decide()
     assert e.value.status == z.ZERO_ERR_TIMEOUT
     torch.cuda.synchronize()
-    assert dps.t == 0 and int(dps.flag.item()) == 0 and dps.host_fed_status() == 0
+    assert dps.t == 1 and int(dps.flag.item()) == 0 and dps.host_fed_status() == 0
     for a, b in zip(before, dps.state[rank].tensors()):
         assert torch.equal(a, b)
-    # the next step runs normally and gives the fused step's result
+    # the next step runs normally: two committed steps, as the fused driver's
     dps.launch_host_fed(rank, host, desc[rank], bucket, copy)
     assert not dps.decide()
     dps.commit(False)
     ref = make_group(w, ranks=[rank], gathered="full")
     _, rdesc = shard_rows(w, ref, rank, 0)
-    assert not ref.step(rdesc)
-    assert _equal_state(dps, ref, rank)
+    for _ in range(2):
+        assert not ref.step(rdesc)
+    assert dps.t == ref.t == 2 and _equal_state(dps, ref, rank)
 
 
 def _flag_timeout_on(calls: set, monkeypatch):
