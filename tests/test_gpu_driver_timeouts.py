@@ -10,6 +10,10 @@ behind a sleeping kernel on another stream) or are reported by a wrapper
 that sets the flag bit after the real kernels: no GPU is faulted or hung.
 """
 import dataclasses
+import os
+import subprocess
+import sys
+import textwrap
 
 import pytest
 import torch
@@ -139,3 +143,36 @@ def test_step_kernel_wait_expiry_in_the_pipelined_driver(monkeypatch):
     assert all(torch.equal(a.view(torch.int32), b.view(torch.int32))
                for a, b in zip(dps.state[rank].tensors(), ref.state[rank].tensors()))
     assert int(dps.flags.abs().sum().item()) == 0
+
+
+def test_first_host_fed_step_of_a_process_completes():
+    """The first bucket-ready step of a fresh process, whose kernels are not
+    loaded yet (CUDA's lazy loading), lands within its wait limit: the
+    library loads every kernel it will launch before the first wait starts,
+    so loading cannot wait for that wait while the copies it needs are not
+    yet issued."""
+    tests = os.path.dirname(os.path.abspath(__file__))
+    script = textwrap.dedent(f"""
+        import dataclasses, sys, time
+        sys.path[:0] = [{os.path.dirname(tests)!r}, {tests!r}]
+        import torch
+        import synth
+        from gpu_util import make_group, shard_rows
+        w = dataclasses.replace(synth.WORKLOADS["c1"], psi=200_003, nd=8, plant=None)
+        dps = make_group(w, ranks=[1], gathered="full")
+        rows, desc = shard_rows(w, dps, 1, 0)
+        host = rows.cpu().pin_memory()
+        rows.zero_()
+        copy = torch.cuda.Stream()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dps.launch_host_fed(1, host, desc[1], 4096, copy, timeout_ns=3_000_000_000)
+        assert not dps.decide()
+        print("elapsed", time.perf_counter() - t0)
+    """)
+    env = dict(os.environ, CUDA_MODULE_LOADING="LAZY")
+    out = subprocess.run([sys.executable, "-c", script], capture_output=True, text=True,
+                         timeout=300, env=env)
+    assert out.returncode == 0, out.stderr[-3000:]
+    elapsed = float(out.stdout.split("elapsed")[-1])
+    assert elapsed < 2.0, elapsed

@@ -57,6 +57,15 @@ zero_status_t resolve_ptr(const void* p, void** out, bool* on_host = nullptr);
 // rows are in host memory.
 zero_status_t resolve_grads(const zero_grads_t* g, zero_grads_t* out, bool* in_host = nullptr);
 
+// Loads now, once per device, every instance of the fused-step kernel that
+// launch_fused_bucket can launch for `dtype` and rows where host_rows says.
+// Under CUDA's lazy loading a kernel is otherwise loaded at its first
+// launch, and loading can wait for kernels already running: if one of those
+// is a bucket wait whose words are written only by copies the caller issues
+// after this call returns, the two would wait on each other until the wait's
+// time limit.
+void preload_fused(int dtype, bool host_rows);
+
 // Launches the fused step over elements [b0, b0 + len) of a shard -- one
 // bucket -- as the fewest equal launch windows of at most
 // ZERO_FUSED_WINDOW_ELEMS elements.  rows: the rows at shard element 0, at

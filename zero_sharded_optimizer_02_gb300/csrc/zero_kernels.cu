@@ -700,11 +700,26 @@ void launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaSt
     }
 }
 
+// The shared-memory opt-in of one ring / bulk-copy kernel instance (once
+// per device).
 template <int DT, int W, bool V8, int MODE>
-void launch_ring(unsigned grid, const FusedArgs& a, cudaStream_t s)
+void ring_opt_in()
 {
     static std::atomic<uint64_t> opted{0};
     smem_opt_in(k_step_fused_ring<DT, W, V8, MODE>, kRingBytes, opted);
+}
+
+template <int DT, int W, bool V8>
+void tma_opt_in()
+{
+    static std::atomic<uint64_t> opted{0};
+    smem_opt_in(k_step_fused_tma<DT, W, V8>, kTmaBytes, opted);
+}
+
+template <int DT, int W, bool V8, int MODE>
+void launch_ring(unsigned grid, const FusedArgs& a, cudaStream_t s)
+{
+    ring_opt_in<DT, W, V8, MODE>();
     launch_k(k_step_fused_ring<DT, W, V8, MODE>, dim3(grid), dim3(kRingThreads), kRingBytes, s,
              a);
 }
@@ -714,8 +729,7 @@ void launch_fused_w(const FusedArgs& a, int variant, cudaStream_t s)
 {
     const uint64_t work = a.sp.nvec > a.sp.nscalar() ? a.sp.nvec : a.sp.nscalar();
     if (variant == 2) {
-        static std::atomic<uint64_t> opted{0};
-        smem_opt_in(k_step_fused_tma<DT, W, V8>, kTmaBytes, opted);
+        tma_opt_in<DT, W, V8>();
         const uint64_t tiles = (a.sp.nvec + kTmaConsumers - 1) / kTmaConsumers;
         const uint64_t cap = (uint64_t)sm_count();
         const unsigned grid = (unsigned)(tiles < cap ? (tiles ? tiles : 1) : cap);
@@ -890,6 +904,61 @@ zero_status_t check_step_args(const zero_grads_t* g, const zero_layout_t* L,
     if (n && spans_overlap(slot, 2 * n, rows, 2 * row_span))
         return ZERO_ERR_INVALID_ARG;
     return ZERO_OK;
+}
+
+namespace {
+
+// Loads one fused-step kernel instance of `variant` now (asking CUDA for its
+// attributes loads a lazily loaded kernel) and makes its shared-memory
+// opt-in, so that launching it later calls nothing that could wait.
+template <int DT, int W, bool V8>
+void load_fused_w(int variant)
+{
+    cudaFuncAttributes fa;
+    if (variant == 2) {
+        (void)cudaFuncGetAttributes(&fa, k_step_fused_tma<DT, W, V8>);
+        tma_opt_in<DT, W, V8>();
+    } else if (variant == 1) {
+        (void)cudaFuncGetAttributes(&fa, k_step_fused_ring<DT, W, V8, kModeStep>);
+        ring_opt_in<DT, W, V8, kModeStep>();
+    } else {
+        (void)cudaFuncGetAttributes(&fa, k_step_fused<DT, W, V8>);
+    }
+}
+
+template <int DT>
+void load_fused_dt(int variant)
+{
+    load_fused_w<DT, 16, true>(variant);
+    load_fused_w<DT, 8, true>(variant);
+    load_fused_w<DT, 4, true>(variant);
+    load_fused_w<DT, 2, true>(variant);
+    load_fused_w<DT, 16, false>(variant);
+    load_fused_w<DT, 8, false>(variant);
+    load_fused_w<DT, 4, false>(variant);
+    load_fused_w<DT, 2, false>(variant);
+}
+
+}  // namespace
+
+void preload_fused(int dtype, bool host_rows)
+{
+    const int variant = fused_variant(host_rows);
+    static std::atomic<uint64_t> done[2][3];   // per dtype and variant: a bit per device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        dev = 64;
+    const uint64_t bit = dev < 64 ? 1ull << dev : 0;
+    std::atomic<uint64_t>& d = done[dtype == ZERO_F16 ? 0 : 1][variant];
+    if (bit && (d.load(std::memory_order_relaxed) & bit))
+        return;
+    if (dtype == ZERO_F16)
+        load_fused_dt<ZERO_F16>(variant);
+    else
+        load_fused_dt<ZERO_BF16>(variant);
+    (void)cudaGetLastError();
+    if (bit)
+        d.fetch_or(bit, std::memory_order_relaxed);
 }
 
 zero_status_t launch_fused_bucket(const uint16_t* rows, const zero_grads_t* g,

@@ -110,6 +110,8 @@ extern "C" zero_status_t zero_step_shard_streamed(
     rs = resolve_ptr(gathered, &gdev);
     if (rs != ZERO_OK)
         return rs;
+    // every kernel this call launches is loaded before its first wait starts
+    preload_fused(g->dtype, host_rows);
     const StepScalars k = make_scalars(h, g->nd, loss_scale);
     const uint16_t* rows = static_cast<const uint16_t*>(gr.base) + g->offset;
     uint16_t* gath = static_cast<uint16_t*>(gdev) + gathered_offset_elems;
