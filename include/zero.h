@@ -282,7 +282,9 @@ zero_status_t zero_check_nonfinite(const zero_grads_t* g, uint64_t begin, uint64
  * writes d_ready[b] after the bucket's contributions are in place -- e.g. a
  * cudaMemcpyAsync of the word on the copy stream that copied the data.  The
  * ready words must be written by a copy engine or the host, never by a kernel
- * that would have to run concurrently with this one.
+ * that would have to run concurrently with this one.  The call loads every
+ * kernel it launches before its first wait starts, so that under lazy module
+ * loading none of its own launches waits for that wait.
  * Each wait is bounded by timeout_ns of GPU time (%globaltimer) and an
  * iteration cap; on expiry the kernel stores ZERO_ERR_TIMEOUT into *d_status
  * (if it is still 0), touches no element of a bucket that was not seen ready,
