@@ -204,10 +204,12 @@ class DataParallelStep:
     def decide(self) -> bool:
         """Read the nonfinite flag (OR-ed over the process group if any).
 
-        After a host-fed step whose bucket wait expired, raises ZeroError
-        (ZERO_ERR_TIMEOUT) instead: that step is neither committed nor
-        skipped, the committed state is untouched, and the status and flag
-        words are cleared so the next step can run."""
+        If a device wait of the step expired (a host-fed step's bucket wait,
+        or a step kernel's pipeline wait), every rank still takes part in the
+        decision, where it counts as a skip, and then this rank raises
+        ZeroError (ZERO_ERR_TIMEOUT): the step is not committed, the committed
+        state is untouched, and the flag and status words are cleared so the
+        next step can run."""
         with torch.cuda.stream(self.stream):
             self.flag_host.copy_(self.flag, non_blocking=True)
         self.stream.synchronize()
