@@ -79,6 +79,25 @@ def test_gpu_arm_line():
     assert set(d["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
 
 
+def test_reference_arm_under_torchrun_prints_one_line():
+    """With two processes (as the driver launches N > 1) rank 0 alone runs
+    the reference arm and prints its line; the other rank exits 0."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--config",
+           "c0", "--steps", "1", "--warmup", "3", "--ref-sample", "256"]
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-3000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, out.stdout[-3000:]
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+
+
 @pytest.mark.gpu
 def test_gpu_arm_two_processes():
     """The N > 1 choreography of the benchmark (barriers, max over ranks, one
