@@ -55,7 +55,7 @@ typedef enum zero_status {
     ZERO_ERR_INVALID_ARG = 1,  /* NULL pointer, bad size, overflow, bad enum, overlap */
     ZERO_ERR_ALIGNMENT = 2,    /* a pointer or stride breaks the documented alignment */
     ZERO_ERR_CUDA = 3,         /* the CUDA runtime reported an error */
-    ZERO_ERR_TIMEOUT = 4,      /* a bounded wait expired (reserved) */
+    ZERO_ERR_TIMEOUT = 4,      /* a bounded device wait expired (bucket-ready step) */
     ZERO_ERR_UNSUPPORTED = 5,  /* valid request this build does not implement */
     ZERO_ERR_IO = 6            /* a checkpoint file is missing, unreadable, torn or corrupt */
 } zero_status_t;
@@ -176,12 +176,13 @@ zero_status_t zero_gather_params_shard(const float* master, uint64_t n, void* ga
  * contribution rows are folded.  g->nd is normally L->nd (Stage 2: one
  * contribution per rank) but need not be: under Stage 1 every rank holds the
  * gradient already all-reduced, so it folds a single row (g->nd = 1) and
- * passes loss_scale * Nd to keep the 1/Nd averaging.  The shard is walked in
- * buckets of bucket_elems elements; each bucket runs as the fewest equal
- * launches of at most ZERO_FUSED_WINDOW_ELEMS elements (kernel boundaries keep
- * every SM at the same place in the rows; single launches much longer than
- * this read several percent more DRAM than the data).  Results depend on
- * neither size.
+ * passes loss_scale * Nd to keep the 1/Nd averaging.  The reduced sums stay
+ * in registers, so no bucket is ever materialised and the bucket is no
+ * boundary of the work: bucket_elems (>= 1) is validated but the whole shard
+ * runs as the fewest equal launches of at most ZERO_FUSED_WINDOW_ELEMS
+ * elements (kernel boundaries keep every SM at the same place in the rows;
+ * single launches much longer than this read several percent more DRAM than
+ * the data).  Results depend on neither size.
  * The kernel is the cp.async-ring variant unless the environment variable
  * ZERO_FUSED_VARIANT, read at each call, names another ("registers", "ring"
  * or "tma": bulk copies and mbarriers); rows in host memory always use the
@@ -241,8 +242,11 @@ zero_status_t zero_step_shard_unfused(const zero_grads_t* g, const zero_layout_t
  * floats.  The caller still provides every input and output.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *   - The first call on a device looks up that device's address of the array
- *     (cudaGetSymbolAddress, with the device current) and caches it; make
- *     that first call before any stream capture.
+ *     (cudaGetSymbolAddress, with the device current) and caches it with the
+ *     id of the device's CUDA context.  A later call in another context of
+ *     the device (after cudaDeviceReset, the array is loaded anew and may
+ *     move) looks it up again.  Make the first call on a device, and the
+ *     first after its context is re-created, before any stream capture.
  *   - ZERO_ERR_INVALID_ARG, with nothing launched, if
  *     min(bucket_elems, L->length) > ZERO_STATIC_CB_MAX_BUCKET; the other
  *     validation is that of zero_step_shard_unfused.

@@ -263,7 +263,11 @@ def test_binding_constants_match_header(z):
     assert e.value.status == z.ZERO_ERR_TIMEOUT
     assert z._abi.fused_launch_count(117_187_500, 500_000_000) == 5
     assert z._abi.fused_launch_count(23_437_500, 50_000_000) == 1
-    assert z._abi.fused_launch_count(16, 1) == 16 and z._abi.fused_launch_count(0, 8) == 0
+    # the fused step plans its windows over the whole shard: the bucket size
+    # does not add launches (the 4-rank workload's 4 buckets are one launch)
+    assert z._abi.fused_launch_count(16, 1) == 1 and z._abi.fused_launch_count(0, 8) == 0
+    assert z._abi.fused_launch_count(262_144, 65_536) == 1
+    assert z._abi.fused_launch_count(117_187_500, 7) == 5
     # unfused: the reduction in the same windows, plus AdamW and cast, per bucket
     assert z._abi.unfused_launch_count(117_187_500, 500_000_000) == 5 + 2
     assert z._abi.unfused_launch_count(262_144, 65_536) == 4 * 3
@@ -288,20 +292,9 @@ def test_binding_constants_match_header(z):
 
 
 def _window_cuts(length: int, phase: int):
-    """The launch windows of one bucket, restated from zero.h's description:
-    the fewest equal windows of at most ZERO_FUSED_WINDOW_ELEMS elements,
-    cut on 8-element row boundaries, a remainder under 64 joining the last."""
-    W = z_abi().ZERO_FUSED_WINDOW_ELEMS
-    nwin = -(-length // W)
-    target = -(-(-(-length // nwin)) // 8) * 8
-    cuts, w0, cut = [], 0, target - (phase & 7)
-    while w0 < length:
-        w1 = min(cut, length)
-        if length - w1 < 64:
-            w1 = length
-        cuts.append((w0, w1))
-        w0, cut = w1, cut + target
-    return cuts
+    from window_rule import window_cuts
+    assert z_abi().ZERO_FUSED_WINDOW_ELEMS == 25165824
+    return window_cuts(length, phase)
 
 
 def z_abi():

@@ -107,8 +107,12 @@ def _windows(length: int, phase: int) -> int:
 
 def fused_launch_count(n: int, bucket: int, offset: int = 0) -> int:
     """Kernel launches zero_step_shard issues for a shard of n elements whose
-    rows start at element `offset` (the same window split as the library)."""
-    return sum(_windows(min(bucket, n - b0), offset + b0) for b0 in range(0, n, bucket))
+    rows start at element `offset`: the launch windows of the whole shard
+    (the same split as the library).  The bucket size does not change them:
+    the fused kernel never materialises a bucket."""
+    if bucket <= 0:
+        raise ValueError("bucket must be positive")
+    return _windows(n, offset) if n > 0 else 0
 
 
 # Least step traffic of a launch group of zero_step_shard_streamed (zero.h).

@@ -58,7 +58,7 @@ zero_status_t resolve_ptr(const void* p, void** out, bool* on_host = nullptr);
 zero_status_t resolve_grads(const zero_grads_t* g, zero_grads_t* out, bool* in_host = nullptr);
 
 // Loads now, once per device, every instance of the fused-step kernel that
-// launch_fused_bucket can launch for `dtype` and rows where host_rows says.
+// launch_fused_range can launch for `dtype` and rows where host_rows says.
 // Under CUDA's lazy loading a kernel is otherwise loaded at its first
 // launch, and loading can wait for kernels already running: if one of those
 // is a bucket wait whose words are written only by copies the caller issues
@@ -66,14 +66,14 @@ zero_status_t resolve_grads(const zero_grads_t* g, zero_grads_t* out, bool* in_h
 // time limit.
 void preload_fused(int dtype, bool host_rows);
 
-// Launches the fused step over elements [b0, b0 + len) of a shard -- one
-// bucket -- as the fewest equal launch windows of at most
-// ZERO_FUSED_WINDOW_ELEMS elements.  rows: the rows at shard element 0, at
+// Launches the fused step over elements [b0, b0 + len) of a shard (the
+// whole shard, or one launch group of buckets) as the fewest equal launch
+// windows of at most ZERO_FUSED_WINDOW_ELEMS elements.  rows: the rows at shard element 0, at
 // the address the device reads them (resolve_grads); gath: the gathered slot
 // of shard element 0.  The variant follows ZERO_FUSED_VARIANT (the register
 // kernel for host_rows).  gate: if non-null, every launch reads it first and
 // does nothing if it is nonzero.  Returns ZERO_ERR_CUDA if a launch failed.
-zero_status_t launch_fused_bucket(const uint16_t* rows, const zero_grads_t* g,
+zero_status_t launch_fused_range(const uint16_t* rows, const zero_grads_t* g,
                                   const zero_state_t* in, const zero_state_t* out,
                                   uint16_t* gath, uint64_t b0, uint64_t len,
                                   const StepScalars& k, bool host_rows, uint32_t* d_nonfinite,

@@ -23,12 +23,14 @@
 // intrinsic (__fadd_rn/__fmul_rn/__fdiv_rn/__fsqrt_rn), so no multiply-add is
 // contracted, and the reduction is a per-element sequential fold over ranks
 // 0..Nd-1.  Warp votes are used only for the nonfinite flag.
+#include <cuda.h>   // CUcontext and CUresult for two driver queries found at run time
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 
 #include <atomic>
+#include <mutex>
 #include <utility>
 
 #include "zero_device.cuh"
@@ -100,7 +102,7 @@ constexpr int kCtasPerSmLight = 8;
 #define ZERO_FUSED_IMPL 1
 #endif
 // Longest launch window of the fused step (elements, a multiple of 8; a
-// window can exceed it by under 64 elements when a bucket's remainder joins it).
+// window can exceed it by under 64 elements when a range's remainder joins it).
 #ifndef ZERO_WINDOW_ELEMS
 #define ZERO_WINDOW_ELEMS ZERO_FUSED_WINDOW_ELEMS
 #endif
@@ -961,7 +963,7 @@ void preload_fused(int dtype, bool host_rows)
         d.fetch_or(bit, std::memory_order_relaxed);
 }
 
-zero_status_t launch_fused_bucket(const uint16_t* rows, const zero_grads_t* g,
+zero_status_t launch_fused_range(const uint16_t* rows, const zero_grads_t* g,
                                   const zero_state_t* in, const zero_state_t* out,
                                   uint16_t* gath, uint64_t b0, uint64_t len,
                                   const StepScalars& k, bool host_rows, uint32_t* d_nonfinite,
@@ -1120,16 +1122,12 @@ extern "C" zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layou
     const StepScalars k = make_scalars(h, g->nd, loss_scale);
     const uint16_t* rows = static_cast<const uint16_t*>(gr.base) + g->offset;
     uint16_t* gath = static_cast<uint16_t*>(gdev) + gathered_offset_elems;
-    for (uint64_t b0 = 0; b0 < n; b0 += bucket_elems) {
-        const uint64_t len = n - b0 < bucket_elems ? n - b0 : bucket_elems;
-        st = launch_fused_bucket(rows, g, in, out, gath, b0, len, k, host_rows, d_nonfinite,
-                                 nullptr, stream);
-        if (st != ZERO_OK)
-            return st;
-        if (len < bucket_elems)
-            break;
-    }
-    return ZERO_OK;
+    // The fused kernel keeps each reduced sum in registers, so a bucket is
+    // never materialised and is no boundary of its work: the launch windows
+    // are planned over the whole shard (one launch for shards of up to
+    // kWindow elements, whatever the bucket size).
+    return launch_fused_range(rows, g, in, out, gath, 0, n, k, host_rows, d_nonfinite, nullptr,
+                               stream);
 }
 
 extern "C" zero_status_t zero_step_shard_unfused(const zero_grads_t* g, const zero_layout_t* L,
@@ -1208,11 +1206,50 @@ namespace {
 // symbol; kernels get the device address from cudaGetSymbolAddress.
 __device__ __align__(256) float g_static_cb[ZERO_STATIC_CB_ELEMS];
 
-constexpr int kMaxDevices = 128;
-std::atomic<float*> g_static_cb_addr[kMaxDevices];   // per device, null until looked up
+// The id of the calling thread's current CUDA context (unique for the life of
+// the process, never reused), or 0 if there is none or the driver cannot say.
+// The two driver calls are found through the runtime, so the library still
+// links no driver library; they only read the thread's context.
+unsigned long long current_context_id()
+{
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag found;
+    std::call_once(found, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(f);
+        (void)cudaGetLastError();
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
-// Device address of g_static_cb on the current device, looked up once per
-// device (with that device current) and cached.
+constexpr int kMaxDevices = 128;
+struct StaticCbEntry {
+    unsigned long long ctx_id;   // context the address was looked up in (0: none yet)
+    float* addr;
+};
+StaticCbEntry g_static_cb_addr[kMaxDevices];
+std::mutex g_static_cb_mutex;
+
+// Device address of g_static_cb on the current device.  It is looked up with
+// cudaGetSymbolAddress (the device current) on the first call on a device and
+// again whenever the device's context is not the one the address was found
+// in (after cudaDeviceReset the library's device memory is loaded anew and
+// the array may move); otherwise the cached address is returned.
 zero_status_t static_cb_address(float** out)
 {
     int dev = 0;
@@ -1220,15 +1257,19 @@ zero_status_t static_cb_address(float** out)
         return ZERO_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices)
         return ZERO_ERR_UNSUPPORTED;
-    float* p = g_static_cb_addr[dev].load(std::memory_order_acquire);
-    if (p == nullptr) {
+    std::lock_guard<std::mutex> lock(g_static_cb_mutex);
+    StaticCbEntry& e = g_static_cb_addr[dev];
+    const unsigned long long id = current_context_id();
+    if (id == 0 || e.addr == nullptr || e.ctx_id != id) {
         void* a = nullptr;
-        if (cudaGetSymbolAddress(&a, g_static_cb) != cudaSuccess || a == nullptr)
+        if (cudaGetSymbolAddress(&a, g_static_cb) != cudaSuccess || a == nullptr) {
+            (void)cudaGetLastError();
             return ZERO_ERR_CUDA;
-        p = static_cast<float*>(a);
-        g_static_cb_addr[dev].store(p, std::memory_order_release);
+        }
+        e.addr = static_cast<float*>(a);
+        e.ctx_id = current_context_id();   // the lookup made the context current if it was not
     }
-    *out = p;
+    *out = e.addr;
     return ZERO_OK;
 }
 

@@ -141,7 +141,7 @@ extern "C" zero_status_t zero_step_shard_streamed(
                                       d_status);
         if (cudaGetLastError() != cudaSuccess)
             return ZERO_ERR_CUDA;
-        const zero_status_t ls = launch_fused_bucket(rows, g, in, out, gath, g0, glen, k,
+        const zero_status_t ls = launch_fused_range(rows, g, in, out, gath, g0, glen, k,
                                                      host_rows, d_nonfinite, d_status, stream);
         if (ls != ZERO_OK)
             return ls;
