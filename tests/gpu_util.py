@@ -16,6 +16,7 @@ import oracle
 import synth
 import zero_sharded_optimizer_02_gb300 as z
 from zero_sharded_optimizer_02_gb300.step import DataParallelStep
+from window_rule import inner_cuts
 
 DEV = "cuda"
 DT_CODE = {"f16": oracle.F16, "bf16": oracle.BF16}
@@ -123,9 +124,26 @@ def oracle_trajectory(w, idx: np.ndarray, steps: int, psi=None, nd=None):
     return tr, history
 
 
+def oracle_shard_step(w, rank: int, step: int = 0):
+    """The oracle's step t = 1 of one rank's whole shard from the workload's
+    initial state, on the contributions of generator step ``step``:
+    (flag, master, m, v, params), params being the cast into the rank's slot."""
+    s, b, n = synth.shard_of(w.psi, w.nd, rank)
+    I = torch.arange(b, b + n, dtype=torch.int64)
+    p0, m0, v0 = (synth.state_values(w, k, I).numpy() for k in ("master", "m", "v"))
+    rows = np.stack([u16(synth.grad_values(w, step, j, I)) for j in range(w.nd)])
+    params = np.zeros(max(n, 1), np.uint16)
+    f, p, m, v = oracle.step_rank(rows, n, 0, n, w.nd, DT_CODE[w.grad_dtype], w.bucket,
+                                  w.loss_scale, w.hparams, 1, p0, m0, v0, params, 0)
+    return f, p, m, v, params[:n]
+
+
 def sample_indices(psi: int, nd: int, ranks, per_rank: int, seed: int, extra=()):
     """Flat indices: each rank's first/last elements, neighbours of every
-    8-element boundary near the ends, random interior points, and ``extra``."""
+    8-element boundary near the ends, the 16 elements on each side of every
+    cut between two launch windows of the fused step (shards longer than one
+    window; the rows of every test start on a 16-byte boundary), random
+    interior points, and ``extra``."""
     rng = np.random.default_rng(seed)
     s = -(-psi // nd)
     out = set(int(e) for e in extra)
@@ -137,6 +155,8 @@ def sample_indices(psi: int, nd: int, ranks, per_rank: int, seed: int, extra=())
         for d in range(min(n, 17)):
             out.add(b + d)
             out.add(b + n - 1 - d)
+        for c in inner_cuts(n, 0):
+            out.update(b + c + d for d in range(-16, 16) if 0 <= c + d < n)
         out.update(int(x) for x in b + rng.integers(0, n, per_rank))
     return np.array(sorted(out), np.int64)
 

@@ -3,6 +3,9 @@ times, checked against the oracle on sampled elements (the oracle computes
 any element on its own from the seeded generator) and through properties that
 hold at any size (padding untouched, skip decisions, step count).
 
+Samples include the 16 elements on each side of every cut between two launch
+windows of the fused step (the 7.5B shard runs as 5 windows).
+
 Workloads: GPT-2-small-sized ZeRO-2 shard (psi = 124,439,808, Nd = 8, bf16,
 10 steps); padding and overflow (psi = 350,000,017, Nd = 16, fp16 x 1024,
 all 16 ranks, +inf planted at step 5); GPT-2 1.5B shard view (Nd = 64, fp16,
@@ -20,6 +23,7 @@ import synth
 import zero_sharded_optimizer_02_gb300 as z
 from gpu_util import (assert_params_close, assert_state_close, f32, full_rows, make_group,
                       oracle_trajectory, sample_indices, shard_rows, u16)
+from window_rule import inner_cuts
 
 pytestmark = pytest.mark.gpu
 
@@ -91,6 +95,11 @@ def test_shard_view_sampled(key, rank, bench_cfg):
     w = synth.WORKLOADS[key]
     dps = _bench_driver(w, rank) if bench_cfg else make_group(w, ranks=[rank])
     idx = sample_indices(w.psi, w.nd, [rank], 2048, seed=rank + 17)
+    # every cut between two launch windows of the step is sampled on both sides
+    s, b, n = synth.shard_of(w.psi, w.nd, rank)
+    cuts = inner_cuts(n)
+    assert len(cuts) == z.fused_launch_count(n, w.bucket) - 1
+    assert all(np.isin(b + c + np.arange(-16, 16), idx).all() for c in cuts)
     _, hist = oracle_trajectory(w, idx, w.steps)
     buf = None
     for k in range(w.steps):
