@@ -132,6 +132,100 @@ def workload(args):
     return w
 
 
+def bench_config(args, w, dp_rank: int, world: int) -> dict:
+    """The workload description both arms print (host arithmetic only): the
+    shard this process runs, its row layout and where its parameters go."""
+    import synth
+    s, begin, n = synth.shard_of(w.psi, w.nd, dp_rank)
+    pitch = synth.pitch_of(s)
+    step_bytes = w.bytes_per_param * n
+    overridden = bool(args.psi or args.nd or args.grad_dtype or args.bucket)
+    return {"workload": f"{args.config}: {w.title}" + (" (overridden)" if overridden else ""),
+            "psi": w.psi, "nd": w.nd,
+            "rank": dp_rank, "shard_params": n, "grad_dtype": w.grad_dtype,
+            "bucket": w.bucket, "loss_scale": w.loss_scale,
+            "row_stride_elems": pitch + args.row_pad,
+            "gathered": args.gathered + (
+                f" (slot at element {begin}, 16-byte phase {(begin * 2) % 16} B)"
+                if args.gathered == "full" else " (the rank's own S-element buffer)"),
+            "l2": (f"inputs larger than L2 ({step_bytes / 1e9:.1f} GB per step), no flush"
+                   if step_bytes > L2_BYTES else
+                   f"inputs L2-resident ({step_bytes / 1e6:.1f} MB per step, L2 129 MB), no "
+                   "flush: a latency figure, not a bandwidth one"),
+            "parallelism": f"zero-dp{w.nd} emulated, {world} process(es)"}
+
+
+def time_back_to_back(torch, stream, dev, call, reps: int) -> float:
+    """Milliseconds per call of `reps` back-to-back calls, CUDA events on
+    `stream` (synchronised on both sides)."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / reps
+
+
+# The other workloads the default line also times (kernel time only): the
+# 1.5B shard is the second target workload; its odd rank writes its
+# parameters into its slot of the flat buffer, 8 bytes off a 16-byte line.
+PER_CONFIG = [("c0", 0, "slot"), ("c1", 0, "slot"), ("c2", 0, "slot"), ("c3", 0, "slot"),
+              ("c3", 1, "full")]
+
+
+def measure_config(key: str, rank: int, gathered: str, dev, stream, peak: float,
+                   reps: int = 100) -> dict:
+    """The fused step of one more workload's shard (shard-view rows resident
+    in HBM), timed like the headline's kernel figure: `reps` back-to-back
+    steps, each step's output feeding the next, CUDA events on the launching
+    stream.  Checks that no step was skipped."""
+    import torch
+
+    import synth
+    from zero_sharded_optimizer_02_gb300 import _abi
+    from zero_sharded_optimizer_02_gb300.step import DataParallelStep
+    w = synth.WORKLOADS[key]
+    with torch.cuda.stream(stream):
+        dps = DataParallelStep(w.psi, w.nd, [rank], w.grad_dtype, w.hparams, w.loss_scale,
+                               w.bucket, dev, gathered=gathered, fused=True, stream=stream)
+        L = dps.layouts[rank]
+        n, pitch = int(L.length), int(L.row_pitch)
+        st = dps.state[rank]
+        for row, which in zip(st.bufs[st.cur], ("master", "m", "v")):
+            synth.fill_shard_state(w, rank, which, row)
+        grads = torch.empty(w.nd, pitch, dtype=w.torch_grad_dtype, device=dev)
+        synth.fill_shard_rows(w, 0, rank, grads)
+    desc = {rank: _abi.grads(grads, pitch, 0, w.nd, w.grad_dtype)}
+
+    def call():
+        dps.launch(desc)
+        dps.commit(False)
+    for _ in range(3):
+        call()
+    ms = time_back_to_back(torch, stream, dev, call, reps)
+    torch.cuda.synchronize(dev)
+    skipped = int(dps.flag.item()) != 0
+    launches = _abi.fused_launch_count(n, w.bucket, 0)
+    step_bytes = w.bytes_per_param * n
+    gbs = step_bytes / (ms * 1e-3) / 1e9
+    out = {"workload": f"{key}: {w.title}", "rank": rank, "nd": w.nd, "shard_params": n,
+           "grad_dtype": w.grad_dtype,
+           "gathered": gathered + (f" (slot at element {int(L.begin)}, 16-byte phase "
+                                   f"{(int(L.begin) * 2) % 16} B)" if gathered == "full" else ""),
+           "kernel": kernel_name(), "kernel_ms_per_step": ms, "launches_per_step": launches,
+           "kernel_ms": ms / launches, "algorithmic_bytes_per_param": w.bytes_per_param,
+           "achieved": gbs, "frac": gbs / peak, "params_per_s": n / (ms * 1e-3),
+           "steps_timed_back_to_back": reps, "skipped": skipped}
+    if step_bytes <= L2_BYTES:
+        out["l2"] = (f"L2-resident ({step_bytes / 1e6:.1f} MB per step): a latency figure, not "
+                     "a bandwidth one")
+    del dps, grads
+    torch.cuda.empty_cache()
+    return out
+
+
 def smi_index(local: int) -> str:
     """nvidia-smi's id of this process's device (honours CUDA_VISIBLE_DEVICES)."""
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
@@ -319,6 +413,17 @@ def run_gpu(args) -> None:
     k1.record(stream)
     torch.cuda.synchronize(dev)
     back_to_back_ms = k0.elapsed_time(k1) / nk
+    # -- a read-only stream over the same rows: the nonfinite pre-check reads
+    #    the Nd contribution rows (2 Nd B/param) and writes nothing, in the
+    #    same launch windows.  The step is 2 Nd + 12 B read to 14 B written
+    #    a parameter; a pure read is the best stream HBM gives that mix, so
+    #    the step's fraction of it shows how much is left. --------------------
+    def read_pass():
+        _abi.zero_check_nonfinite(desc[dp_rank], 0, n, dps.flag, stream)
+    for _ in range(3):
+        read_pass()
+    read_ms = time_back_to_back(torch, stream, dev, read_pass, nk)
+    read_gbs = 2 * w.nd * n / (read_ms * 1e-3) / 1e9
     with torch.cuda.stream(stream):
         dps.flag.zero_()
     time.sleep(0.2 if sampler else 0.0)
@@ -481,13 +586,23 @@ def run_gpu(args) -> None:
                                        "reads of host memory in this run: not a bound")
             del host_grads, host_params, dps_h
 
+    # -- the other workloads' fused step (kernel time), rank 0 at N = 1 only --
+    peaks = measured_peaks()
+    per_config = None
+    if world == 1 and not args.no_per_config and not (args.psi or args.nd or args.grad_dtype or
+                                                       args.bucket or args.row_pad):
+        pk = peaks.get("hbm_gbs") or 6800.0
+        per_config = {f"{k} rank {r}" + (" (flat buffer slot)" if g == "full" else ""):
+                      measure_config(k, r, g, dev, stream, pk)
+                      for k, r, g in PER_CONFIG if (k, r, g) != (args.config, dp_rank,
+                                                                   args.gathered)}
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
     # -- report -----------------------------------------------------------------
-    peaks = measured_peaks()
     ms_per_step = total_ms / args.steps
     bytes_per_param = w.bytes_per_param
     kern_step_ms = statistics.fmean(kernel_ms)
@@ -515,22 +630,7 @@ def run_gpu(args) -> None:
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded counter-based generator; no dataset or weights)",
-        "config": {"workload": f"{args.config}: {w.title}" + (
-                       " (overridden)" if (args.psi or args.nd or args.grad_dtype or args.bucket)
-                       else ""),
-                   "psi": w.psi, "nd": w.nd,
-                   "rank": dp_rank, "shard_params": n, "grad_dtype": w.grad_dtype,
-                   "bucket": w.bucket, "loss_scale": w.loss_scale,
-                   "row_stride_elems": row_stride,
-                   "gathered": args.gathered + (
-                       f" (slot at element {int(L.begin)}, 16-byte phase "
-                       f"{(int(L.begin) * 2) % 16} B)" if args.gathered == "full" else
-                       " (the rank's own S-element buffer)"),
-                   "l2": (f"inputs larger than L2 ({bytes_per_param * n / 1e9:.1f} GB per step),"
-                          " no flush" if bytes_per_param * n > L2_BYTES else
-                          f"inputs L2-resident ({bytes_per_param * n / 1e6:.1f} MB per step, "
-                          "L2 129 MB), no flush: a latency figure, not a bandwidth one"),
-                   "parallelism": f"zero-dp{w.nd} emulated, {world} process(es)"},
+        "config": bench_config(args, w, dp_rank, world),
         "gbs": bytes_per_param * n / (ms_per_step * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src,
@@ -543,7 +643,13 @@ def run_gpu(args) -> None:
                      "kernel_ms_in_sync_step_median": statistics.median(kernel_ms),
                      "kernel_ms_in_sync_step_min": min(kernel_ms),
                      "steps_timed_back_to_back": nk,
-                     "algorithmic_bytes_per_launch": launch_bytes},
+                     "algorithmic_bytes_per_launch": launch_bytes,
+                     "read_ceiling_gbs": read_gbs,
+                     "frac_of_read_ceiling": achieved / read_gbs,
+                     "read_ceiling": "zero_check_nonfinite over the same Nd rows (reads "
+                                     "2 Nd B/param, writes nothing), same launch windows, "
+                                     f"{nk} back-to-back passes"},
+        "per_config": per_config,
         "e2e": e2e,
         "gpu_launches": launches,
         "driver": f"pipelined (up to {pipe.depth} steps launched ahead of the oldest "
@@ -685,8 +791,8 @@ def run_reference(args) -> None:
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded counter-based generator)",
-        "config": {"workload": f"{args.config}: {w.title}", "psi": w.psi, "nd": w.nd,
-                   "rank": args.rank, "sample_params_per_step": params // args.steps},
+        "config": bench_config(args, w, args.rank, world),
+        "sample_params_per_step": params // args.steps,
         "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample, "per_core_value": rate / cores,
                          "cpu_model": cpu_model()},
@@ -925,6 +1031,8 @@ def main():
                     help="transfer buckets of the host-fed e2e step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other workloads' kernel timings of the default line")
     ap.add_argument("--ref-sample", type=int, default=1 << 13,
                     help="params per core per step of the reference (oracle) arm")
     args = ap.parse_args()

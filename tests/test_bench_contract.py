@@ -40,11 +40,32 @@ def test_reference_arm_line():
     assert (d["steps"], d["warmup"], d["n_gpus"]) == (2, 3, 1)
     assert d["vs_baseline"] is None
     assert d["config"]["workload"].startswith("c0")
-    assert d["config"]["sample_params_per_step"] == 2 * 512
+    assert d["sample_params_per_step"] == 2 * 512
+    # the same config keys and values as the GPU arm prints for this workload
+    assert d["config"] == _gpu_arm_config("c0", 0)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] == 2 and cb["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def _gpu_arm_config(key: str, rank: int, world: int = 1) -> dict:
+    import argparse
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    args = argparse.Namespace(config=key, psi=0, nd=0, grad_dtype=None, bucket=0, row_pad=0,
+                              gathered="slot")
+    return bench.bench_config(args, synth.WORKLOADS[key], rank, world)
+
+
+def test_config_block_of_the_default_workload():
+    c = _gpu_arm_config("c4", 0)
+    assert (c["psi"], c["nd"], c["shard_params"], c["row_stride_elems"]) == \
+        (7_500_000_000, 64, 117_187_500, 117_187_504)
+    assert c["grad_dtype"] == "bf16" and c["bucket"] == 500_000_000
+    assert c["l2"].startswith("inputs larger than L2 (18.0 GB per step)")
+    assert _gpu_arm_config("c0", 0)["l2"].startswith("inputs L2-resident")
 
 
 @pytest.mark.gpu
@@ -63,6 +84,18 @@ def test_gpu_arm_line():
     per_step = _abi.fused_launch_count(n, 50_000_000, 0)
     assert r["launches_per_step"] == per_step == 1
     assert r["algorithmic_bytes_per_launch"] == (2 * 8 + 26) * n / per_step
+    # the read-only ceiling over the same rows is measured beside the copy peak
+    assert r["read_ceiling_gbs"] > 0
+    assert r["frac_of_read_ceiling"] == pytest.approx(r["achieved"] / r["read_ceiling_gbs"])
+    assert d["config"] == _gpu_arm_config("c1", 0)
+    # the other workloads' kernel timings: every target workload but this one
+    pc = d["per_config"]
+    assert set(pc) == {"c0 rank 0", "c2 rank 0", "c3 rank 0", "c3 rank 1 (flat buffer slot)"}
+    for v in pc.values():
+        assert v["skipped"] is False and v["kernel_ms_per_step"] > 0
+        assert v["frac"] == pytest.approx(v["achieved"] / r["peak"])
+    assert pc["c3 rank 0"]["shard_params"] == 23_437_500
+    assert pc["c3 rank 0"]["launches_per_step"] == 1 and "l2" in pc["c0 rank 0"]
     # the timed region launches exactly one fused step per timed step
     assert d["gpu_launches"] == 6 * per_step
     e = d["e2e"]
