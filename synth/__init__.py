@@ -173,6 +173,18 @@ def fill_full_rows(w: Workload, step: int, out: torch.Tensor, chunk: int = 1 << 
     """
     s = -(-w.psi // w.nd)
     pitch = out.shape[1] // w.nd
+    if w.nd * s <= chunk:
+        # small vectors: one generator call per contributor over all psi
+        # indices, placed into the padded partitions (zero past each shard)
+        idx = torch.arange(w.psi, dtype=torch.int64, device=out.device)
+        for j in range(w.nd):
+            vals = grad_values(w, step, j, idx)
+            flat = torch.zeros(w.nd * s, dtype=vals.dtype, device=out.device)
+            flat[:w.psi] = vals
+            row = out[j].view(w.nd, pitch)
+            row[:, :s] = flat.view(w.nd, s)
+            row[:, s:].zero_()
+        return
     for r in range(w.nd):
         fill_shard_rows(w, step, r, out[:, r * pitch:(r + 1) * pitch], chunk)
 

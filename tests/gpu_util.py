@@ -172,6 +172,7 @@ EDGE_CASES = [
     (70_001, 16, "f16", 7),      # S mod 8 = 3: every slot phase
     (130_003, 64, "bf16", 2049), # 64 ranks, S mod 8 = 4
     (250_000, 2, "f16", 250_000),
+    (102_407, 1024, "bf16", 4099),   # the pages' largest Nd: 1,024 rows folded, S mod 8 = 5
 ]
 
 

@@ -12,6 +12,7 @@ all 16 ranks, +inf planted at step 5); GPT-2 1.5B shard view (Nd = 64, fp16,
 20 steps); 7.5B shard view (Nd = 64, bf16, bucket 5e8, 20 steps); the
 end-to-end forms (rows in pinned host memory) on the 1.5B shard view.
 """
+import dataclasses
 import gc
 
 import numpy as np
@@ -186,3 +187,55 @@ def test_c3_end_to_end_forms_sampled(form):
         assert_state_close(gv, v, 1e-20, f"{form} v step {k}")
         assert_params_close(_slot_params(dps, rank, idx), params, f"{form} params step {k}")
         assert dps.t == t
+
+
+def test_shard_past_the_int32_range():
+    """Rank 1 of two holds 2,147,483,657 elements (2^31 + 9, bf16): every
+    element index of the second half is past the int32 range and its flat
+    indices pass 2^32; the fused step runs it as 86 launch windows.  Two
+    steps, sampled against the oracle at both ends, around every window cut
+    and at random points; the state past the shard stays zero.  About 70 GB
+    on the device."""
+    n = 2 ** 31 + 9
+    w = dataclasses.replace(synth.WORKLOADS["c1"], psi=2 * n, nd=2, plant=None,
+                            bucket=1 << 30, fresh_grads=False, steps=2)
+    rank = 1
+    dps = make_group(w, ranks=[rank], gathered="slot")
+    assert int(dps.layouts[rank].length) == n
+    assert z.fused_launch_count(n, w.bucket) == 86
+    idx = sample_indices(w.psi, w.nd, [rank], 4096, seed=31,
+                         extra=[n + 2 ** 31 - 1, n + 2 ** 31, n + 2 ** 32 - n])
+    _, hist = oracle_trajectory(w, idx, 2)
+    buf, desc = shard_rows(w, dps, rank, 0)
+    for k in range(2):
+        assert not dps.step(desc)
+        p, m, v, params, t = hist[k]
+        (gp, gm, gv), _ = _sampled_state(dps, idx, with_params=False)
+        assert_state_close(gp, p, 1e-12, f"master step {k}")
+        assert_state_close(gm, m, 1e-20, f"m step {k}")
+        assert_state_close(gv, v, 1e-20, f"v step {k}")
+        assert_params_close(_slot_params(dps, rank, idx), params, f"params step {k}")
+        assert dps.t == t
+    for b in dps.state[rank].bufs:
+        assert not b[:, n:].any()
+
+
+def test_7p5b_shard_at_nd_1024():
+    """The 7.5B model at Nd = 1,024 (the largest data-parallel degree of the
+    pages' Stage-3 memory table): rank 517's shard of 7,324,219 parameters
+    folds 1,024 bf16 rows (15 GB).  One step, sampled against the oracle."""
+    w = dataclasses.replace(synth.WORKLOADS["c4"], nd=1024, plant=None, steps=1)
+    rank = 517
+    dps = make_group(w, ranks=[rank], gathered="slot")
+    n = int(dps.layouts[rank].length)
+    assert n == 7_324_219
+    idx = sample_indices(w.psi, w.nd, [rank], 1024, seed=1024)
+    _, hist = oracle_trajectory(w, idx, 1)
+    buf, desc = shard_rows(w, dps, rank, 0)
+    assert not dps.step(desc)
+    p, m, v, params, t = hist[0]
+    (gp, gm, gv), _ = _sampled_state(dps, idx, with_params=False)
+    assert_state_close(gp, p, 1e-12, "master")
+    assert_state_close(gm, m, 1e-20, "m")
+    assert_state_close(gv, v, 1e-20, "v")
+    assert_params_close(_slot_params(dps, rank, idx), params, "params")

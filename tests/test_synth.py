@@ -74,3 +74,19 @@ def test_workload_table():
     assert [WORKLOADS[k].shard for k in ("c0", "c1", "c2", "c3", "c4")] == \
         [262_144, 15_554_976, 21_875_002, 23_437_500, 117_187_500]
     assert WORKLOADS["c4"].bytes_per_param == 154 and WORKLOADS["c1"].bytes_per_param == 42
+
+
+def test_full_rows_placements_agree():
+    """The one-call-per-contributor placement of small vectors gives the same
+    bytes as the shard-by-shard one (padding zero, a planted +inf kept)."""
+    import dataclasses
+    for psi, nd in [(1000, 3), (3, 5), (70_001, 16), (102_407, 64)]:
+        w = dataclasses.replace(synth.WORKLOADS["c2"], psi=psi, nd=nd, plant=(0, 1, psi // 2))
+        s = -(-psi // nd)
+        pitch = synth.pitch_of(s)
+        a = torch.full((nd, nd * pitch), 7, dtype=torch.float16)
+        b = torch.full((nd, nd * pitch), 7, dtype=torch.float16)
+        synth.fill_full_rows(w, 0, a)
+        synth.fill_full_rows(w, 0, b, chunk=nd * s - 1)    # below nd*S: shard by shard
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), (psi, nd)
+        assert bool(torch.isinf(a).any())
