@@ -57,6 +57,11 @@ zero_status_t resolve_ptr(const void* p, void** out, bool* on_host = nullptr);
 // rows are in host memory.
 zero_status_t resolve_grads(const zero_grads_t* g, zero_grads_t* out, bool* in_host = nullptr);
 
+// True unless the environment variable ZERO_PDL (read at each call) is "0":
+// step kernels, and the bucket-ready step's waits, are then launched as
+// programmatic dependent launches.
+bool pdl_launches();
+
 // Loads now, once per device, every instance of the fused-step kernel that
 // launch_fused_range can launch for `dtype` and rows where host_rows says.
 // Under CUDA's lazy loading a kernel is otherwise loaded at its first

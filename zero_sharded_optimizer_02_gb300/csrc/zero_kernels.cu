@@ -943,6 +943,8 @@ void load_fused_dt(int variant)
 
 }  // namespace
 
+bool pdl_launches() { return pdl_enabled(); }
+
 void preload_fused(int dtype, bool host_rows)
 {
     const int variant = fused_variant(host_rows);

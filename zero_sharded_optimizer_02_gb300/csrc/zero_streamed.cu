@@ -62,16 +62,49 @@ __device__ bool wait_ready(const uint32_t* word, uint32_t epoch, uint64_t timeou
 // One launch group's wait: a single thread polls the ready words of `count`
 // consecutive buckets in order (each wait bounded).  If an earlier wait of
 // the call ran out (status nonzero), it does not wait again.
+//
+// Launched as a programmatic dependent launch, it starts while the previous
+// group's step kernel is still running: it lets the next group's launch be
+// scheduled at once, polls, and only then waits (griddepcontrol.wait) for
+// its predecessor in the stream to complete.  It therefore never completes
+// before that kernel, so every later kernel that waits for its own
+// predecessor also waits for all earlier ones; the next group's step kernel
+// starts as the previous one drains, as between two launch windows.  On a
+// plain launch both instructions are no-ops and the kernel runs after its
+// predecessor, as before.
 __global__ void k_wait_ready(const uint32_t* words, uint32_t count, uint32_t epoch,
                              uint64_t timeout_ns, uint32_t* status)
 {
-    if (*static_cast<volatile uint32_t*>(status) != 0)
-        return;
-    for (uint32_t i = 0; i < count; ++i)
-        if (!wait_ready(words + i, epoch, timeout_ns)) {
-            atomicCAS(status, 0u, (uint32_t)ZERO_ERR_TIMEOUT);
-            return;
-        }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (ld_acquire(status) == 0) {
+        for (uint32_t i = 0; i < count; ++i)
+            if (!wait_ready(words + i, epoch, timeout_ns)) {
+                atomicCAS(status, 0u, (uint32_t)ZERO_ERR_TIMEOUT);
+                break;
+            }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// k_wait_ready on `stream`, as a programmatic dependent launch unless
+// ZERO_PDL is "0".
+cudaError_t launch_wait(cudaStream_t stream, const uint32_t* words, uint32_t count,
+                        uint32_t epoch, uint64_t timeout_ns, uint32_t* status)
+{
+    if (!pdl_launches()) {
+        k_wait_ready<<<1, 1, 0, stream>>>(words, count, epoch, timeout_ns, status);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_wait_ready, words, count, epoch, timeout_ns, status);
 }
 
 bool is_aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
@@ -137,9 +170,8 @@ extern "C" zero_status_t zero_step_shard_streamed(
         const uint64_t g0 = b * bucket_elems;
         const uint64_t b_end = b + base + (grp < extra ? 1 : 0);
         const uint64_t glen = (b_end * bucket_elems < n ? b_end * bucket_elems : n) - g0;
-        k_wait_ready<<<1, 1, 0, st>>>(d_ready + b, (uint32_t)(b_end - b), epoch, timeout_ns,
-                                      d_status);
-        if (cudaGetLastError() != cudaSuccess)
+        if (launch_wait(st, d_ready + b, (uint32_t)(b_end - b), epoch, timeout_ns, d_status) !=
+            cudaSuccess)
             return ZERO_ERR_CUDA;
         const zero_status_t ls = launch_fused_range(rows, g, in, out, gath, g0, glen, k,
                                                      host_rows, d_nonfinite, d_status, stream);
