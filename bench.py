@@ -169,10 +169,11 @@ def time_back_to_back(torch, stream, dev, call, reps: int) -> float:
 
 
 # The other workloads the default line also times (kernel time only): the
-# 1.5B shard is the second target workload; its odd rank writes its
-# parameters into its slot of the flat buffer, 8 bytes off a 16-byte line.
+# 1.5B shard is the second target workload; rank 1 of the 1.5B and 7.5B
+# shards writes its parameters into its slot of the flat Nd*S buffer, 8 bytes
+# off a 16-byte line (S mod 8 = 4), so its cast runs with 8-byte stores.
 PER_CONFIG = [("c0", 0, "slot"), ("c1", 0, "slot"), ("c2", 0, "slot"), ("c3", 0, "slot"),
-              ("c3", 1, "full")]
+              ("c3", 1, "full"), ("c4", 1, "full")]
 
 
 def measure_config(key: str, rank: int, gathered: str, dev, stream, peak: float,

@@ -90,7 +90,8 @@ def test_gpu_arm_line():
     assert d["config"] == _gpu_arm_config("c1", 0)
     # the other workloads' kernel timings: every target workload but this one
     pc = d["per_config"]
-    assert set(pc) == {"c0 rank 0", "c2 rank 0", "c3 rank 0", "c3 rank 1 (flat buffer slot)"}
+    assert set(pc) == {"c0 rank 0", "c2 rank 0", "c3 rank 0", "c3 rank 1 (flat buffer slot)",
+                       "c4 rank 1 (flat buffer slot)"}
     for v in pc.values():
         assert v["skipped"] is False and v["kernel_ms_per_step"] > 0
         assert v["frac"] == pytest.approx(v["achieved"] / r["peak"])
