@@ -87,11 +87,17 @@ typedef struct zero_layout {
  * offset = rank * row_pitch.  Shard view: row j holds only this shard,
  * row_stride = row_pitch, offset = 0.
  * Alignment: base 16-byte aligned; row_stride and offset multiples of 8.
+ * nd: 1 <= nd <= ZERO_MAX_ND (ZERO_ERR_INVALID_ARG otherwise).
  * Memory: device (or managed) memory, or page-locked host memory registered
  * with CUDA (cudaHostAlloc, cudaHostRegister), which the kernels then read in
  * place over the host link (zero-copy: no device copy of the gradients).  Any
  * other pointer, pageable host memory included, is ZERO_ERR_INVALID_ARG
  * before anything is launched. */
+/* Largest number of contribution rows a gradient descriptor may name: the
+ * pages' largest data-parallel degree is 1,024; 2^24 leaves every row-count
+ * computation of the kernels far from 32-bit overflow. */
+#define ZERO_MAX_ND 16777216u
+
 typedef struct zero_grads {
     const void* base;     /* device or page-locked host memory, read-only */
     uint64_t row_stride;  /* elements between consecutive ranks' rows */

@@ -137,6 +137,7 @@ def _state(z, base):
     ("null_base", "ZERO_ERR_INVALID_ARG"), ("misaligned_base", "ZERO_ERR_ALIGNMENT"),
     ("odd_row_stride", "ZERO_ERR_ALIGNMENT"), ("odd_offset", "ZERO_ERR_ALIGNMENT"),
     ("bad_dtype", "ZERO_ERR_INVALID_ARG"), ("nd_zero", "ZERO_ERR_INVALID_ARG"),
+    ("nd_too_large", "ZERO_ERR_INVALID_ARG"),
     ("shard_longer_than_s", "ZERO_ERR_INVALID_ARG"), ("misaligned_state", "ZERO_ERR_ALIGNMENT"),
     ("overlap_state", "ZERO_ERR_INVALID_ARG"), ("bucket_zero", "ZERO_ERR_INVALID_ARG"),
     ("step_zero", "ZERO_ERR_INVALID_ARG"), ("bad_beta", "ZERO_ERR_INVALID_ARG"),
@@ -164,6 +165,9 @@ def test_step_shard_rejects(z, case, status):
         g.dtype = 7
     elif case == "nd_zero":
         g.nd = 0
+    elif case == "nd_too_large":                 # past the kernels' row-count range
+        g.nd = z._abi.ZERO_MAX_ND + 1
+        g.row_stride = 8
     elif case == "shard_longer_than_s":
         L.length = L.shard_elems + 1
     elif case == "misaligned_state":
@@ -254,6 +258,8 @@ def test_binding_constants_match_header(z):
                  "ZERO_GATHER_SEGMENTS_PER_LAUNCH", "ZERO_STREAM_GROUP_BYTES"):
         m = re.search(rf"#define {name} (\d+)ull", text)
         assert m and int(m.group(1)) == getattr(z._abi, name), name
+    m = re.search(r"#define ZERO_MAX_ND (\d+)u", text)
+    assert m and int(m.group(1)) == z._abi.ZERO_MAX_ND == 1 << 24
     m = re.search(r"#define ZERO_STEP_FLAG_WAIT_TIMEOUT (0x[0-9A-Fa-f]+)u", text)
     assert m and int(m.group(1), 16) == z._abi.ZERO_STEP_FLAG_WAIT_TIMEOUT
     # the flag word: zero commits, any nonfinite bit skips, the wait bit raises

@@ -94,6 +94,37 @@ def test_streamed_matches_fused(psi, nd, rank, dt, bucket, group_bytes, monkeypa
     assert np.array_equal(u16(gath[b:b + n]), u16(gath_ref[b:b + n]))
 
 
+@pytest.mark.parametrize("bucket", [2 ** 64 - 1, 2 ** 63 + 5])
+def test_bucket_near_the_top_of_the_range(bucket):
+    """A bucket size near 2^64 is one bucket of the whole shard: the feeder
+    lands it with one copy and its ready word, and the bucket-ready step waits
+    for that word and steps everything (its bucket count must not wrap)."""
+    w, dps, rows, g = _setup(200_003, 4, 2, "bf16")
+    out_ref, gath_ref = _fused_reference(w, dps, rank=2, g=g, bucket=64)
+    L = dps.layouts[2]
+    n = int(L.length)
+    host = rows.cpu().pin_memory()
+    rows.zero_()
+    ready = torch.zeros(1, dtype=torch.int32, device=DEV)
+    epoch = torch.ones(1, dtype=torch.int32).pin_memory()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    st = dps.state[2]
+    out = torch.full_like(st.bufs[0], -1.0)
+    gath = torch.zeros_like(dps.gathered[0])
+    compute, copy = torch.cuda.Stream(DEV), torch.cuda.Stream(DEV)
+    torch.cuda.synchronize()
+    h = z.adamw(w.hparams["lr"], 0.9, 0.999, 1e-8, 0.01, 1)
+    z.zero_step_shard_streamed(g, L, st.states[st.cur], z.state(*out), gath, L.begin, bucket,
+                               w.loss_scale, h, ready, 1, 5_000_000_000, flag, status, compute)
+    z.zero_feed_buckets(host, int(L.row_pitch), g, n, bucket, ready, epoch, copy)
+    torch.cuda.synchronize()
+    assert int(ready.item()) == 1 and int(status.item()) == 0 and int(flag.item()) == 0
+    assert torch.equal(out[:, :n].view(torch.int32), out_ref[:, :n].view(torch.int32))
+    b = int(L.begin)
+    assert np.array_equal(u16(gath[b:b + n]), u16(gath_ref[b:b + n]))
+
+
 def test_wait_that_nothing_satisfies_times_out(monkeypatch):
     monkeypatch.setenv("ZERO_STREAM_GROUP_BYTES", "0")     # every bucket its own group
     psi, nd, rank, bucket = 300_000, 4, 0, 10_000

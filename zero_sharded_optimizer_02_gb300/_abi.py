@@ -87,6 +87,9 @@ _SIGNATURES = {
                                         vp, vp], i32),
 }
 
+# Most contribution rows a gradient descriptor may name (include/zero.h).
+ZERO_MAX_ND = 1 << 24
+
 # Longest launch window of the fused step (include/zero.h).
 ZERO_FUSED_WINDOW_ELEMS = 25165824
 

@@ -570,7 +570,10 @@ bool mul_overflows(uint64_t a, uint64_t b) { return a != 0 && b > UINT64_MAX / a
 // Validates a gradient descriptor for elements [begin, begin + n) of the shard.
 zero_status_t check_grads(const zero_grads_t* g, uint64_t begin, uint64_t n)
 {
-    if (!g || !g->base || g->nd == 0 || (g->dtype != ZERO_F16 && g->dtype != ZERO_BF16))
+    // nd <= ZERO_MAX_ND keeps the kernels' 32-bit row counts (nd + 7,
+    // j0 += 8) far from wrapping
+    if (!g || !g->base || g->nd == 0 || g->nd > ZERO_MAX_ND ||
+        (g->dtype != ZERO_F16 && g->dtype != ZERO_BF16))
         return ZERO_ERR_INVALID_ARG;
     if (!aligned(g->base, 16) || (g->row_stride & 7) != 0 || (g->offset & 7) != 0)
         return ZERO_ERR_ALIGNMENT;

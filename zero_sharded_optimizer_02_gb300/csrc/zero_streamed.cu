@@ -72,12 +72,12 @@ __device__ bool wait_ready(const uint32_t* word, uint32_t epoch, uint64_t timeou
 // starts as the previous one drains, as between two launch windows.  On a
 // plain launch both instructions are no-ops and the kernel runs after its
 // predecessor, as before.
-__global__ void k_wait_ready(const uint32_t* words, uint32_t count, uint32_t epoch,
+__global__ void k_wait_ready(const uint32_t* words, uint64_t count, uint32_t epoch,
                              uint64_t timeout_ns, uint32_t* status)
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (ld_acquire(status) == 0) {
-        for (uint32_t i = 0; i < count; ++i)
+        for (uint64_t i = 0; i < count; ++i)
             if (!wait_ready(words + i, epoch, timeout_ns)) {
                 atomicCAS(status, 0u, (uint32_t)ZERO_ERR_TIMEOUT);
                 break;
@@ -88,7 +88,7 @@ __global__ void k_wait_ready(const uint32_t* words, uint32_t count, uint32_t epo
 
 // k_wait_ready on `stream`, as a programmatic dependent launch unless
 // ZERO_PDL is "0".
-cudaError_t launch_wait(cudaStream_t stream, const uint32_t* words, uint32_t count,
+cudaError_t launch_wait(cudaStream_t stream, const uint32_t* words, uint64_t count,
                         uint32_t epoch, uint64_t timeout_ns, uint32_t* status)
 {
     if (!pdl_launches()) {
@@ -108,6 +108,9 @@ cudaError_t launch_wait(cudaStream_t stream, const uint32_t* words, uint32_t cou
 }
 
 bool is_aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+// ceil(n / bucket) for any bucket >= 1 (no overflow for a bucket near 2^64).
+uint64_t buckets_of(uint64_t n, uint64_t bucket) { return n / bucket + (n % bucket != 0); }
 
 }  // namespace
 }  // namespace zero
@@ -161,7 +164,7 @@ extern "C" zero_status_t zero_step_shard_streamed(
         if (end != e && *end == '\0')
             group_bytes = v;
     }
-    const uint64_t nb = (n + bucket_elems - 1) / bucket_elems;
+    const uint64_t nb = buckets_of(n, bucket_elems);
     const uint64_t traffic = n * (2ull * g->nd + 26);
     uint64_t ngroups = group_bytes ? traffic / group_bytes : nb;
     ngroups = ngroups < 1 ? 1 : (ngroups > nb ? nb : ngroups);
@@ -170,8 +173,7 @@ extern "C" zero_status_t zero_step_shard_streamed(
         const uint64_t g0 = b * bucket_elems;
         const uint64_t b_end = b + base + (grp < extra ? 1 : 0);
         const uint64_t glen = (b_end * bucket_elems < n ? b_end * bucket_elems : n) - g0;
-        if (launch_wait(st, d_ready + b, (uint32_t)(b_end - b), epoch, timeout_ns, d_status) !=
-            cudaSuccess)
+        if (launch_wait(st, d_ready + b, b_end - b, epoch, timeout_ns, d_status) != cudaSuccess)
             return ZERO_ERR_CUDA;
         const zero_status_t ls = launch_fused_range(rows, g, in, out, gath, g0, glen, k,
                                                      host_rows, d_nonfinite, d_status, stream);
@@ -187,7 +189,8 @@ extern "C" zero_status_t zero_feed_buckets(const void* host, uint64_t host_row_s
                                            uint64_t bucket_elems, uint32_t* d_ready,
                                            const uint32_t* h_epoch, void* copy_stream)
 {
-    if (!host || !g || !g->base || g->nd == 0 || !d_ready || !h_epoch || bucket_elems == 0)
+    if (!host || !g || !g->base || g->nd == 0 || g->nd > ZERO_MAX_ND || !d_ready || !h_epoch ||
+        bucket_elems == 0)
         return ZERO_ERR_INVALID_ARG;
     if (host_row_stride < n || g->row_stride < g->offset + n ||
         host_row_stride > (1ull << 60) / 2 || g->row_stride > (1ull << 60) / 2)
@@ -198,7 +201,7 @@ extern "C" zero_status_t zero_feed_buckets(const void* host, uint64_t host_row_s
     cudaStream_t st = static_cast<cudaStream_t>(copy_stream);
     const char* src = static_cast<const char*>(host);
     char* dst = const_cast<char*>(static_cast<const char*>(g->base)) + 2 * g->offset;
-    const uint64_t nb = (n + bucket_elems - 1) / bucket_elems;
+    const uint64_t nb = buckets_of(n, bucket_elems);
     for (uint64_t b = 0; b < nb; ++b) {
         const uint64_t b0 = b * bucket_elems;
         const uint64_t len = n - b0 < bucket_elems ? n - b0 : bucket_elems;
