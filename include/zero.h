@@ -335,8 +335,11 @@ zero_status_t zero_feed_buckets(const void* host, uint64_t host_row_stride,
  * gives (S = ceil(psi / nd)); shard r's elements sit at
  * shards[r * pitch + local], local < S, pitch >= S.  elem_bytes is 2 (fp16 or
  * bf16 parameters) or 4 (fp32 state, e.g. to reshard to another nd).
- * shards and out: device, aligned to elem_bytes; out must not overlap the
- * shards; only the range's own elements are read.  The range spans at most
+ * shards and out: device memory, or page-locked host memory registered with
+ * CUDA (accessed in place at its device mapping), aligned to elem_bytes;
+ * any other pointer (pageable host memory) is ZERO_ERR_INVALID_ARG before
+ * anything is launched.  out must not overlap the shards; only the range's
+ * own elements are read.  The range spans at most
  * ceil(len / S) + 1 shard segments; one launch copies up to
  * ZERO_GATHER_SEGMENTS_PER_LAUNCH of them.  ZERO_ERR_INVALID_ARG on a range
  * outside [0, psi), pitch < S, NULL pointers or overlap. */

@@ -92,3 +92,35 @@ def test_zero3_layer_gather_after_step():
         z.zero_gather_range(rows, pitch, w.psi, w.nd, int(a), int(b - a), 2, out)
         torch.cuda.synchronize()
         assert np.array_equal(u16(out), params_ref[a:b]), (a, b)
+
+
+def test_gather_from_and_into_host_memory():
+    """Shards and destination in page-locked host memory are accessed in
+    place at their device mapping and give the oracle's range; a pageable host
+    pointer is refused with ZERO_ERR_INVALID_ARG before anything is launched
+    (the destination is left untouched)."""
+    psi, nd = 100_003, 7
+    s = -(-psi // nd)
+    pitch = -(-s // 8) * 8 + 8
+    rng = np.random.default_rng(5)
+    host = rng.integers(0, 1 << 16, (nd, pitch), dtype=np.uint64).astype(np.uint16)
+    begin, length = s - 77, 3 * s + 5
+    ref = oracle.gather_range(host, psi, nd, begin, length)
+    shards_dev = torch.from_numpy(host.view(np.int16)).to(DEV)
+    shards_pin = torch.from_numpy(host.view(np.int16)).pin_memory()
+    out_pin = torch.zeros(length, dtype=torch.int16).pin_memory()
+    out_dev = torch.zeros(length, dtype=torch.int16, device=DEV)
+    for src, dst in ((shards_pin, out_dev), (shards_dev, out_pin), (shards_pin, out_pin)):
+        dst.zero_()
+        z.zero_gather_range(src, pitch, psi, nd, begin, length, 2, dst)
+        torch.cuda.synchronize()
+        assert np.array_equal(dst.cpu().numpy().view(np.uint16), ref)
+    pageable_out = torch.full((length,), 7, dtype=torch.int16)
+    pageable_src = torch.from_numpy(host.view(np.int16).copy())
+    for src, dst in ((shards_dev, pageable_out), (pageable_src, out_dev)):
+        out_dev.fill_(7)
+        with pytest.raises(z.ZeroError) as e:
+            z.zero_gather_range(src, pitch, psi, nd, begin, length, 2, dst)
+        assert e.value.status == z.ZERO_ERR_INVALID_ARG
+        torch.cuda.synchronize()
+        assert bool((dst == 7).all()), "a refused gather wrote"

@@ -20,6 +20,7 @@
 #include <stdint.h>
 
 #include "zero.h"
+#include "zero_internal.h"
 
 namespace zero {
 namespace {
@@ -197,6 +198,21 @@ extern "C" zero_status_t zero_gather_range(const void* shards, uint64_t pitch, u
     const uintptr_t ob = (uintptr_t)out, oe = ob + len * elem_bytes;
     if (len && ob < se && sb < oe)
         return ZERO_ERR_INVALID_ARG;   // out overlaps the shards
+    if (len == 0)
+        return ZERO_OK;
+    // where the kernel reads and writes: device or managed memory as is,
+    // page-locked host memory at its device mapping; anything else (pageable
+    // host memory) is refused before anything is launched
+    void* sdev = nullptr;
+    void* odev = nullptr;
+    zero_status_t rs = zero::resolve_ptr(shards, &sdev);
+    if (rs != ZERO_OK)
+        return rs;
+    rs = zero::resolve_ptr(out, &odev);
+    if (rs != ZERO_OK)
+        return rs;
+    shards = sdev;
+    out = odev;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const uint64_t units_per_elem = elem_bytes / 2;
     zero::SegBatch batch;
