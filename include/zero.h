@@ -19,9 +19,12 @@
  *   - Ownership: the caller owns all memory.  The library borrows the pointers
  *     for stream-ordered work and allocates nothing.  Every call is
  *     thread-safe; calls on one stream execute in order.
- *   - Pointers named d_* or documented "device" must be device memory of the
- *     current CUDA device; structs passed by pointer are host memory and are
- *     read before the call returns.
+ *   - Pointers named d_* or documented "device" must be device (or managed)
+ *     memory of the current CUDA device: the fp32 state, fusion buffers, the
+ *     primitives' fp32 inputs and the flag, status and ready words.  A host
+ *     pointer there (pageable or page-locked) is ZERO_ERR_INVALID_ARG before
+ *     anything is launched.  Structs passed by pointer are host memory and
+ *     are read before the call returns.
  *   - Gradient rows (zero_grads_t.base) and gathered parameter buffers may
  *     also be page-locked host memory registered with CUDA (cudaHostAlloc,
  *     cudaHostRegister): the kernels then read the rows, or write the cast

@@ -147,3 +147,58 @@ def test_in_place_with_precheck():
     assert_state_close(m, hist[0][1], 1e-20, "in-place m")
     assert_state_close(v, hist[0][2], 1e-20, "in-place v")
     assert_params_close(u16(gath[:n]), hist[0][3], "in-place params")
+
+
+@pytest.mark.parametrize("where", ["pageable", "pinned"])
+@pytest.mark.parametrize("what", ["state_in", "state_out", "flag", "cb", "adam_grad",
+                                  "cast_master"])
+def test_host_memory_is_refused_where_device_memory_is_required(what, where):
+    """The fp32 state, the flag word, the fusion buffer and the primitives'
+    fp32 inputs must be device memory: a host pointer there is
+    ZERO_ERR_INVALID_ARG before anything is launched, and nothing is written."""
+    w = dataclasses.replace(synth.WORKLOADS["c1"], psi=80_003, nd=4, plant=None)
+    dps = make_group(w, ranks=[1], gathered="slot")
+    buf, desc = shard_rows(w, dps, 1, 0)
+    L = dps.layouts[1]
+    n = int(L.length)
+    st = dps.state[1]
+
+    def host_like(t):
+        h = torch.full(t.shape, 3.0, dtype=t.dtype)
+        return h.pin_memory() if where == "pinned" else h
+    s_in, s_out = st.states[st.cur], st.states[1 - st.cur]
+    flag = dps.flag
+    cb = torch.zeros(n + 4, dtype=torch.float32, device=DEV)
+    gath = dps.gathered_view(1)
+    out_dev = torch.full((3, n), 5.0, device=DEV)
+    keep = []
+    if what == "state_in":
+        keep = [host_like(st.bufs[st.cur])]
+        s_in = z.state(*keep[0])
+    elif what == "state_out":
+        keep = [host_like(st.bufs[1 - st.cur])]
+        s_out = z.state(*keep[0])
+    elif what == "flag":
+        keep = [host_like(dps.flag)]
+        flag = keep[0]
+    elif what == "cb":
+        keep = [host_like(cb)]
+        cb = keep[0]
+    before = [t.clone() for t in st.bufs] + [gath.clone(), out_dev.clone()]
+    h = z.adamw(1e-4, 0.9, 0.999, 1e-8, 0.01, 1)
+    with pytest.raises(z.ZeroError) as e:
+        if what == "adam_grad":
+            z.zero_adam_step_shard(host_like(cb)[:n], z.state(*st.bufs[st.cur][:, :n]),
+                                   z.state(*out_dev), n, h)
+        elif what == "cast_master":
+            z.zero_gather_params_shard(host_like(out_dev)[0], n, gath, 0, w.grad_dtype)
+        elif what == "cb":
+            z.zero_step_shard_unfused(desc[1], L, s_in, s_out, gath, 0, 4096, w.loss_scale, h,
+                                      cb, cb.numel(), flag)
+        else:
+            z.zero_step_shard(desc[1], L, s_in, s_out, gath, 0, 4096, w.loss_scale, h, flag)
+    assert e.value.status == z.ZERO_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    after = [t for t in st.bufs] + [gath, out_dev]
+    assert all(torch.equal(a, b) for a, b in zip(before, after)), "a refused call wrote"
+    assert all(bool((k == 3.0).all()) for k in keep)

@@ -62,6 +62,18 @@ zero_status_t resolve_grads(const zero_grads_t* g, zero_grads_t* out, bool* in_h
 // programmatic dependent launches.
 bool pdl_launches();
 
+// ZERO_OK if each of the `count` pointers is device or managed memory;
+// ZERO_ERR_INVALID_ARG for host memory (pageable or page-locked) or a pointer
+// CUDA does not know; ZERO_ERR_CUDA if the runtime cannot answer (no device
+// or driver).  For the buffers the kernels must find in device memory: the
+// fp32 state, the fusion buffer and the flag and status words.
+zero_status_t require_device(const void* const* ptrs, int count);
+
+// require_device over the six state arrays of in and out and, if non-null,
+// one more word (a flag, or the gradient of the AdamW primitive).
+zero_status_t require_device_state(const zero_state_t* in, const zero_state_t* out,
+                                   const void* word);
+
 // Loads now, once per device, every instance of the fused-step kernel that
 // launch_fused_range can launch for `dtype` and rows where host_rows says.
 // Under CUDA's lazy loading a kernel is otherwise loaded at its first

@@ -78,6 +78,28 @@ zero_status_t resolve_grads(const zero_grads_t* g, zero_grads_t* out, bool* in_h
     return st;
 }
 
+zero_status_t require_device(const void* const* ptrs, int count)
+{
+    for (int i = 0; i < count; ++i) {
+        cudaPointerAttributes at;
+        const cudaError_t e = cudaPointerGetAttributes(&at, ptrs[i]);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return e == cudaErrorInvalidValue ? ZERO_ERR_INVALID_ARG : ZERO_ERR_CUDA;
+        }
+        if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+            return ZERO_ERR_INVALID_ARG;
+    }
+    return ZERO_OK;
+}
+
+zero_status_t require_device_state(const zero_state_t* in, const zero_state_t* out,
+                                   const void* word)
+{
+    const void* p[7] = {in->master, in->m, in->v, out->master, out->m, out->v, word};
+    return require_device(p, word ? 7 : 6);
+}
+
 namespace {
 
 constexpr int kThreads = 256;       // threads per CTA
@@ -1019,6 +1041,10 @@ extern "C" zero_status_t zero_reduce_scatter_bucket(const zero_grads_t* g, uint6
     st = resolve_grads(g, &gr, &host_rows);
     if (st != ZERO_OK)
         return st;
+    const void* words[2] = {cb_out, d_nonfinite};
+    st = require_device(words, 2);
+    if (st != ZERO_OK)
+        return st;
     const int variant = fused_variant(host_rows);
     const uint16_t* first = static_cast<const uint16_t*>(gr.base) + g->offset + bucket_begin;
     return for_each_window(g->offset + bucket_begin, bucket_len, kWindow,
@@ -1048,6 +1074,10 @@ extern "C" zero_status_t zero_check_nonfinite(const zero_grads_t* g, uint64_t be
     st = resolve_grads(g, &gr, &host_rows);
     if (st != ZERO_OK)
         return st;
+    const void* word = d_nonfinite;
+    st = require_device(&word, 1);
+    if (st != ZERO_OK)
+        return st;
     const int variant = fused_variant(host_rows);
     const uint16_t* first = static_cast<const uint16_t*>(gr.base) + g->offset + begin;
     return for_each_window(g->offset + begin, n, kWindow, [&](uint64_t w0, uint64_t w1) {
@@ -1074,6 +1104,9 @@ extern "C" zero_status_t zero_adam_step_shard(const float* grad, const zero_stat
         return ZERO_ERR_INVALID_ARG;
     if (n == 0)
         return ZERO_OK;
+    st = require_device_state(in, out, grad);
+    if (st != ZERO_OK)
+        return st;
     launch_adam(grad, in, out, n, make_scalars(h, 1, 1.0), static_cast<cudaStream_t>(stream));
     return launch_status();
 }
@@ -1093,7 +1126,11 @@ extern "C" zero_status_t zero_gather_params_shard(const float* master, uint64_t 
     if (ranges_overlap(static_cast<uint16_t*>(gathered) + slot_offset_elems, master, n * 4))
         return ZERO_ERR_INVALID_ARG;   // conservative: the larger extent
     void* gdev = nullptr;   // the slot at the address the device writes it
-    const zero_status_t st = resolve_ptr(gathered, &gdev);
+    zero_status_t st = resolve_ptr(gathered, &gdev);
+    if (st != ZERO_OK)
+        return st;
+    const void* src = master;
+    st = require_device(&src, 1);
     if (st != ZERO_OK)
         return st;
     uint16_t* slot = static_cast<uint16_t*>(gdev) + slot_offset_elems;
@@ -1122,6 +1159,9 @@ extern "C" zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layou
         return st;
     void* gdev = nullptr;   // the gathered buffer at the address the device writes it
     st = resolve_ptr(gathered, &gdev);
+    if (st != ZERO_OK)
+        return st;
+    st = require_device_state(in, out, d_nonfinite);
     if (st != ZERO_OK)
         return st;
     const StepScalars k = make_scalars(h, g->nd, loss_scale);
@@ -1162,6 +1202,13 @@ extern "C" zero_status_t zero_step_shard_unfused(const zero_grads_t* g, const ze
         return st;
     void* gdev = nullptr;   // the gathered buffer at the address the device writes it
     st = resolve_ptr(gathered, &gdev);
+    if (st != ZERO_OK)
+        return st;
+    st = require_device_state(in, out, d_nonfinite);
+    if (st != ZERO_OK)
+        return st;
+    const void* workspace = cb;
+    st = require_device(&workspace, 1);
     if (st != ZERO_OK)
         return st;
     const int variant = fused_variant(host_rows);

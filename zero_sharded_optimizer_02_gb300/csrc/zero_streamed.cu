@@ -146,6 +146,13 @@ extern "C" zero_status_t zero_step_shard_streamed(
     rs = resolve_ptr(gathered, &gdev);
     if (rs != ZERO_OK)
         return rs;
+    rs = require_device_state(in, out, d_nonfinite);
+    if (rs != ZERO_OK)
+        return rs;
+    const void* words[2] = {d_ready, d_status};
+    rs = require_device(words, 2);
+    if (rs != ZERO_OK)
+        return rs;
     // every kernel this call launches is loaded before its first wait starts
     preload_fused(g->dtype, host_rows);
     const StepScalars k = make_scalars(h, g->nd, loss_scale);
