@@ -305,7 +305,7 @@ zero_status_t zero_check_nonfinite(const zero_grads_t* g, uint64_t begin, uint64
  * timeout_ns must be in [1, ZERO_MAX_WAIT_NS] (ZERO_ERR_INVALID_ARG otherwise).
  * Other arguments, alignment and results as zero_step_shard (bitwise equal). */
 #define ZERO_MAX_WAIT_NS 60000000000ull
-#define ZERO_STREAM_GROUP_BYTES 500000000ull
+#define ZERO_STREAM_GROUP_BYTES 1000000000ull
 zero_status_t zero_step_shard_streamed(const zero_grads_t* g, const zero_layout_t* L,
                                        const zero_state_t* in, const zero_state_t* out,
                                        void* gathered, uint64_t gathered_offset_elems,

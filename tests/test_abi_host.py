@@ -278,13 +278,13 @@ def test_binding_constants_match_header(z):
     assert z._abi.unfused_launch_count(117_187_500, 500_000_000) == 5 + 2
     assert z._abi.unfused_launch_count(262_144, 65_536) == 4 * 3
     # bucket-ready groups: the 7.5B shard (18 GB of step traffic) keeps its 16
-    # buckets apart; the 1.5B shard (3.6 GB) deals 16 buckets into 7 groups of
-    # 3 or 2; the 8-row shard (0.65 GB) is one group; the groups tile the shard
+    # buckets apart; the 1.5B shard (3.6 GB) deals 16 buckets into 3 groups of
+    # 6, 5 and 5; the 8-row shard (0.65 GB) is one group; the groups tile the shard
     g4 = z._abi.stream_groups(117_187_500, 7_324_224, 64)
     g3 = z._abi.stream_groups(23_437_500, 1_464_848, 64)
     g1 = z._abi.stream_groups(15_554_976, 972_192, 8)
     assert len(g4) == 16 and len(g1) == 1
-    assert [round(x[1] / 1_464_848) for x in g3] == [3, 3, 2, 2, 2, 2, 2]
+    assert [round(x[1] / 1_464_848) for x in g3] == [6, 5, 5]
     for gs, n in ((g4, 117_187_500), (g3, 23_437_500), (g1, 15_554_976)):
         assert gs[0][0] == 0 and sum(x[1] for x in gs) == n
         assert all(a[0] + a[1] == b[0] for a, b in zip(gs, gs[1:]))

@@ -119,7 +119,7 @@ def fused_launch_count(n: int, bucket: int, offset: int = 0) -> int:
 
 
 # Least step traffic of a launch group of zero_step_shard_streamed (zero.h).
-ZERO_STREAM_GROUP_BYTES = 500000000
+ZERO_STREAM_GROUP_BYTES = 1000000000
 
 
 def stream_groups(n: int, bucket: int, nd: int) -> list:
