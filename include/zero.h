@@ -180,7 +180,7 @@ zero_status_t zero_gather_params_shard(const float* master, uint64_t n, void* ga
                                        void* stream);
 
 /* The fused shard step: reduce (1) + scale + AdamW (2) + cast into the
- * gathered slot (3) in one pass per bucket, with the reduced gradient kept in
+ * gathered slot (3) in one pass over the shard, with the reduced gradient kept in
  * registers (never materialised).  The shard length comes from L; the g->nd
  * contribution rows are folded.  g->nd is normally L->nd (Stage 2: one
  * contribution per rank) but need not be: under Stage 1 every rank holds the

@@ -6,9 +6,9 @@
 // during the backward pass.  Here the producer of a bucket -- in one GPU's
 // emulation, a copy stream landing the bucket's Nd contribution slices --
 // writes the bucket's ready word after its data.  The consumer is the fused
-// step itself, launched bucket by bucket on one stream, each bucket's
-// launches behind a one-thread kernel that waits for the bucket's ready
-// word.  The step kernels therefore run at their full rate on data that no
+// step itself, launched group of buckets by group on one stream, each
+// group's launches behind a one-thread kernel that waits for the group's
+// ready words.  The step kernels therefore run at their full rate on data that no
 // longer changes, and only the waits run while a bucket is in flight.
 //
 // Every wait is bounded: the waiting thread polls the word with an acquire
