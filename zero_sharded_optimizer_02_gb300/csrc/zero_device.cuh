@@ -336,6 +336,7 @@ struct FusedArgs {
     uint32_t* flag;
     const uint32_t* gate;  // if non-null and nonzero at launch, the launch does nothing
     float* cb;             // reduction-only launches: cb[e] = sum * k.inv (null: check only)
+    uint32_t early;        // 1: start at once, wait for the predecessor only at the end
 };
 
 // First instructions of every step kernel: under a programmatic dependent
@@ -346,6 +347,24 @@ __device__ __forceinline__ void pdl_entry()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// The same for a launch window after the first of one call: its elements are
+// disjoint from its predecessor's, so it starts work at once and waits for
+// the predecessor only before it ends (pdl_end).  It therefore never
+// completes before its predecessor, and a kernel that waits for it also
+// waits for every earlier window.
+__device__ __forceinline__ void pdl_begin(uint32_t early)
+{
+    if (!early)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_end(uint32_t early)
+{
+    if (early)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // True if the launch is gated off (a bucket wait before it ran out).

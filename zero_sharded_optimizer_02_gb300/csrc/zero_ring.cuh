@@ -89,8 +89,8 @@ template <int DT, int W, bool V8, int MODE = kModeStep>
 __global__ void __launch_bounds__(kRingThreads, 1) k_step_fused_ring(const FusedArgs a)
 {
     extern __shared__ uint4 ring[];
-    pdl_entry();
-    if (gated(a))
+    pdl_begin(a.early);
+    if (gated(a))           // a gate is only ever given to launches that waited at entry
         return;
     bool bad = false;
     const int t = threadIdx.x;
@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_step_fused_ring(const Fused
     }
     cp_async_wait<0>();
     flag_if_any(bad, a.flag);
+    pdl_end(a.early);
 }
 
 }  // namespace
