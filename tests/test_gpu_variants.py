@@ -134,3 +134,45 @@ def test_plain_and_programmatic_launches_agree(fused, monkeypatch):
             buf, desc = full_rows(w, dps, k, buf)
             assert not dps.step(desc)
             check_against_oracle(w, dps, hist[k], f"ZERO_PDL={pdl} fused={fused} step {k}")
+
+
+@pytest.mark.parametrize("variant", ["ring", "registers"], indirect=True)
+def test_reductions_over_two_launch_windows_match_oracle(variant):
+    """The reductions cut a long range into launch windows like the fused step
+    (the second starting as the first drains): zero_reduce_scatter_bucket over
+    30,000,002 elements of 2 bf16 rows, bit for bit against the oracle; the
+    pre-check over the same range with a +inf planted in the second window;
+    and the unfused step with one bucket of the whole shard (two reduction
+    windows, then AdamW and cast) against the oracle's shard step."""
+    from window_rule import inner_cuts
+    w = dataclasses.replace(synth.WORKLOADS["c1"], psi=60_000_005, nd=2, plant=None,
+                            bucket=1 << 30)
+    rank = 1
+    dps = make_group(w, ranks=[rank], gathered="slot", fused=False)
+    buf, desc = shard_rows(w, dps, rank, 0)
+    L = dps.layouts[rank]
+    n = int(L.length)
+    pitch = int(L.row_pitch)
+    assert inner_cuts(n) == [15_000_008]
+    inv = float(np.float32(1.0 / w.nd))
+    cb = torch.empty(n, dtype=torch.float32, device="cuda")
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    z.zero_reduce_scatter_bucket(desc[rank], 0, n, inv, cb, flag)
+    torch.cuda.synchronize()
+    host = u16(buf).reshape(-1)
+    f, ref = oracle.reduce_scaled(host, oracle.BF16, pitch, 0, n, w.nd, inv)
+    assert f == 0 and int(flag.item()) == 0
+    assert np.array_equal(cb.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    # the unfused step: two reduction windows into the fusion buffer
+    f, rp, rm, rv, rparams = oracle_shard_step(w, rank)
+    assert not dps.step(desc)
+    got = [t.cpu().numpy() for t in dps.state[rank].tensors("cur")]
+    for g, r, name, tau in zip(got, (rp, rm, rv), ("master", "m", "v"), (1e-12, 1e-20, 1e-20)):
+        assert_state_close(g, r, tau, f"unfused {name}")
+    assert_params_close(u16(dps.gathered_view(rank)[:n]), rparams, "unfused params")
+    # the pre-check sees a +inf that only the second window reads
+    buf[1, 20_000_001] = float("inf")
+    flag.zero_()
+    z.zero_check_nonfinite(desc[rank], 0, n, flag)
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 1
