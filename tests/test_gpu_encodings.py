@@ -182,3 +182,42 @@ def test_step_over_extreme_rows(dt, path, monkeypatch):
     assert_params_close(u16(gath[slot:slot + n]), params, f"{dt} {path} params")
     rest = torch.cat([gath[:slot], gath[slot + n:]])
     assert not rest.any(), "write outside the slot"
+
+
+@pytest.mark.parametrize("variant", ["ring", "registers"])
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_every_encoding_through_the_scalar_path(dt, variant, monkeypatch):
+    """Ragged heads and tails of a window are folded one element at a time
+    (widen1 / fold1), not in 8-element vectors.  Encoding i sits at element
+    8*(i // 7) + 1 + i % 7 of its row, so every 7-element block starts one
+    element past a 16-byte line; one call per block reduces the block alone,
+    all of it as the window's scalar head.  One row (the decode alone) and
+    two rows (the second rotated by 12,345), scale 1 and 1/(nd * 1024), bit
+    for bit against the oracle (NaN payloads aside)."""
+    monkeypatch.setenv("ZERO_FUSED_VARIANT", variant)
+    code = oracle.dtype_code(dt)
+    e = _all_encodings()
+    nblk = -(-e.size // 7)
+    pos = 8 * (np.arange(e.size) // 7) + 1 + np.arange(e.size) % 7
+    stride = 8 * nblk + 8
+    for nd in (1, 2):
+        host = np.zeros((nd, stride), np.uint16)
+        host[0, pos] = e
+        if nd == 2:
+            host[1, pos] = np.roll(e, 12_345)
+        dev = torch.from_numpy(host.view(np.int16)).to(DEV)
+        g = z.grads(dev, stride, 0, nd, dt)
+        for inv in (1.0, float(np.float32(1.0 / (nd * 1024.0)))):
+            cb = torch.full((stride,), -7.0, dtype=torch.float32, device=DEV)
+            flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+            for k in range(nblk):
+                b0 = 8 * k + 1
+                cnt = min(7, e.size - 7 * k)
+                z.zero_reduce_scatter_bucket(g, b0, cnt, inv, cb[b0:b0 + cnt], flag)
+            torch.cuda.synchronize()
+            f, ref = oracle.reduce_scaled(host.reshape(-1), code, stride, 0, stride, nd, inv)
+            what = f"{dt} {variant} nd={nd} inv={inv} scalar path"
+            _same_bits_or_both_nan(f32(cb)[pos], ref[pos], what)
+            assert int(flag.item()) == f == 1, what
+            gaps = np.setdiff1d(np.arange(stride), pos)
+            assert bool((f32(cb)[gaps] == -7.0).all()), f"{what}: a gap was written"
