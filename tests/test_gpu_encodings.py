@@ -221,3 +221,67 @@ def test_every_encoding_through_the_scalar_path(dt, variant, monkeypatch):
             assert int(flag.item()) == f == 1, what
             gaps = np.setdiff1d(np.arange(stride), pos)
             assert bool((f32(cb)[gaps] == -7.0).all()), f"{what}: a gap was written"
+
+
+@pytest.mark.parametrize("path", ["ring", "registers", "tma", "unfused"])
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_step_scalar_path_over_extreme_rows(dt, path, monkeypatch):
+    """The step's scalar path (a shard's last n mod 8 elements) over the
+    extreme rows: each 7-element block of them is stepped as a shard of its
+    own, so every element goes through the one-element fold, AdamW and cast.
+    Against the oracle's step of the same elements, bit for bit; the element
+    after each block is never written."""
+    if path != "unfused":
+        monkeypatch.setenv("ZERO_FUSED_VARIANT", path)
+    rows = _extreme_rows(dt)
+    nd, cnt_all = rows.shape
+    nblk = -(-cnt_all // 7)
+    stride = 8 * nblk
+    i = np.arange(cnt_all)
+    pos = 8 * (i // 7) + i % 7
+    host = np.zeros((nd, stride), np.uint16)
+    host[:, pos] = rows
+    ls = 1024.0 if dt == "f16" else 1.0
+    t = 3
+    code = oracle.dtype_code(dt)
+    rng = np.random.default_rng(cnt_all + 1)
+    p = (rng.standard_normal(stride) * 0.02).astype(np.float32)
+    m = (rng.standard_normal(stride) * 1e-4).astype(np.float32)
+    v = np.abs(rng.standard_normal(stride) * 1e-6).astype(np.float32)
+    params = np.zeros(stride, np.uint16)
+    f, rp, rm, rv = oracle.step_rank(host.reshape(-1), stride, 0, stride, nd, code, 4096, ls, H,
+                                     t, p, m, v, params, 0)
+    assert f == 0
+    dev = torch.from_numpy(host.view(np.int16)).to(DEV)
+    st_in = torch.from_numpy(np.stack([p, m, v])).to(DEV)
+    st_out = torch.full((3, stride), -5.0, dtype=torch.float32, device=DEV)
+    gath = torch.zeros(stride + 8, dtype=torch.int16, device=DEV)
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    cb = torch.empty(16, dtype=torch.float32, device=DEV)
+    h = z.adamw(H["lr"], H["beta1"], H["beta2"], H["eps"], H["weight_decay"], t)
+    for k in range(nblk):
+        b0 = 8 * k
+        cnt = min(7, cnt_all - 7 * k)
+        L = z.zero_partition_layout(cnt, 1, 0, 8)
+        g = z.grads(dev, stride, b0, nd, dt)
+        s_in = z.state(st_in[0, b0:], st_in[1, b0:], st_in[2, b0:])
+        s_out = z.state(st_out[0, b0:], st_out[1, b0:], st_out[2, b0:])
+        if path == "unfused":
+            z.zero_step_shard_unfused(g, L, s_in, s_out, gath, b0, 4096, ls, h, cb, cb.numel(),
+                                      flag)
+        else:
+            z.zero_step_shard(g, L, s_in, s_out, gath, b0, 4096, ls, h, flag)
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 0
+    for k, (ref, name, tau) in enumerate(((rp, "master", 1e-12), (rm, "m", 1e-20),
+                                          (rv, "v", 1e-20))):
+        got = f32(st_out[k])[pos]
+        r = ref[pos]
+        if name == "v":
+            inf = np.isinf(r)
+            assert np.array_equal(np.isinf(got), inf), f"{dt} {path} v: inf positions"
+            got, r = got[~inf], r[~inf]
+        assert_state_close(got, r, tau, f"{dt} {path} {name} (scalar path)")
+    assert_params_close(u16(gath[:stride])[pos], params[pos], f"{dt} {path} params (scalar path)")
+    gaps = np.setdiff1d(np.arange(stride), pos)
+    assert bool((f32(st_out)[:, gaps] == -5.0).all()), "an element after a block was written"
