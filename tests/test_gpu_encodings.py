@@ -17,9 +17,12 @@ kernels' decode and rank-ordered fp32 fold:
 The reduced, scaled sums must equal the oracle's bit for bit, except that a
 NaN may carry any payload (the GPU's arithmetic returns its canonical NaN);
 the nonfinite flag must agree.  The scale is 1 and 1/(nd * 1024), so scaled
-subnormal sums are rounded too.  Then one whole shard step runs over rows
-that hold subnormals and +-max finite values (and no nonfinite sum) on every
-kernel variant and on the unfused path, against the oracle's shard step.
+subnormal sums are rounded too.  The same runs through the kernels'
+one-element path (a window's ragged head), which decodes separately.  Then
+the step runs over rows that hold subnormals and +-max finite values (and no
+nonfinite sum) on every kernel variant and on the unfused path, against the
+oracle's shard step: once as one shard (the 8-element path) and once with
+every 7-element block as a shard of its own (the one-element path).
 """
 import numpy as np
 import pytest
