@@ -189,9 +189,11 @@ zero_status_t zero_gather_params_shard(const float* master, uint64_t n, void* ga
  * in registers, so no bucket is ever materialised and the bucket is no
  * boundary of the work: bucket_elems (>= 1) is validated but the whole shard
  * runs as the fewest equal launches of at most ZERO_FUSED_WINDOW_ELEMS
- * elements (kernel boundaries keep every SM at the same place in the rows;
- * single launches much longer than this read several percent more DRAM than
- * the data).  Results depend on neither size.
+ * elements, every cut on a 32-byte boundary of row 0 at the address the
+ * device reads it (kernel boundaries keep every SM at the same place in the
+ * rows; launches much longer than this let the SMs drift apart, and a cut
+ * inside a 32-byte sector slows every launch after it).  A window after the
+ * first starts as its predecessor drains.  Results depend on neither size.
  * The kernel is the cp.async-ring variant unless the environment variable
  * ZERO_FUSED_VARIANT, read at each call, names another ("registers", "ring"
  * or "tma": bulk copies and mbarriers); rows in host memory always use the
@@ -219,7 +221,7 @@ zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layout_t* L,
 #define ZERO_STEP_FLAG_WAIT_TIMEOUT 0x80000000u
 
 /* Longest launch window of the fused step, in elements (see zero_step_shard). */
-#define ZERO_FUSED_WINDOW_ELEMS 25165824ull
+#define ZERO_FUSED_WINDOW_ELEMS 10485760ull
 
 /* The same step unfused, through the constant-size fusion buffer: per bucket,
  * zero_reduce_scatter_bucket into cb (in the fused step's launch windows),

@@ -142,8 +142,8 @@ def sample_indices(psi: int, nd: int, ranks, per_rank: int, seed: int, extra=())
     """Flat indices: each rank's first/last elements, neighbours of every
     8-element boundary near the ends, the 16 elements on each side of every
     cut between two launch windows of the fused step (shards longer than one
-    window; the rows of every test start on a 16-byte boundary), random
-    interior points, and ``extra``."""
+    window, rows starting on a 32-byte boundary as in every sampled test),
+    random interior points, and ``extra``."""
     rng = np.random.default_rng(seed)
     s = -(-psi // nd)
     out = set(int(e) for e in extra)

@@ -267,15 +267,15 @@ def test_binding_constants_match_header(z):
     with pytest.raises(z.ZeroError) as e:
         z._abi.check_step_flag(-(1 << 31) | 1)      # as an int32 read back from the device
     assert e.value.status == z.ZERO_ERR_TIMEOUT
-    assert z._abi.fused_launch_count(117_187_500, 500_000_000) == 5
-    assert z._abi.fused_launch_count(23_437_500, 50_000_000) == 1
+    assert z._abi.fused_launch_count(117_187_500, 500_000_000) == 12
+    assert z._abi.fused_launch_count(23_437_500, 50_000_000) == 3
     # the fused step plans its windows over the whole shard: the bucket size
     # does not add launches (the 4-rank workload's 4 buckets are one launch)
     assert z._abi.fused_launch_count(16, 1) == 1 and z._abi.fused_launch_count(0, 8) == 0
     assert z._abi.fused_launch_count(262_144, 65_536) == 1
-    assert z._abi.fused_launch_count(117_187_500, 7) == 5
+    assert z._abi.fused_launch_count(117_187_500, 7) == 12
     # unfused: the reduction in the same windows, plus AdamW and cast, per bucket
-    assert z._abi.unfused_launch_count(117_187_500, 500_000_000) == 5 + 2
+    assert z._abi.unfused_launch_count(117_187_500, 500_000_000) == 12 + 2
     assert z._abi.unfused_launch_count(262_144, 65_536) == 4 * 3
     # bucket-ready groups: the 7.5B shard (18 GB of step traffic) keeps its 16
     # buckets apart; the 1.5B shard (3.6 GB) deals 16 buckets into 3 groups of
@@ -299,7 +299,7 @@ def test_binding_constants_match_header(z):
 
 def _window_cuts(length: int, phase: int):
     from window_rule import window_cuts
-    assert z_abi().ZERO_FUSED_WINDOW_ELEMS == 25165824
+    assert z_abi().ZERO_FUSED_WINDOW_ELEMS == 10485760
     return window_cuts(length, phase)
 
 
@@ -312,21 +312,22 @@ def test_launch_windows_properties():
     import random
     rng = random.Random(7)
     W = z_abi().ZERO_FUSED_WINDOW_ELEMS
-    cases = [(117_187_500, 0), (23_437_500, 4), (25_165_824, 0), (25_165_825, 3),
+    cases = [(117_187_500, 0), (23_437_500, 4), (10_485_760, 0), (10_485_761, 3),
+             (25_165_824, 8), (25_165_825, 11), (2 ** 31 + 9, 0),
              (50_331_648 + 63, 5), (64, 7), (1, 0)]
-    cases += [(rng.randrange(1, 400_000_000), rng.randrange(8)) for _ in range(300)]
+    cases += [(rng.randrange(1, 400_000_000), rng.randrange(16)) for _ in range(300)]
     for length, phase in cases:
         cuts = _window_cuts(length, phase)
         # they tile the bucket in order
         assert cuts[0][0] == 0 and cuts[-1][1] == length
         assert all(a[1] == b[0] for a, b in zip(cuts, cuts[1:]))
-        # every inner cut falls on a 16-byte boundary of the rows
-        assert all((phase + c[0]) % 8 == 0 for c in cuts[1:])
+        # every inner cut falls on a 32-byte (one L2 sector) boundary of the rows
+        assert all((phase + c[0]) % 16 == 0 for c in cuts[1:])
         # the fewest windows (a remainder under 64 may join the last one), each
-        # at most one window plus such a remainder
+        # at most one window, the row phase and such a remainder
         nwin = -(-length // W)
         assert len(cuts) in (nwin, max(nwin - 1, 1))
-        assert all(c[1] - c[0] <= W + 63 for c in cuts)
+        assert all(c[1] - c[0] <= W + 15 + 63 for c in cuts)
         # and the binding's launch count is exactly this split
         assert z_abi()._windows(length, phase) == len(cuts)
 

@@ -82,7 +82,7 @@ def test_gpu_arm_line():
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] > 0
     assert r["frac"] == pytest.approx(r["achieved"] / r["peak"], rel=1e-9)
     per_step = _abi.fused_launch_count(n, 50_000_000, 0)
-    assert r["launches_per_step"] == per_step == 1
+    assert r["launches_per_step"] == per_step == 2
     assert r["algorithmic_bytes_per_launch"] == (2 * 8 + 26) * n / per_step
     # the read-only ceiling over the same rows is measured beside the copy peak
     assert r["read_ceiling_gbs"] > 0
@@ -96,7 +96,7 @@ def test_gpu_arm_line():
         assert v["skipped"] is False and v["kernel_ms_per_step"] > 0
         assert v["frac"] == pytest.approx(v["achieved"] / r["peak"])
     assert pc["c3 rank 0"]["shard_params"] == 23_437_500
-    assert pc["c3 rank 0"]["launches_per_step"] == 1 and "l2" in pc["c0 rank 0"]
+    assert pc["c3 rank 0"]["launches_per_step"] == 3 and "l2" in pc["c0 rank 0"]
     # the timed region launches exactly one fused step per timed step
     assert d["gpu_launches"] == 6 * per_step
     e = d["e2e"]
@@ -156,6 +156,8 @@ def test_gpu_arm_two_processes():
     assert d["n_gpus"] == 2 and d["scaling"] == "weak"
     assert d["value"] == pytest.approx(2 * n / (d["ms_per_step"] * 1e-3), rel=1e-9)
     assert d["config"]["rank"] == 0 and d["skipped_steps"] == 0
-    assert d["gpu_launches"] == 2 * 6          # both processes' launches
+    from zero_sharded_optimizer_02_gb300 import _abi
+    per_step = _abi.fused_launch_count(n, 50_000_000, 0)
+    assert d["gpu_launches"] == 2 * 6 * per_step     # both processes' launches
     assert d["e2e"]["value"] > 0
     assert "cpu_baseline" not in d             # the host-core baseline is timed at N = 1 only

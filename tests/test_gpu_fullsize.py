@@ -4,7 +4,7 @@ any element on its own from the seeded generator) and through properties that
 hold at any size (padding untouched, skip decisions, step count).
 
 Samples include the 16 elements on each side of every cut between two launch
-windows of the fused step (the 7.5B shard runs as 5 windows).
+windows of the fused step (the 7.5B shard runs as 12 windows).
 
 Workloads: GPT-2-small-sized ZeRO-2 shard (psi = 124,439,808, Nd = 8, bf16,
 10 steps); padding and overflow (psi = 350,000,017, Nd = 16, fp16 x 1024,
@@ -192,7 +192,7 @@ def test_c3_end_to_end_forms_sampled(form):
 def test_shard_past_the_int32_range():
     """Rank 1 of two holds 2,147,483,657 elements (2^31 + 9, bf16): every
     element index of the second half is past the int32 range and its flat
-    indices pass 2^32; the fused step runs it as 86 launch windows.  Two
+    indices pass 2^32; the fused step runs it as 205 launch windows.  Two
     steps, sampled against the oracle at both ends, around every window cut
     and at random points; the state past the shard stays zero.  About 70 GB
     on the device."""
@@ -202,7 +202,7 @@ def test_shard_past_the_int32_range():
     rank = 1
     dps = make_group(w, ranks=[rank], gathered="slot")
     assert int(dps.layouts[rank].length) == n
-    assert z.fused_launch_count(n, w.bucket) == 86
+    assert z.fused_launch_count(n, w.bucket) == 205
     idx = sample_indices(w.psi, w.nd, [rank], 4096, seed=31,
                          extra=[n + 2 ** 31 - 1, n + 2 ** 31, n + 2 ** 32 - n])
     _, hist = oracle_trajectory(w, idx, 2)

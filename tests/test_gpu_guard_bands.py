@@ -4,8 +4,9 @@ Every output buffer (new state, gathered parameters, fusion buffer, flag,
 gather destination) is carved out of a larger allocation with 4 KiB canary
 bands of a fixed byte pattern before and after it.  The entry points run on
 ragged shards (lengths not a multiple of 8, slots off a 16-byte boundary):
-one of 20,004 elements in buckets of 6,001, and one of 25,165,898 elements,
-which the fused step runs as two launch windows.  The bands must come back
+one of 20,004 elements in buckets of 6,001, and one of 25,165,890 elements,
+which the fused step runs as three launch windows whose rows start half a
+32-byte sector in (the cuts move by that phase).  The bands must come back
 byte for byte.
 """
 import dataclasses
@@ -59,13 +60,15 @@ def _guarded_state(n):
 # (psi, nd, rank, bucket):
 #  - psi = 64 * 20003 + 5: shards of 20,004 (S mod 8 = 4); rank 3's slot in a
 #    flat buffer starts 8 bytes past a 16-byte boundary; buckets of 6,001;
-#  - S = 25,165,901 over 2 ranks: rank 1 holds 25,165,898 elements (two launch
-#    windows of the fused step), its slot starts 10 bytes past a 16-byte
+#  - S = 25,165,893 over 2 ranks: rank 1 holds 25,165,890 elements (three launch
+#    windows of the fused step); the row pitch is 8 elements past a multiple of
+#    16, so rank 1's rows start 16 bytes into a 32-byte sector and the window
+#    cuts shift by 8 elements; its slot starts 10 bytes past a 16-byte
 #    boundary; buckets of 4,194,304.
-SHAPES = [(64 * 20_003 + 5, 64, 3, 6_001), (2 * 25_165_901 - 3, 2, 1, 1 << 22)]
+SHAPES = [(64 * 20_003 + 5, 64, 3, 6_001), (2 * 25_165_893 - 3, 2, 1, 1 << 22)]
 
 
-@pytest.mark.parametrize("shape", SHAPES, ids=["64 ranks", "two launch windows"])
+@pytest.mark.parametrize("shape", SHAPES, ids=["64 ranks", "three launch windows"])
 @pytest.mark.parametrize("path", ["ring", "registers", "tma", "unfused", "streamed"])
 def test_step_paths_stay_inside_their_buffers(path, shape, monkeypatch):
     psi, nd, rank, bucket = shape
@@ -77,7 +80,7 @@ def test_step_paths_stay_inside_their_buffers(path, shape, monkeypatch):
     buf, desc = full_rows(w, dps, 0)
     L = dps.layouts[rank]
     n = int(L.length)
-    assert z.fused_launch_count(n, bucket) == (2 if nd == 2 else 1)
+    assert z.fused_launch_count(n, bucket) == (3 if nd == 2 else 1)
     st = dps.state[rank]
     outs, s_out = _guarded_state(n)
     gath = Guarded(n, torch.bfloat16, phase=int(L.begin) % 8)

@@ -6,7 +6,7 @@ the kernel for host-resident rows) or the bulk-copy kernel ("tma": a
 producer warp, mbarrier-tracked cp.async.bulk copies of rows and state).
 Each is checked here on the same cases as the default: the 4-rank workload
 against the oracle, ragged shapes and every slot phase, a global skip, and
-whole shards of two launch windows against the oracle.
+whole shards of several launch windows against the oracle.
 """
 import dataclasses
 
@@ -87,19 +87,19 @@ def test_global_skip(variant):
     assert dps.t == 1 and int(dps.flag.item()) == 0
 
 
-def test_two_launch_windows_match_oracle_on_every_variant(monkeypatch):
+def test_several_launch_windows_match_oracle_on_every_variant(monkeypatch):
     """Whole shards against the oracle, element by element, on every variant:
-    rank 1 of psi = 60,000,005 over 2 bf16 rows (30,000,002 elements, two
-    launch windows cut at element 15,000,008) and rank 5 of a 64-row fp16
-    shard of 1,000,003 elements.  The bulk-copy kernel runs twice (a race
+    rank 1 of psi = 60,000,005 over 2 bf16 rows (30,000,002 elements, three
+    launch windows cut at elements 10,000,016 and 20,000,032) and rank 5 of a
+    64-row fp16 shard of 1,000,003 elements.  The bulk-copy kernel runs twice (a race
     would vary between runs)."""
     from window_rule import inner_cuts
     cases = [(dataclasses.replace(synth.WORKLOADS["c1"], psi=60_000_005, nd=2, plant=None,
                                   bucket=1 << 30), 1),
              (dataclasses.replace(synth.WORKLOADS["c3"], psi=64 * 1_000_003, plant=None,
                                   bucket=1 << 30), 5)]
-    assert z.fused_launch_count(30_000_002, 1 << 30) == 2
-    assert inner_cuts(30_000_002) == [15_000_008]
+    assert z.fused_launch_count(30_000_002, 1 << 30) == 3
+    assert inner_cuts(30_000_002) == [10_000_016, 20_000_032]
     for w, rank in cases:
         f, rp, rm, rv, rparams = oracle_shard_step(w, rank)
         assert f == 0
@@ -137,13 +137,14 @@ def test_plain_and_programmatic_launches_agree(fused, monkeypatch):
 
 
 @pytest.mark.parametrize("variant", ["ring", "registers"], indirect=True)
-def test_reductions_over_two_launch_windows_match_oracle(variant):
+def test_reductions_over_several_launch_windows_match_oracle(variant):
     """The reductions cut a long range into launch windows like the fused step
-    (the second starting as the first drains): zero_reduce_scatter_bucket over
-    30,000,002 elements of 2 bf16 rows, bit for bit against the oracle; the
-    pre-check over the same range with a +inf planted in the second window;
-    and the unfused step with one bucket of the whole shard (two reduction
-    windows, then AdamW and cast) against the oracle's shard step."""
+    (each after the first starting as its predecessor drains):
+    zero_reduce_scatter_bucket over 30,000,002 elements of 2 bf16 rows (three
+    windows), bit for bit against the oracle; the pre-check over the same
+    range with a +inf planted in the second window; and the unfused step with
+    one bucket of the whole shard (three reduction windows, then AdamW and
+    cast) against the oracle's shard step."""
     from window_rule import inner_cuts
     w = dataclasses.replace(synth.WORKLOADS["c1"], psi=60_000_005, nd=2, plant=None,
                             bucket=1 << 30)
@@ -153,7 +154,7 @@ def test_reductions_over_two_launch_windows_match_oracle(variant):
     L = dps.layouts[rank]
     n = int(L.length)
     pitch = int(L.row_pitch)
-    assert inner_cuts(n) == [15_000_008]
+    assert inner_cuts(n) == [10_000_016, 20_000_032]
     inv = float(np.float32(1.0 / w.nd))
     cb = torch.empty(n, dtype=torch.float32, device="cuda")
     flag = torch.zeros(1, dtype=torch.int32, device="cuda")

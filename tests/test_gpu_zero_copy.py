@@ -64,12 +64,12 @@ def test_host_rows_match_the_oracle(fused):
 
 
 def test_host_rows_over_several_launch_windows_match_oracle():
-    """A 30,000,003-element shard (two launch windows of the fused step),
+    """A 30,000,003-element shard (three launch windows of the fused step),
     Nd = 2 bf16: host-resident and device-resident contributions each give
     the oracle's state and parameters over the whole shard."""
     w = dataclasses.replace(synth.WORKLOADS["c1"], psi=60_000_005, nd=2, plant=None,
                             bucket=1 << 30)
-    assert z.fused_launch_count(30_000_003, 1 << 30) == 2
+    assert z.fused_launch_count(30_000_003, 1 << 30) == 3
     f, rp, rm, rv, rparams = oracle_shard_step(w, 0)
     assert f == 0
     for where in ("device", "host"):

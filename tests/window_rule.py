@@ -1,11 +1,12 @@
 """The fused step's launch-window split, restated from include/zero.h for the
 tests: the fewest equal windows of at most ZERO_FUSED_WINDOW_ELEMS elements
-over a shard, every inner cut on an 8-element boundary of the rows (rows
-whose element 0 sits `phase` elements past a 16-byte boundary), and a
-remainder of under 64 elements joined to the last window.  Used to put
-sampled oracle checks on every cut, and to pin the binding's launch count."""
+over a shard, every inner cut on a 16-element (32-byte) boundary of row 0
+(whose element 0 sits `phase` elements past a 32-byte boundary: its offset in
+the row, for the 32-byte aligned torch buffers of the tests), and a remainder
+of under 64 elements joined to the last window.  Used to put sampled oracle
+checks on every cut, and to pin the binding's launch count."""
 
-WINDOW_ELEMS = 25165824   # ZERO_FUSED_WINDOW_ELEMS
+WINDOW_ELEMS = 10485760   # ZERO_FUSED_WINDOW_ELEMS
 
 
 def window_cuts(length: int, phase: int = 0, window: int = WINDOW_ELEMS):
@@ -13,8 +14,8 @@ def window_cuts(length: int, phase: int = 0, window: int = WINDOW_ELEMS):
     if length <= 0:
         return []
     nwin = -(-length // window)
-    target = -(-(-(-length // nwin)) // 8) * 8
-    cuts, w0, cut = [], 0, target - (phase & 7)
+    target = -(-(-(-length // nwin)) // 16) * 16
+    cuts, w0, cut = [], 0, target - (phase & 15)
     while w0 < length:
         w1 = min(cut, length)
         if length - w1 < 64:

@@ -91,14 +91,16 @@ _SIGNATURES = {
 ZERO_MAX_ND = 1 << 24
 
 # Longest launch window of the fused step (include/zero.h).
-ZERO_FUSED_WINDOW_ELEMS = 25165824
+ZERO_FUSED_WINDOW_ELEMS = 10485760
 
 
 def _windows(length: int, phase: int) -> int:
-    """Launch windows of one bucket (the library's split, see zero.h)."""
+    """Launch windows of one range (the library's split, see zero.h); `phase`
+    is row 0's element offset past a 32-byte boundary (its element offset
+    within the row when the rows' base is 32-byte aligned, as torch's are)."""
     nwin = -(-length // ZERO_FUSED_WINDOW_ELEMS)
-    target = -(-(-(-length // nwin)) // 8) * 8
-    cut, w0, count = target - (phase & 7), 0, 0
+    target = -(-(-(-length // nwin)) // 16) * 16
+    cut, w0, count = target - (phase & 15), 0, 0
     while w0 < length:
         w1 = min(cut, length)
         if length - w1 < 64:

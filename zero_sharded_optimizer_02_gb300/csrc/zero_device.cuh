@@ -496,17 +496,17 @@ __device__ __forceinline__ bool fused_epilogue_loaded(const FusedArgs& a, uint64
 }
 
 // Calls fn(w0, w1) for the fewest equal launch windows of at most
-// max_window elements (a multiple of 8) covering [0, len) of a bucket whose
-// rows' element 0 has phase `phase` (elements past a 16-byte boundary): every
-// cut falls on an 8-element boundary of the rows, and a remainder of under
-// 64 elements joins the last window.  Stops at the first status other than
-// ZERO_OK.
+// max_window elements (a multiple of 16) covering [0, len) of a range whose
+// rows' element 0 has phase `phase` (elements past a 32-byte boundary): every
+// cut falls on a 16-element (32-byte, one L2 sector) boundary of the rows, and
+// a remainder of under 64 elements joins the last window.  Stops at the
+// first status other than ZERO_OK.
 template <typename F>
 zero_status_t for_each_window(uint64_t phase, uint64_t len, uint64_t max_window, F&& fn)
 {
     const uint64_t nwin = (len + max_window - 1) / max_window;
-    const uint64_t target = ((len + nwin - 1) / nwin + 7) / 8 * 8;
-    uint64_t cut = target - (phase & 7);
+    const uint64_t target = ((len + nwin - 1) / nwin + 15) / 16 * 16;
+    uint64_t cut = target - (phase & 15);
     for (uint64_t w0 = 0; w0 < len; cut += target) {
         uint64_t w1 = cut < len ? cut : len;
         if (len - w1 < 64)

@@ -129,7 +129,7 @@ constexpr int kCtasPerSmLight = 8;
 #define ZERO_WINDOW_ELEMS ZERO_FUSED_WINDOW_ELEMS
 #endif
 constexpr uint64_t kWindow = ZERO_WINDOW_ELEMS;
-static_assert(kWindow % 8 == 0 && kWindow >= 64, "window must be a multiple of 8");
+static_assert(kWindow % 16 == 0 && kWindow >= 64, "window must be a multiple of 16");
 
 // Fused step, bulk-copy variant (ZERO_FUSED_IMPL 2): a producer warp streams
 // each tile's fp32 state (master, m, v) into a 2-slot ring and its rank rows
@@ -551,6 +551,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSmLight) k_cast(const CastAr
 // ---------------------------------------------------------------------------
 
 bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+// 2-byte elements from the last 32-byte boundary to p: the phase for which
+// for_each_window puts every cut on a 32-byte sector boundary of the row.
+uint64_t elem_phase(const uint16_t* p) { return ((uintptr_t)p & 31) / 2; }
 
 // Widest store (16/8/4/2 bytes) that a 16-bit element address allows.
 int store_width(const void* p)
@@ -1008,7 +1012,7 @@ zero_status_t launch_fused_range(const uint16_t* rows, const zero_grads_t* g,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const float* const sp[6] = {in->master, in->m, in->v, out->master, out->m, out->v};
     const bool v8 = state_v8_ok(sp);
-    return for_each_window(g->offset + b0, len, kWindow, [&](uint64_t w0, uint64_t w1) {
+    return for_each_window(elem_phase(rows + b0), len, kWindow, [&](uint64_t w0, uint64_t w1) {
         const uint64_t e0 = b0 + w0;
         FusedArgs a{rows + e0, g->row_stride, g->nd, split_window(g->offset + e0, w1 - w0),
                     in->master + e0, in->m + e0, in->v + e0, out->master + e0, out->m + e0,
@@ -1056,7 +1060,7 @@ extern "C" zero_status_t zero_reduce_scatter_bucket(const zero_grads_t* g, uint6
         return st;
     const int variant = fused_variant(host_rows);
     const uint16_t* first = static_cast<const uint16_t*>(gr.base) + g->offset + bucket_begin;
-    return for_each_window(g->offset + bucket_begin, bucket_len, kWindow,
+    return for_each_window(elem_phase(first), bucket_len, kWindow,
                            [&](uint64_t w0, uint64_t w1) {
         ReduceArgs a{first + w0, g->row_stride, g->nd,
                      split_window(g->offset + bucket_begin + w0, w1 - w0), inv_scale, cb_out + w0,
@@ -1089,7 +1093,7 @@ extern "C" zero_status_t zero_check_nonfinite(const zero_grads_t* g, uint64_t be
         return st;
     const int variant = fused_variant(host_rows);
     const uint16_t* first = static_cast<const uint16_t*>(gr.base) + g->offset + begin;
-    return for_each_window(g->offset + begin, n, kWindow, [&](uint64_t w0, uint64_t w1) {
+    return for_each_window(elem_phase(first), n, kWindow, [&](uint64_t w0, uint64_t w1) {
         ReduceArgs a{first + w0, g->row_stride, g->nd, split_window(g->offset + begin + w0, w1 - w0),
                      1.0f, nullptr, d_nonfinite, (uint32_t)(w0 > 0)};
         launch_reduce(a, g->dtype, variant, static_cast<cudaStream_t>(stream));
@@ -1232,7 +1236,7 @@ extern "C" zero_status_t zero_step_shard_unfused(const zero_grads_t* g, const ze
         // phase and the optimizer pass runs on float4s.
         float* cbb = cb + (b0 & 3);
         // the reduction in launch windows, like the fused step
-        st = for_each_window(g->offset + b0, len, kWindow, [&](uint64_t w0, uint64_t w1) {
+        st = for_each_window(elem_phase(rows + b0), len, kWindow, [&](uint64_t w0, uint64_t w1) {
             ReduceArgs r{rows + b0 + w0, g->row_stride, g->nd,
                          split_window(g->offset + b0 + w0, w1 - w0), k.inv, cbb + w0,
                          d_nonfinite, (uint32_t)(w0 > 0)};
