@@ -704,11 +704,15 @@ void smem_opt_in(F* fn, size_t bytes, std::atomic<uint64_t>& done)
 // the environment, read at each call): the next launch in the stream is
 // scheduled while this one's last CTAs drain, and waits in the kernel (not
 // at the launch) for its predecessor's results.  Consecutive windows and
-// steps lose their launch gap: +2% on the 7.5B shard's 5-launch step.  A
-// window after the first of one call works on elements disjoint from its
+// steps lose their launch gap: +2% on the 7.5B shard's step.  A window
+// after the first of one call works on elements disjoint from its
 // predecessor's, so it waits for the predecessor only before it ends
 // (pdl_begin / pdl_end with FusedArgs::early): its CTAs start as the
-// previous window's drain, another +0.7% on that step.
+// previous window drains, another +0.7% on that step.  Behind a bucket-ready
+// wait this still holds: the first window waits at entry for the wait
+// kernel, and a later window is scheduled only after every CTA of the first
+// has passed that wait, so the wait has completed (and its status word is
+// written) before a later window reads its gate.
 bool pdl_enabled()
 {
     const char* v = getenv("ZERO_PDL");
@@ -1017,7 +1021,7 @@ zero_status_t launch_fused_range(const uint16_t* rows, const zero_grads_t* g,
         FusedArgs a{rows + e0, g->row_stride, g->nd, split_window(g->offset + e0, w1 - w0),
                     in->master + e0, in->m + e0, in->v + e0, out->master + e0, out->m + e0,
                     out->v + e0, gath + e0, k, d_nonfinite, gate, nullptr,
-                    (uint32_t)(w0 > 0 && gate == nullptr)};
+                    (uint32_t)(w0 > 0)};
         const int width = store_width(gath + e0 + a.sp.head);
         if (g->dtype == ZERO_F16)
             launch_fused_dt<ZERO_F16>(a, width, v8, variant, s);
