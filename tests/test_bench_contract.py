@@ -61,8 +61,9 @@ def _gpu_arm_config(key: str, rank: int, world: int = 1) -> dict:
 
 def test_config_block_of_the_default_workload():
     c = _gpu_arm_config("c4", 0)
+    # rows at a 512-element (1 KB) pitch
     assert (c["psi"], c["nd"], c["shard_params"], c["row_stride_elems"]) == \
-        (7_500_000_000, 64, 117_187_500, 117_187_504)
+        (7_500_000_000, 64, 117_187_500, 117_187_584)
     assert c["grad_dtype"] == "bf16" and c["bucket"] == 500_000_000
     assert c["l2"].startswith("inputs larger than L2 (18.0 GB per step)")
     assert _gpu_arm_config("c0", 0)["l2"].startswith("inputs L2-resident")

@@ -72,10 +72,12 @@ def _check(dps, idx, entry, what):
 
 
 def _bench_driver(w, rank):
-    """The driver configuration bench.py times: PipelinedStep, slot buffers."""
+    """The driver configuration bench.py times: PipelinedStep, slot buffers,
+    the benchmark's row pitch."""
+    from bench import ROW_ALIGN
     from zero_sharded_optimizer_02_gb300.step import PipelinedStep
     dps = PipelinedStep(w.psi, w.nd, [rank], w.grad_dtype, w.hparams, w.loss_scale, w.bucket,
-                        "cuda", gathered="slot")
+                        "cuda", gathered="slot", row_align=ROW_ALIGN)
     st = dps.state[rank]
     for row, which in zip(st.bufs[st.cur], ("master", "m", "v")):
         synth.fill_shard_state(w, rank, which, row)
