@@ -112,6 +112,11 @@ class DataParallelStep:
                  the kernels write the cast parameters there in place over
                  the host link, so they reach the host with no copy of
                  their own
+    row_align    the row pitch of the layouts (and of the state rows) is S
+                 rounded up to this many elements: 8, the default, is the
+                 least the kernels accept; 512 puts every 2-byte gradient
+                 row on a 1 KB boundary, which streams faster when the
+                 shard's own pitch leaves rows only 32-byte aligned
     """
 
     def __init__(self, psi: int, nd: int, ranks, grad_dtype: str, hparams: dict,
