@@ -123,8 +123,9 @@ constexpr int kCtasPerSmLight = 8;
 #ifndef ZERO_FUSED_IMPL
 #define ZERO_FUSED_IMPL 1
 #endif
-// Longest launch window of the fused step (elements, a multiple of 8; a
-// window can exceed it by under 64 elements when a range's remainder joins it).
+// Longest launch window of the fused step (elements, a multiple of 16; a
+// window can exceed it by the rows' phase within a 32-byte sector plus under
+// 64 elements when a range's remainder joins it).
 #ifndef ZERO_WINDOW_ELEMS
 #define ZERO_WINDOW_ELEMS ZERO_FUSED_WINDOW_ELEMS
 #endif
