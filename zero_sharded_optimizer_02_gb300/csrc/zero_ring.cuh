@@ -90,7 +90,11 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_step_fused_ring(const Fused
 {
     extern __shared__ uint4 ring[];
     pdl_begin(a.early);
-    if (gated(a))           // a gate is only ever given to launches that waited at entry
+    // Gated off: a bucket wait of this call ran out.  Only a wait sets the
+    // gate, and every window of a group runs after the group's wait, so
+    // either all of the group's windows see it set and write nothing, or none
+    // does; returning without the end wait of an early window is then safe.
+    if (gated(a))
         return;
     bool bad = false;
     const int t = threadIdx.x;
