@@ -174,7 +174,7 @@ template <int DT, int W, bool V8>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_step_fused(const FusedArgs a)
 {
     pdl_begin(a.early);
-    if (gated(a))
+    if (gated(a))   // all of a group's windows see the gate alike (see k_step_fused_ring)
         return;
     bool bad = false;
     const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
