@@ -248,8 +248,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_step_fused_tma(const FusedAr
     const float* slots =                                              // [slot][array][consumer][8]
         reinterpret_cast<const float*>(tma_smem + kTmaStages * kTmaStageBytes);
     uint64_t* bars = reinterpret_cast<uint64_t*>(tma_smem + kTmaBarOffset);
-    pdl_entry();
-    if (gated(a))                       // uniform: every thread returns before any barrier
+    pdl_begin(a.early);
+    // uniform: every thread returns before any barrier; all of a group's
+    // windows see the gate alike (see k_step_fused_ring)
+    if (gated(a))
         return;
     const uint32_t full0 = smem_u32(bars);                                    // + 8 s
     const uint32_t empty0 = smem_u32(bars + kTmaStages);                      // + 8 s
@@ -335,6 +337,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_step_fused_tma(const FusedAr
                 if ((sarmed >> s) & 1)
                     (void)mbar_wait(sfull0 + 8 * s, (sarmed_parity >> s) & 1, kTmaDrainNs);
         }
+        pdl_end(a.early);
         return;
     }
 
@@ -403,6 +406,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_step_fused_tma(const FusedAr
     if (!ok)
         atomicOr(a.flag, ZERO_STEP_FLAG_WAIT_TIMEOUT);
     flag_if_any(bad, a.flag);
+    pdl_end(a.early);   // the producer and the consumers wait; the CTA outlives neither
 }
 
 struct ReduceArgs {
