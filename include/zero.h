@@ -188,9 +188,10 @@ zero_status_t zero_gather_params_shard(const float* master, uint64_t n, void* ga
  * passes loss_scale * Nd to keep the 1/Nd averaging.  The reduced sums stay
  * in registers, so no bucket is ever materialised and the bucket is no
  * boundary of the work: bucket_elems (>= 1) is validated but the whole shard
- * runs as the fewest equal launches of at most ZERO_FUSED_WINDOW_ELEMS
- * elements, every cut on a 32-byte boundary of row 0 at the address the
- * device reads it (kernel boundaries keep every SM at the same place in the
+ * runs as ceil(n / ZERO_FUSED_WINDOW_ELEMS) launches of about equal length,
+ * every cut on a 32-byte boundary of row 0 at the address the device reads
+ * it (moving the cuts back to those boundaries shortens the first window and
+ * can lengthen the last to ZERO_FUSED_WINDOW_ELEMS + 15 elements) (kernel boundaries keep every SM at the same place in the
  * rows; launches much longer than this let the SMs drift apart, and a cut
  * inside a 32-byte sector slows every launch after it).  A window after the
  * first starts as its predecessor drains.  Results depend on neither size.
@@ -220,7 +221,11 @@ zero_status_t zero_step_shard(const zero_grads_t* g, const zero_layout_t* L,
  * flag, and the caller should report ZERO_ERR_TIMEOUT. */
 #define ZERO_STEP_FLAG_WAIT_TIMEOUT 0x80000000u
 
-/* Longest launch window of the fused step, in elements (see zero_step_shard). */
+/* Launch-window size of the fused step, in elements: a range of n elements
+ * runs as ceil(n / ZERO_FUSED_WINDOW_ELEMS) windows of about equal length,
+ * none more than 15 elements longer than this (for n below 3.4e12; beyond,
+ * a remainder of under 64 elements can join a full window; see
+ * zero_step_shard). */
 #define ZERO_FUSED_WINDOW_ELEMS 10485760ull
 
 /* The same step unfused, through the constant-size fusion buffer: per bucket,
@@ -291,8 +296,8 @@ zero_status_t zero_check_nonfinite(const zero_grads_t* g, uint64_t begin, uint64
  * makes every bucket its own group); for each group in order a
  * one-thread kernel waits until d_ready[b] >= epoch (wrap-around comparison)
  * for each of its buckets, then the fused step's launches for the group follow
- * on the same stream (as zero_step_shard: launch windows of at most
- * ZERO_FUSED_WINDOW_ELEMS elements, the same kernel variant).  The producer
+ * on the same stream (as zero_step_shard: launch windows of about
+ * ZERO_FUSED_WINDOW_ELEMS elements at most, the same kernel variant).  The producer
  * of bucket b
  * writes d_ready[b] after the bucket's contributions are in place -- e.g. a
  * cudaMemcpyAsync of the word on the copy stream that copied the data.  The

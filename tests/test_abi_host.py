@@ -323,11 +323,12 @@ def test_launch_windows_properties():
         assert all(a[1] == b[0] for a, b in zip(cuts, cuts[1:]))
         # every inner cut falls on a 32-byte (one L2 sector) boundary of the rows
         assert all((phase + c[0]) % 16 == 0 for c in cuts[1:])
-        # the fewest windows (a remainder under 64 may join the last one), each
-        # at most one window, the row phase and such a remainder
+        # ceil(length / W) windows (below 3.4e12 elements no remainder under
+        # 64 is left after the last full window), none longer than W plus the
+        # row phase (at most 15)
         nwin = -(-length // W)
-        assert len(cuts) in (nwin, max(nwin - 1, 1))
-        assert all(c[1] - c[0] <= W + 15 + 63 for c in cuts)
+        assert len(cuts) == nwin
+        assert all(c[1] - c[0] <= W + 15 for c in cuts)
         # and the binding's launch count is exactly this split
         assert z_abi()._windows(length, phase) == len(cuts)
 
@@ -357,3 +358,20 @@ def test_header_is_plain_c_and_host_calls_work_from_c(z, tmp_path):
     assert out[5] == f"invalid {z.ZERO_ERR_INVALID_ARG}"
     assert out[6] == f"status {z.zero_status_string(z.ZERO_ERR_TIMEOUT)}"
     assert out[7] == f"window {z._abi.ZERO_FUSED_WINDOW_ELEMS}"
+
+
+def test_launch_window_bounds_brute_force():
+    """The split's bounds, brute force over small windows: with a window of
+    W >= 1024 elements every range runs as ceil(n / W) windows, none longer
+    than W + 15 (the row phase); with windows under 64 * 16 a remainder of
+    under 64 elements may join a full window, the longest then W + 63."""
+    from window_rule import window_cuts
+    for W, lengths in ((1024, range(1, 12_000)), (4096, range(1, 40_000, 7)),
+                       (64, range(1, 3_000)), (128, range(1, 3_000))):
+        for length in lengths:
+            for phase in range(16):
+                cuts = window_cuts(length, phase, W)
+                sizes = [b - a for a, b in cuts]
+                assert max(sizes) <= W + (15 if W >= 1024 else 63), (W, length, phase)
+                if W >= 1024:
+                    assert len(cuts) == -(-length // W), (W, length, phase)

@@ -1,6 +1,6 @@
 """The fused step's launch-window split, restated from include/zero.h for the
-tests: the fewest equal windows of at most ZERO_FUSED_WINDOW_ELEMS elements
-over a shard, every inner cut on a 16-element (32-byte) boundary of row 0
+tests: ceil(length / ZERO_FUSED_WINDOW_ELEMS) windows of about equal length
+(none longer than ZERO_FUSED_WINDOW_ELEMS + 15) over a shard, every inner cut on a 16-element (32-byte) boundary of row 0
 (whose element 0 sits `phase` elements past a 32-byte boundary: its offset in
 the row, for the 32-byte aligned torch buffers of the tests), and a remainder
 of under 64 elements joined to the last window.  Used to put sampled oracle

@@ -495,11 +495,13 @@ __device__ __forceinline__ bool fused_epilogue_loaded(const FusedArgs& a, uint64
     return bad;
 }
 
-// Calls fn(w0, w1) for the fewest equal launch windows of at most
-// max_window elements (a multiple of 16) covering [0, len) of a range whose
+// Calls fn(w0, w1) for ceil(len / max_window) launch windows of about equal
+// length (max_window a multiple of 16) covering [0, len) of a range whose
 // rows' element 0 has phase `phase` (elements past a 32-byte boundary): every
 // cut falls on a 16-element (32-byte, one L2 sector) boundary of the rows, and
-// a remainder of under 64 elements joins the last window.  Stops at the
+// a remainder of under 64 elements joins the last window.  Moving the cuts
+// back to those boundaries shortens the first window by the phase and can
+// lengthen the last to max_window + 15 elements.  Stops at the
 // first status other than ZERO_OK.
 template <typename F>
 zero_status_t for_each_window(uint64_t phase, uint64_t len, uint64_t max_window, F&& fn)

@@ -84,8 +84,9 @@ zero_status_t require_device_state(const zero_state_t* in, const zero_state_t* o
 void preload_fused(int dtype, bool host_rows);
 
 // Launches the fused step over elements [b0, b0 + len) of a shard (the
-// whole shard, or one launch group of buckets) as the fewest equal launch
-// windows of at most ZERO_FUSED_WINDOW_ELEMS elements.  rows: the rows at shard element 0, at
+// whole shard, or one launch group of buckets) as ceil(len /
+// ZERO_FUSED_WINDOW_ELEMS) launch windows of about equal length
+// (for_each_window).  rows: the rows at shard element 0, at
 // the address the device reads them (resolve_grads); gath: the gathered slot
 // of shard element 0.  The variant follows ZERO_FUSED_VARIANT (the register
 // kernel for host_rows).  gate: if non-null, every launch reads it first and
