@@ -69,17 +69,32 @@ def measured_peaks() -> dict:
         return {}
 
 
-def kernel_name() -> str:
+# Elements a SM covers in one wave of the short-window kernel (3 CTAs of 256
+# threads, 4 elements a thread): by default the library runs a launch window
+# of at most SMs times this on that kernel instead of the ring.
+SMALL_WAVE_ELEMS_PER_SM = 3 * 256 * 4
+
+
+def kernel_name(shard_elems: int = None) -> str:
     """The fused-step kernel the run uses: ZERO_FUSED_VARIANT if set, else the
     build's ZERO_FUSED_IMPL (0 registers, 1 cp.async ring (default), 2 bulk
-    copies)."""
+    copies), the default ring giving a shard of at most SMs x 3,072 elements
+    (one window) to the short-window kernel."""
     import re
-    names = {0: "k_step_fused", 1: "k_step_fused_ring", 2: "k_step_fused_tma"}
+    names = {0: "k_step_fused", 1: "k_step_fused_ring", 2: "k_step_fused_tma",
+             3: "k_step_fused_small"}
     v = os.environ.get("ZERO_FUSED_VARIANT")
-    if v in ("registers", "ring", "tma"):
-        return names[{"registers": 0, "ring": 1, "tma": 2}[v]]
-    m = re.search(r"ZERO_FUSED_IMPL=(\d)", os.environ.get("ZERO_NVCC_FLAGS", ""))
-    return names.get(int(m.group(1)) if m else 1, "k_step_fused_ring")
+    if v in ("registers", "ring", "tma", "small"):
+        return names[{"registers": 0, "ring": 1, "tma": 2, "small": 3}[v]]
+    flags = os.environ.get("ZERO_NVCC_FLAGS", "")
+    m = re.search(r"ZERO_FUSED_IMPL=(\d)", flags)
+    impl = int(m.group(1)) if m else 1
+    if impl == 1 and "ZERO_SMALL_WINDOWS=0" not in flags and shard_elems is not None:
+        import torch
+        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+        if shard_elems <= sms * SMALL_WAVE_ELEMS_PER_SM:
+            return names[3]
+    return names.get(impl, "k_step_fused_ring")
 
 
 def kernel_source_hash() -> str:
@@ -98,7 +113,7 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, shard_elems: int):
     """DRAM bytes per parameter of the fused kernel from the committed ncu
     summary, if it was taken on the current kernel source for this workload."""
     try:
@@ -114,7 +129,7 @@ def recorded_traffic(workload: str):
         return None
     if kv.get("build_flags", "") != os.environ.get("ZERO_NVCC_FLAGS", ""):
         return None
-    if kernel_name() != "k_step_fused_ring":      # recorded for the default kernel
+    if kernel_name(shard_elems) != "k_step_fused_ring":   # recorded for the ring kernel
         return None
     v = kv.get(f"dram_bytes_per_param.{workload}")
     return None if v is None else float(v)
@@ -175,6 +190,32 @@ def time_back_to_back(torch, stream, dev, call, reps: int) -> float:
     return e0.elapsed_time(e1) / reps
 
 
+def time_graph(torch, stream, dev, call, steps: int, reps: int = 5) -> float:
+    """Milliseconds per call of `steps` calls captured once as a CUDA graph on
+    `stream` and replayed `reps` times, CUDA events on `stream`: the GPU's
+    time for the calls with no host issue time between them.  The calls'
+    arguments are frozen at capture, so the replays repeat the same steps;
+    the driver's bookkeeping (its step count, its current buffers) no longer
+    matches the data afterwards."""
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+        for _ in range(steps):
+            call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / (reps * steps)
+    del g
+    return ms
+
+
 # The other workloads the default line also times (kernel time only): the
 # 1.5B shard is the second target workload; rank 1 of the 1.5B and 7.5B
 # shards writes its parameters into its slot of the flat Nd*S buffer, 8 bytes
@@ -223,13 +264,25 @@ def measure_config(key: str, rank: int, gathered: str, dev, stream, peak: float,
            "grad_dtype": w.grad_dtype,
            "gathered": gathered + (f" (slot at element {int(L.begin)}, 16-byte phase "
                                    f"{(int(L.begin) * 2) % 16} B)" if gathered == "full" else ""),
-           "kernel": kernel_name(), "kernel_ms_per_step": ms, "launches_per_step": launches,
+           "kernel": kernel_name(n), "kernel_ms_per_step": ms, "launches_per_step": launches,
            "kernel_ms": ms / launches, "algorithmic_bytes_per_param": w.bytes_per_param,
            "achieved": gbs, "frac": gbs / peak, "params_per_s": n / (ms * 1e-3),
            "steps_timed_back_to_back": reps, "skipped": skipped}
     if step_bytes <= L2_BYTES:
         out["l2"] = (f"L2-resident ({step_bytes / 1e6:.1f} MB per step): a latency figure, not "
                      "a bandwidth one")
+        # Such a short step is issued slower than it runs: time its kernels
+        # without the host's issue time too, as one CUDA graph of the same
+        # back-to-back steps (the last measurement on this driver).
+        try:
+            gms = time_graph(torch, stream, dev, call, reps)
+        except RuntimeError as e:      # a capture this torch build refuses: no figure
+            out["graph"] = f"unavailable: {str(e).splitlines()[0][:200]}"
+        else:
+            gbs_graph = step_bytes / (gms * 1e-3) / 1e9
+            out["kernel_ms_per_step_graph"] = gms
+            out["achieved_graph"] = gbs_graph
+            out["frac_graph"] = gbs_graph / peak
     del dps, grads
     torch.cuda.empty_cache()
     return out
@@ -595,6 +648,17 @@ def run_gpu(args) -> None:
                                        "reads of host memory in this run: not a bound")
             del host_grads, host_params, dps_h
 
+    # -- optionally the back-to-back steps once more as one CUDA graph: their
+    #    kernels' time without the host's issue time (for shards whose step is
+    #    issued slower than it runs).  Last, since the replays leave the
+    #    driver's bookkeeping behind its data. ----------------------------------
+    graph_ms = None
+    if args.graph:
+        def b2b():
+            dps.launch(desc)
+            dps.commit(False)
+        graph_ms = max_over_ranks(time_graph(torch, stream, dev, b2b, nk), group, dev)
+
     # -- the other workloads' fused step (kernel time), rank 0 at N = 1 only --
     peaks = measured_peaks()
     per_config = None
@@ -625,7 +689,7 @@ def run_gpu(args) -> None:
     peak = peak or 6800.0
     traffic_pp = None if (args.psi or args.nd or args.grad_dtype or args.row_pad or
                           args.bucket) else \
-        recorded_traffic(args.config)
+        recorded_traffic(args.config, n)
     line = {
         "metric": METRIC,
         "value": world * n / (ms_per_step * 1e-3),
@@ -645,9 +709,12 @@ def run_gpu(args) -> None:
                      "frac": achieved / peak, "peak_source": peak_src,
                      "frac_of_nominal_7900": achieved / NOMINAL_HBM_GBS,
                      "traffic": None if traffic_pp is None else traffic_pp * n / per_step,
-                     "kernel": kernel_name(), "kernel_ms": kern_avg_ms,
+                     "kernel": kernel_name(n), "kernel_ms": kern_avg_ms,
                      "launches_per_step": per_step,
                      "kernel_ms_per_step": back_to_back_ms,
+                     **({} if graph_ms is None else {
+                         "kernel_ms_per_step_graph": graph_ms,
+                         "frac_graph": bytes_per_param * n / (graph_ms * 1e-3) / 1e9 / peak}),
                      "kernel_ms_in_sync_step": kern_step_ms,
                      "kernel_ms_in_sync_step_median": statistics.median(kernel_ms),
                      "kernel_ms_in_sync_step_min": min(kernel_ms),
@@ -1022,8 +1089,13 @@ def main():
                     help="step (the benchmark line) or a measurement of another entry point")
     ap.add_argument("--config", default="c4", choices=["c0", "c1", "c2", "c3", "c4"])
     ap.add_argument("--rank", type=int, default=0, help="first data-parallel rank to run")
-    ap.add_argument("--variant", choices=["registers", "ring", "tma"], default=None,
-                    help="fused-step kernel (sets ZERO_FUSED_VARIANT; default: the ring)")
+    ap.add_argument("--variant", choices=["registers", "ring", "tma", "small"], default=None,
+                    help="fused-step kernel for every window (sets ZERO_FUSED_VARIANT; "
+                         "default: the ring, and the short-window kernel for a shard "
+                         "shorter than one pass of the ring's grid)")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the back-to-back steps as one CUDA graph (kernel time "
+                         "without host issue time)")
     ap.add_argument("--gathered", choices=["slot", "full"], default="slot",
                     help="slot: the rank's own S-element parameter buffer; full: its slot at "
                          "r*S of the flat Nd*S buffer (odd ranks then start off the 16-byte "

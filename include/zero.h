@@ -195,13 +195,17 @@ zero_status_t zero_gather_params_shard(const float* master, uint64_t n, void* ga
  * rows; launches much longer than this let the SMs drift apart, and a cut
  * inside a 32-byte sector slows every launch after it).  A window after the
  * first starts as its predecessor drains.  Results depend on neither size.
- * The kernel is the cp.async-ring variant unless the environment variable
- * ZERO_FUSED_VARIANT, read at each call, names another ("registers", "ring"
- * or "tma": bulk copies and mbarriers); rows in host memory always use the
- * register variant.  All variants give bitwise the same results.  Launches
- * are programmatic dependent launches (each kernel waits in-kernel for its
- * predecessor in the stream, so consecutive launches lose their gap) unless
- * the environment variable ZERO_PDL is "0".
+ * The kernel is the cp.async-ring variant, except that a window that one
+ * wave of the short-window kernel covers (SMs x 3 CTAs x 256 threads x 4
+ * elements: 466,944 on 152 SMs) runs on that kernel (4 elements a thread,
+ * so the AdamW arithmetic spreads over every SM), unless the environment
+ * variable ZERO_FUSED_VARIANT, read at each call, names one kernel for every
+ * window ("registers", "ring", "small" or "tma": bulk copies and
+ * mbarriers); rows in host memory always use the register variant.  All
+ * variants give bitwise the same results.  Launches are programmatic
+ * dependent launches (each kernel waits in-kernel for its predecessor in
+ * the stream, so consecutive launches lose their gap) unless the
+ * environment variable ZERO_PDL is "0".
  * The new state goes to `out` and the cast parameters to
  * gathered[gathered_offset_elems + i] (device or page-locked host memory).  *d_nonfinite |= 1 if any reduced sum
  * is nonfinite; the step is then to be skipped on every shard: with out != in

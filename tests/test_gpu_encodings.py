@@ -84,7 +84,7 @@ def _same_bits_or_both_nan(got: np.ndarray, ref: np.ndarray, what: str):
                             f"{got[np.argmax(diff)]!r} vs {ref[np.argmax(diff)]!r}")
 
 
-@pytest.mark.parametrize("variant", ["ring", "registers"])
+@pytest.mark.parametrize("variant", ["ring", "registers", "small"])
 @pytest.mark.parametrize("dt", ["f16", "bf16"])
 def test_every_encoding_folds_like_the_oracle(dt, variant, monkeypatch):
     """zero_reduce_scatter_bucket (the ring's reduction mode, or the register
@@ -131,7 +131,7 @@ def _extreme_rows(dt):
     return np.stack([a, b, c])
 
 
-@pytest.mark.parametrize("path", ["ring", "registers", "tma", "unfused"])
+@pytest.mark.parametrize("path", ["ring", "registers", "tma", "small", "unfused"])
 @pytest.mark.parametrize("dt", ["f16", "bf16"])
 def test_step_over_extreme_rows(dt, path, monkeypatch):
     """zero_step_shard (each kernel) and zero_step_shard_unfused on rows of
@@ -187,7 +187,7 @@ def test_step_over_extreme_rows(dt, path, monkeypatch):
     assert not rest.any(), "write outside the slot"
 
 
-@pytest.mark.parametrize("variant", ["ring", "registers"])
+@pytest.mark.parametrize("variant", ["ring", "registers", "small"])
 @pytest.mark.parametrize("dt", ["f16", "bf16"])
 def test_every_encoding_through_the_scalar_path(dt, variant, monkeypatch):
     """Ragged heads and tails of a window are folded one element at a time
@@ -226,7 +226,7 @@ def test_every_encoding_through_the_scalar_path(dt, variant, monkeypatch):
             assert bool((f32(cb)[gaps] == -7.0).all()), f"{what}: a gap was written"
 
 
-@pytest.mark.parametrize("path", ["ring", "registers", "tma", "unfused"])
+@pytest.mark.parametrize("path", ["ring", "registers", "tma", "small", "unfused"])
 @pytest.mark.parametrize("dt", ["f16", "bf16"])
 def test_step_scalar_path_over_extreme_rows(dt, path, monkeypatch):
     """The step's scalar path (a shard's last n mod 8 elements) over the

@@ -69,11 +69,11 @@ SHAPES = [(64 * 20_003 + 5, 64, 3, 6_001), (2 * 25_165_893 - 3, 2, 1, 1 << 22)]
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=["64 ranks", "three launch windows"])
-@pytest.mark.parametrize("path", ["ring", "registers", "tma", "unfused", "streamed"])
+@pytest.mark.parametrize("path", ["ring", "registers", "tma", "small", "unfused", "streamed"])
 def test_step_paths_stay_inside_their_buffers(path, shape, monkeypatch):
     psi, nd, rank, bucket = shape
     w = dataclasses.replace(synth.WORKLOADS["c1"], psi=psi, nd=nd, plant=None)
-    if path in ("ring", "registers", "tma"):
+    if path in ("ring", "registers", "tma", "small"):
         monkeypatch.setenv("ZERO_FUSED_VARIANT", path)
     monkeypatch.setenv("ZERO_STREAM_GROUP_BYTES", "0")
     dps = make_group(w, ranks=[rank], gathered="full")

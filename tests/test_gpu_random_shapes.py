@@ -1,8 +1,8 @@
 """Seeded random shapes against the oracle, on every path of the step.
 
 Each case draws a flat size, a data-parallel degree, a bucket size, a
-gradient type, the ranks held and the path (fused with each kernel variant,
-unfused, bucket-ready, or fused with the rows and the gathered parameters in
+gradient type, the ranks held and the path (fused with each kernel variant or
+the default choice among them, unfused, bucket-ready, or fused with the rows and the gathered parameters in
 pinned host memory), runs two steps on the GPU with every rank's whole
 gradient resident, and compares every element of state and parameters with
 the oracle's unsharded step.  The draws favour the awkward: sizes not
@@ -22,7 +22,7 @@ from gpu_util import DEV, check_against_oracle, full_rows, make_group, oracle_tr
 
 pytestmark = pytest.mark.gpu
 
-PATHS = ["ring", "registers", "tma", "unfused", "streamed", "host"]
+PATHS = ["ring", "registers", "tma", "small", "auto", "unfused", "streamed", "host"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -76,7 +76,7 @@ def test_random_shape(seed, monkeypatch):
     w = dataclasses.replace(synth.WORKLOADS["c1"], grad_dtype=dt,
                             loss_scale=1024.0 if dt == "f16" else 1.0, plant=None,
                             fresh_grads=True)
-    if path in ("ring", "registers", "tma"):
+    if path in ("ring", "registers", "tma", "small"):
         monkeypatch.setenv("ZERO_FUSED_VARIANT", path)
     if path == "streamed":
         monkeypatch.setenv("ZERO_STREAM_GROUP_BYTES", "0")

@@ -55,7 +55,7 @@ def _run_threads(fn, args_list):
         raise errors[0]
 
 
-@pytest.mark.parametrize("path", ["ring", "tma", "registers", "unfused"])
+@pytest.mark.parametrize("path", ["ring", "tma", "registers", "small", "unfused"])
 def test_threads_step_their_own_ranks(path, monkeypatch):
     if path != "unfused":
         monkeypatch.setenv("ZERO_FUSED_VARIANT", path)

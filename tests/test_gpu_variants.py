@@ -1,12 +1,15 @@
 """Every variant of the fused step kernel gives the oracle's step bit for bit.
 
-zero_step_shard runs the cp.async-ring kernel by default; the environment
-variable ZERO_FUSED_VARIANT selects the register kernel ("registers", also
-the kernel for host-resident rows) or the bulk-copy kernel ("tma": a
-producer warp, mbarrier-tracked cp.async.bulk copies of rows and state).
-Each is checked here on the same cases as the default: the 4-rank workload
-against the oracle, ragged shapes and every slot phase, a global skip, and
-whole shards of several launch windows against the oracle.
+zero_step_shard runs the cp.async-ring kernel by default, and the
+short-window kernel for windows shorter than one pass of the ring's grid; the
+environment variable ZERO_FUSED_VARIANT selects one kernel for every window:
+the ring ("ring"), the short-window kernel ("small": 4 elements a thread),
+the register kernel ("registers", also the kernel for host-resident rows) or
+the bulk-copy kernel ("tma": a producer warp, mbarrier-tracked cp.async.bulk
+copies of rows and state).  Each is checked here on the same cases as the
+default: the 4-rank workload against the oracle, ragged shapes and every slot
+phase, a global skip, and whole shards of several launch windows against the
+oracle.
 """
 import dataclasses
 
@@ -23,7 +26,7 @@ from gpu_util import (EDGE_CASES, assert_params_close, assert_state_close,
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = ["registers", "ring", "tma"]
+VARIANTS = ["registers", "ring", "tma", "small"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -56,7 +59,7 @@ def test_c0_matches_oracle(variant, fused):
 
 
 @pytest.mark.parametrize("psi,nd,dt,bucket", EDGE_CASES)
-@pytest.mark.parametrize("variant", ["registers", "tma"], indirect=True)
+@pytest.mark.parametrize("variant", ["registers", "tma", "ring", "small"], indirect=True)
 def test_edge_shapes(variant, psi, nd, dt, bucket):
     w = dataclasses.replace(synth.WORKLOADS["c1"], grad_dtype=dt,
                             loss_scale=1024.0 if dt == "f16" else 1.0, plant=None)
@@ -70,7 +73,7 @@ def test_edge_shapes(variant, psi, nd, dt, bucket):
                              f"{variant} psi={psi} nd={nd} step {k}")
 
 
-@pytest.mark.parametrize("variant", ["registers", "tma"], indirect=True)
+@pytest.mark.parametrize("variant", ["registers", "tma", "ring", "small"], indirect=True)
 def test_global_skip(variant):
     w = dataclasses.replace(synth.WORKLOADS["c2"], psi=100_003, nd=16, plant=None)
     dps = make_group(w, bucket=4096)
@@ -177,3 +180,38 @@ def test_reductions_over_several_launch_windows_match_oracle(variant):
     z.zero_check_nonfinite(desc[rank], 0, n, flag)
     torch.cuda.synchronize()
     assert int(flag.item()) == 1
+
+
+def test_default_choice_at_the_one_wave_boundary(monkeypatch):
+    """By default a shard that one wave of the short-window kernel covers
+    (SMs x 3 x 256 x 4 elements) runs on that kernel and one element more on
+    the ring: both sides of the boundary, and the same shards on each kernel
+    named explicitly, against the oracle element by element (3 fp16 rows;
+    rank 1 writes its slot of the flat gathered buffer, 16-byte aligned at
+    the boundary and 2 bytes past a line one element later)."""
+    monkeypatch.delenv("ZERO_FUSED_VARIANT", raising=False)
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    wave = sms * 3 * 256 * 4
+    for s in (wave, wave + 1):
+        w = dataclasses.replace(synth.WORKLOADS["c2"], psi=3 * s - 1, nd=3, plant=None,
+                                bucket=1 << 30)
+        f, rp, rm, rv, rparams = oracle_shard_step(w, 1)
+        assert f == 0
+        for v in (None, "small", "ring"):
+            if v is None:
+                monkeypatch.delenv("ZERO_FUSED_VARIANT", raising=False)
+            else:
+                monkeypatch.setenv("ZERO_FUSED_VARIANT", v)
+            dps = make_group(w, ranks=[1], gathered="full")
+            buf, desc = shard_rows(w, dps, 1, 0)
+            assert not dps.step(desc)
+            n = int(dps.layouts[1].length)
+            assert n == s
+            got = [t.cpu().numpy() for t in dps.state[1].tensors("cur")]
+            for g, ref, name, tau in zip(got, (rp, rm, rv), ("master", "m", "v"),
+                                         (1e-12, 1e-20, 1e-20)):
+                assert_state_close(g, ref, tau, f"{v} n={n} {name}")
+            b = int(dps.layouts[1].begin)
+            assert_params_close(u16(dps.gathered_view(1)[b:b + n]), rparams,
+                                f"{v} n={n} params")
+            del dps, buf, desc

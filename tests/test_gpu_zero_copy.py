@@ -141,7 +141,7 @@ def test_pageable_host_rows_are_refused():
         assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("path", ["ring", "registers", "tma", "unfused"])
+@pytest.mark.parametrize("path", ["ring", "registers", "tma", "small", "unfused"])
 def test_host_params_equal_device_params(path, monkeypatch):
     """Every rank's cast parameters written into one flat gathered buffer in
     pinned host memory (16 ranks, S mod 8 = 3: every slot phase; buckets of

@@ -191,6 +191,132 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_step_fused(const Fused
     pdl_end(a.early);
 }
 
+// 8-byte read of gradient data used once (4 elements of one row).
+__device__ __forceinline__ uint2 ld_grad8(const uint16_t* p)
+{
+    uint2 r;
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
+template <int DT>
+__device__ __forceinline__ void add4(float (&a)[4], uint2 w, bool first)
+{
+    const float2 lo = widen2<DT>(w.x), hi = widen2<DT>(w.y);
+    if (first) {
+        a[0] = lo.x;
+        a[1] = lo.y;
+        a[2] = hi.x;
+        a[3] = hi.y;
+    } else {
+        a[0] = __fadd_rn(a[0], lo.x);
+        a[1] = __fadd_rn(a[1], lo.y);
+        a[2] = __fadd_rn(a[2], hi.x);
+        a[3] = __fadd_rn(a[3], hi.y);
+    }
+}
+
+// Store 4 consecutive 16-bit values (packed in 2 words) at q with the widest
+// stores its address allows (W = 8, 4 or 2 bytes).
+template <int W>
+__device__ __forceinline__ void store4(uint16_t* q, uint32_t w0, uint32_t w1)
+{
+    if (W == 8) {
+        __stcs(reinterpret_cast<uint2*>(q), make_uint2(w0, w1));
+    } else if (W == 4) {
+        __stcs(reinterpret_cast<unsigned int*>(q), w0);
+        __stcs(reinterpret_cast<unsigned int*>(q + 2), w1);
+    } else {
+        __stcs(reinterpret_cast<unsigned short*>(q), (unsigned short)(w0 & 0xFFFF));
+        __stcs(reinterpret_cast<unsigned short*>(q + 1), (unsigned short)(w0 >> 16));
+        __stcs(reinterpret_cast<unsigned short*>(q + 2), (unsigned short)(w1 & 0xFFFF));
+        __stcs(reinterpret_cast<unsigned short*>(q + 3), (unsigned short)(w1 >> 16));
+    }
+}
+
+// Element split of a short window into 4-element groups: `head` scalar
+// elements up to the first row element on an 8-byte boundary, `nquad`
+// groups, then a scalar tail (at most 3 + 3 scalar elements in all).
+struct QuadSplit {
+    uint64_t head;
+    uint64_t nquad;
+};
+
+constexpr int kSmallThreads = 256;
+// Resident CTAs a SM the short-window kernel is compiled for (its register
+// budget: 65,536 / (256 x this); 80 registers at 3) and rank rows it loads
+// back to back.  Measured against 4 CTAs with 4 rows (no spills) and 5 with 4
+// on 1 to 64 rows of 65,536 to 622,592 elements: level or faster everywhere
+// within one wave, and up to 20% faster on 16 and 64 rows.
+#ifndef ZERO_SMALL_CTAS_PER_SM
+#define ZERO_SMALL_CTAS_PER_SM 3
+#endif
+constexpr int kSmallCtasPerSm = ZERO_SMALL_CTAS_PER_SM;
+#ifndef ZERO_SMALL_UNROLL
+#define ZERO_SMALL_UNROLL 8
+#endif
+constexpr int kSmallUnroll = ZERO_SMALL_UNROLL;
+
+// K4, short-window variant.  A window shorter than one pass of the ring
+// kernel's grid leaves most of the ring's threads idle and puts the AdamW
+// arithmetic (three correctly rounded divisions and a square root an
+// element) on a few SMs; this kernel gives each thread 4 elements (8-byte
+// row reads, 16-byte state accesses), so the same window spreads over every
+// SM with twice to four times the threads.  Within one wave of its grid
+// (kSmallCtasPerSm CTAs a SM) it beat the ring on every shard measured, by
+// 10% (4 rows of 262,144) to 44% (64 rows of 65,536); past one wave the
+// ring wins.  The fold, the op order and the stores' values are those of
+// every other variant.
+template <int DT, int W>
+__global__ void __launch_bounds__(kSmallThreads, kSmallCtasPerSm)
+    k_step_fused_small(const FusedArgs a, const QuadSplit qs)
+{
+    pdl_begin(a.early);
+    if (gated(a))   // all of a group's windows see the gate alike (see k_step_fused_ring)
+        return;
+    bool bad = false;
+    const uint64_t tid = (uint64_t)blockIdx.x * kSmallThreads + threadIdx.x;
+    const uint64_t nthr = (uint64_t)gridDim.x * kSmallThreads;
+    const uint64_t nscalar = a.sp.len - 4 * qs.nquad;
+    if (tid < nscalar)
+        bad |= fused_scalar<DT>(a, tid < qs.head ? tid : qs.head + 4 * qs.nquad + (tid - qs.head));
+    for (uint64_t q = tid; q < qs.nquad; q += nthr) {
+        const uint64_t e = qs.head + 4 * q;
+        const uint16_t* gp = a.g + e;
+        float s[4];
+        add4<DT>(s, ld_grad8(gp), true);
+        for (uint32_t j0 = 1; j0 < a.nd; j0 += kSmallUnroll) {
+            uint2 w[kSmallUnroll];
+#pragma unroll
+            for (int u = 0; u < kSmallUnroll; ++u)
+                if (j0 + u < a.nd)
+                    w[u] = ld_grad8(gp + (uint64_t)(j0 + u) * a.row_stride);
+#pragma unroll
+            for (int u = 0; u < kSmallUnroll; ++u)
+                if (j0 + u < a.nd)
+                    add4<DT>(s, w[u], false);
+        }
+        const float4 pp = __ldcs(reinterpret_cast<const float4*>(a.p_in + e));
+        const float4 mm = __ldcs(reinterpret_cast<const float4*>(a.m_in + e));
+        const float4 vv = __ldcs(reinterpret_cast<const float4*>(a.v_in + e));
+        float p[4] = {pp.x, pp.y, pp.z, pp.w};
+        float m[4] = {mm.x, mm.y, mm.z, mm.w};
+        float v[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            bad |= nonfinite(s[i]);
+            adamw1(a.k, __fmul_rn(s[i], a.k.inv), p[i], m[i], v[i]);
+        }
+        __stcs(reinterpret_cast<float4*>(a.p_out + e), make_float4(p[0], p[1], p[2], p[3]));
+        __stcs(reinterpret_cast<float4*>(a.m_out + e), make_float4(m[0], m[1], m[2], m[3]));
+        __stcs(reinterpret_cast<float4*>(a.v_out + e), make_float4(v[0], v[1], v[2], v[3]));
+        store4<W>(a.gath + e, (uint32_t)narrow1<DT>(p[0]) | ((uint32_t)narrow1<DT>(p[1]) << 16),
+                  (uint32_t)narrow1<DT>(p[2]) | ((uint32_t)narrow1<DT>(p[3]) << 16));
+    }
+    flag_if_any(bad, a.flag);
+    pdl_end(a.early);
+}
+
 
 // Epilogue of the bulk-copy variant: the state of the 8 elements at e was
 // staged in shared memory; the new state leaves with streaming stores
@@ -670,10 +796,18 @@ int sm_count()
 }
 
 // The fused-step variant of a call: ZERO_FUSED_VARIANT if set, else the
-// build's default.  The ring kernel streams HBM-resident rows best.  Rows
-// read in place from host memory always go to the register kernel, whose
-// loads keep the host link busier (about 203 against 183 GB/s on the 7.5B
-// shard's 64 rows).
+// build's default, which with the ring kernel is kVariantAuto: the ring, and
+// the short-window kernel for windows that one wave of its grid covers
+// (ZERO_SMALL_WINDOWS 0 turns that off).  The ring kernel streams
+// HBM-resident rows best.  Rows read in place from host memory always go to
+// the register kernel, whose loads keep the host link busier (about 203
+// against 183 GB/s on the 7.5B shard's 64 rows).
+#ifndef ZERO_SMALL_WINDOWS
+#define ZERO_SMALL_WINDOWS 1
+#endif
+constexpr int kVariantSmall = 3;
+constexpr int kVariantAuto = -1;
+
 int fused_variant(bool host_rows)
 {
     if (host_rows)
@@ -685,7 +819,16 @@ int fused_variant(bool host_rows)
         return 1;
     if (v && strcmp(v, "tma") == 0)
         return 2;
-    return ZERO_FUSED_IMPL;
+    if (v && strcmp(v, "small") == 0)
+        return kVariantSmall;
+    return ZERO_FUSED_IMPL == 1 && ZERO_SMALL_WINDOWS ? kVariantAuto : ZERO_FUSED_IMPL;
+}
+
+// Elements one wave of the short-window kernel covers (4 a thread): a window
+// of at most this many goes to that kernel under kVariantAuto.
+uint64_t small_window_limit()
+{
+    return (uint64_t)sm_count() * kSmallCtasPerSm * kSmallThreads * 4;
 }
 
 // Opts kernel `fn` in to `bytes` of dynamic shared memory on the current
@@ -789,6 +932,29 @@ void launch_fused_w(const FusedArgs& a, int variant, cudaStream_t s)
         launch_ring<DT, W, V8, kModeStep>(grid, a, s);
     } else {
         launch_k(k_step_fused<DT, W, V8>, dim3(grid_for(work)), dim3(kThreads), 0, s, a);
+    }
+}
+
+// The short-window kernel over one window: quad split from the rows' phase,
+// store width from the gathered slot's (at most 8 bytes), and a CTA for every
+// 256 groups up to one wave (then a grid-stride loop).
+template <int DT>
+void launch_small(const FusedArgs& a, uint64_t row_phase, cudaStream_t s)
+{
+    QuadSplit qs;
+    const uint64_t head = (4 - (row_phase & 3)) & 3;
+    qs.head = head < a.sp.len ? head : a.sp.len;
+    qs.nquad = (a.sp.len - qs.head) / 4;
+    const uint64_t nscalar = a.sp.len - 4 * qs.nquad;
+    const uint64_t work = qs.nquad > nscalar ? qs.nquad : nscalar;
+    const uint64_t want = (work + kSmallThreads - 1) / kSmallThreads;
+    const uint64_t cap = (uint64_t)sm_count() * kSmallCtasPerSm;
+    const dim3 grid((unsigned)(want < cap ? (want ? want : 1) : cap));
+    switch (store_width(a.gath + qs.head)) {
+    case 16:
+    case 8: launch_k(k_step_fused_small<DT, 8>, grid, dim3(kSmallThreads), 0, s, a, qs); break;
+    case 4: launch_k(k_step_fused_small<DT, 4>, grid, dim3(kSmallThreads), 0, s, a, qs); break;
+    default: launch_k(k_step_fused_small<DT, 2>, grid, dim3(kSmallThreads), 0, s, a, qs); break;
     }
 }
 
@@ -977,6 +1143,15 @@ void load_fused_w(int variant)
 template <int DT>
 void load_fused_dt(int variant)
 {
+    if (variant == kVariantSmall || variant == kVariantAuto) {
+        cudaFuncAttributes fa;
+        (void)cudaFuncGetAttributes(&fa, k_step_fused_small<DT, 8>);
+        (void)cudaFuncGetAttributes(&fa, k_step_fused_small<DT, 4>);
+        (void)cudaFuncGetAttributes(&fa, k_step_fused_small<DT, 2>);
+        if (variant == kVariantSmall)
+            return;
+        variant = 1;
+    }
     load_fused_w<DT, 16, true>(variant);
     load_fused_w<DT, 8, true>(variant);
     load_fused_w<DT, 4, true>(variant);
@@ -994,12 +1169,13 @@ bool pdl_launches() { return pdl_enabled(); }
 void preload_fused(int dtype, bool host_rows)
 {
     const int variant = fused_variant(host_rows);
-    static std::atomic<uint64_t> done[2][3];   // per dtype and variant: a bit per device
+    // per dtype and variant (kVariantAuto .. kVariantSmall): a bit per device
+    static std::atomic<uint64_t> done[2][kVariantSmall - kVariantAuto + 1];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         dev = 64;
     const uint64_t bit = dev < 64 ? 1ull << dev : 0;
-    std::atomic<uint64_t>& d = done[dtype == ZERO_F16 ? 0 : 1][variant];
+    std::atomic<uint64_t>& d = done[dtype == ZERO_F16 ? 0 : 1][variant - kVariantAuto];
     if (bit && (d.load(std::memory_order_relaxed) & bit))
         return;
     if (dtype == ZERO_F16)
@@ -1021,17 +1197,27 @@ zero_status_t launch_fused_range(const uint16_t* rows, const zero_grads_t* g,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const float* const sp[6] = {in->master, in->m, in->v, out->master, out->m, out->v};
     const bool v8 = state_v8_ok(sp);
+    const uint64_t small_upto = variant == kVariantAuto ? small_window_limit() : 0;
     return for_each_window(elem_phase(rows + b0), len, kWindow, [&](uint64_t w0, uint64_t w1) {
         const uint64_t e0 = b0 + w0;
         FusedArgs a{rows + e0, g->row_stride, g->nd, split_window(g->offset + e0, w1 - w0),
                     in->master + e0, in->m + e0, in->v + e0, out->master + e0, out->m + e0,
                     out->v + e0, gath + e0, k, d_nonfinite, gate, nullptr,
                     (uint32_t)(w0 > 0)};
+        const int v = variant != kVariantAuto ? variant
+                                              : (w1 - w0 <= small_upto ? kVariantSmall : 1);
+        if (v == kVariantSmall) {
+            if (g->dtype == ZERO_F16)
+                launch_small<ZERO_F16>(a, g->offset + e0, s);
+            else
+                launch_small<ZERO_BF16>(a, g->offset + e0, s);
+            return launch_status();
+        }
         const int width = store_width(gath + e0 + a.sp.head);
         if (g->dtype == ZERO_F16)
-            launch_fused_dt<ZERO_F16>(a, width, v8, variant, s);
+            launch_fused_dt<ZERO_F16>(a, width, v8, v, s);
         else
-            launch_fused_dt<ZERO_BF16>(a, width, v8, variant, s);
+            launch_fused_dt<ZERO_BF16>(a, width, v8, v, s);
         return launch_status();
     });
 }
