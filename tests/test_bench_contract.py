@@ -73,7 +73,7 @@ def test_config_block_of_the_default_workload():
 def test_gpu_arm_line():
     from zero_sharded_optimizer_02_gb300 import _abi
     d = _run(["--config", "c1", "--steps", "6", "--warmup", "3", "--e2e-steps", "1",
-              "--cpu-seconds", "1"], cores=4)
+              "--cpu-seconds", "1", "--graph"], cores=4)
     assert BASE_KEYS | {"roofline", "gpu_launches", "clocks"} <= d.keys()
     n = 15_554_976
     assert d["config"]["shard_params"] == n and d["config"]["workload"].startswith("c1")
@@ -88,6 +88,10 @@ def test_gpu_arm_line():
     # the read-only ceiling over the same rows is measured beside the copy peak
     assert r["read_ceiling_gbs"] > 0
     assert r["frac_of_read_ceiling"] == pytest.approx(r["achieved"] / r["read_ceiling_gbs"])
+    # --graph: the same back-to-back steps timed as one CUDA graph as well
+    assert r["kernel"] == "k_step_fused_ring" and r["kernel_ms_per_step_graph"] > 0
+    assert r["frac_graph"] == pytest.approx(
+        (2 * 8 + 26) * n / (r["kernel_ms_per_step_graph"] * 1e-3) / 1e9 / r["peak"])
     assert d["config"] == _gpu_arm_config("c1", 0)
     # the other workloads' kernel timings: every target workload but this one
     pc = d["per_config"]
@@ -98,6 +102,12 @@ def test_gpu_arm_line():
         assert v["frac"] == pytest.approx(v["achieved"] / r["peak"])
     assert pc["c3 rank 0"]["shard_params"] == 23_437_500
     assert pc["c3 rank 0"]["launches_per_step"] == 3 and "l2" in pc["c0 rank 0"]
+    # the 4-rank shard runs on the short-window kernel, and being L2-resident
+    # (issued slower than it runs) is also timed as one CUDA graph
+    c0 = pc["c0 rank 0"]
+    assert c0["kernel"] == "k_step_fused_small" and pc["c3 rank 0"]["kernel"] == "k_step_fused_ring"
+    assert c0["kernel_ms_per_step_graph"] > 0
+    assert c0["frac_graph"] == pytest.approx(c0["achieved_graph"] / r["peak"])
     # the timed region launches exactly one fused step per timed step
     assert d["gpu_launches"] == 6 * per_step
     e = d["e2e"]

@@ -243,19 +243,27 @@ struct QuadSplit {
 };
 
 constexpr int kSmallThreads = 256;
-// Resident CTAs a SM the short-window kernel is compiled for (its register
-// budget: 65,536 / (256 x this); 80 registers at 3) and rank rows it loads
-// back to back.  Measured against 4 CTAs with 4 rows (no spills) and 5 with 4
-// on 1 to 64 rows of 65,536 to 622,592 elements: level or faster everywhere
-// within one wave, and up to 20% faster on 16 and 64 rows.
-#ifndef ZERO_SMALL_CTAS_PER_SM
-#define ZERO_SMALL_CTAS_PER_SM 3
+
+// The two compiled shapes of the short-window kernel.
+//  - wide: 8 rank rows loaded back to back, the state loaded after the fold,
+//    80 registers, 3 CTAs a SM;
+//  - light: 4 rows back to back, the state loaded before the fold (its
+//    latency then hides behind the rows'), at most 64 registers, 4 CTAs a SM.
+// Measured over 1 to 64 rows of 65,536 to 466,944 elements (graph-timed
+// back-to-back steps): light is 10-22% faster on up to 16 rows while the
+// window needs at most 2 CTAs a SM, wide is faster on 64 rows (light up to
+// 32% slower) and once the window fills a wave of 3 CTAs a SM.
+template <bool LIGHT>
+struct SmallShape {
+    static constexpr int ctas_per_sm = LIGHT ? 4 : 3;
+    static constexpr int unroll = LIGHT ? 4 : 8;
+};
+// The light shape's limits: rows, and windows of at most this many CTAs a SM.
+#ifndef ZERO_SMALL_LIGHT_CTAS
+#define ZERO_SMALL_LIGHT_CTAS 2
 #endif
-constexpr int kSmallCtasPerSm = ZERO_SMALL_CTAS_PER_SM;
-#ifndef ZERO_SMALL_UNROLL
-#define ZERO_SMALL_UNROLL 8
-#endif
-constexpr int kSmallUnroll = ZERO_SMALL_UNROLL;
+constexpr uint32_t kSmallLightMaxNd = 16;
+constexpr uint64_t kSmallLightCtasPerSm = ZERO_SMALL_LIGHT_CTAS;
 
 // K4, short-window variant.  A window shorter than one pass of the ring
 // kernel's grid leaves most of the ring's threads idle and puts the AdamW
@@ -263,14 +271,15 @@ constexpr int kSmallUnroll = ZERO_SMALL_UNROLL;
 // element) on a few SMs; this kernel gives each thread 4 elements (8-byte
 // row reads, 16-byte state accesses), so the same window spreads over every
 // SM with twice to four times the threads.  Within one wave of its grid
-// (kSmallCtasPerSm CTAs a SM) it beat the ring on every shard measured, by
-// 10% (4 rows of 262,144) to 44% (64 rows of 65,536); past one wave the
-// ring wins.  The fold, the op order and the stores' values are those of
-// every other variant.
-template <int DT, int W>
-__global__ void __launch_bounds__(kSmallThreads, kSmallCtasPerSm)
+// (3 CTAs a SM) it beat the ring on every shard measured, by 10% (4 rows of
+// 262,144) to 46% (64 rows of 65,536); past one wave the ring wins.  The
+// fold, the op order and the stores' values are those of every other
+// variant.
+template <int DT, int W, bool LIGHT>
+__global__ void __launch_bounds__(kSmallThreads, SmallShape<LIGHT>::ctas_per_sm)
     k_step_fused_small(const FusedArgs a, const QuadSplit qs)
 {
+    constexpr int kUnroll = SmallShape<LIGHT>::unroll;
     pdl_begin(a.early);
     if (gated(a))   // all of a group's windows see the gate alike (see k_step_fused_ring)
         return;
@@ -283,22 +292,30 @@ __global__ void __launch_bounds__(kSmallThreads, kSmallCtasPerSm)
     for (uint64_t q = tid; q < qs.nquad; q += nthr) {
         const uint64_t e = qs.head + 4 * q;
         const uint16_t* gp = a.g + e;
+        float4 pp, mm, vv;
+        if (LIGHT) {
+            pp = __ldcs(reinterpret_cast<const float4*>(a.p_in + e));
+            mm = __ldcs(reinterpret_cast<const float4*>(a.m_in + e));
+            vv = __ldcs(reinterpret_cast<const float4*>(a.v_in + e));
+        }
         float s[4];
         add4<DT>(s, ld_grad8(gp), true);
-        for (uint32_t j0 = 1; j0 < a.nd; j0 += kSmallUnroll) {
-            uint2 w[kSmallUnroll];
+        for (uint32_t j0 = 1; j0 < a.nd; j0 += kUnroll) {
+            uint2 w[kUnroll];
 #pragma unroll
-            for (int u = 0; u < kSmallUnroll; ++u)
+            for (int u = 0; u < kUnroll; ++u)
                 if (j0 + u < a.nd)
                     w[u] = ld_grad8(gp + (uint64_t)(j0 + u) * a.row_stride);
 #pragma unroll
-            for (int u = 0; u < kSmallUnroll; ++u)
+            for (int u = 0; u < kUnroll; ++u)
                 if (j0 + u < a.nd)
                     add4<DT>(s, w[u], false);
         }
-        const float4 pp = __ldcs(reinterpret_cast<const float4*>(a.p_in + e));
-        const float4 mm = __ldcs(reinterpret_cast<const float4*>(a.m_in + e));
-        const float4 vv = __ldcs(reinterpret_cast<const float4*>(a.v_in + e));
+        if (!LIGHT) {
+            pp = __ldcs(reinterpret_cast<const float4*>(a.p_in + e));
+            mm = __ldcs(reinterpret_cast<const float4*>(a.m_in + e));
+            vv = __ldcs(reinterpret_cast<const float4*>(a.v_in + e));
+        }
         float p[4] = {pp.x, pp.y, pp.z, pp.w};
         float m[4] = {mm.x, mm.y, mm.z, mm.w};
         float v[4] = {vv.x, vv.y, vv.z, vv.w};
@@ -824,11 +841,12 @@ int fused_variant(bool host_rows)
     return ZERO_FUSED_IMPL == 1 && ZERO_SMALL_WINDOWS ? kVariantAuto : ZERO_FUSED_IMPL;
 }
 
-// Elements one wave of the short-window kernel covers (4 a thread): a window
-// of at most this many goes to that kernel under kVariantAuto.
+// Elements one wave of the short-window kernel's wide shape covers (3 CTAs a
+// SM, 4 elements a thread): a window of at most this many goes to that
+// kernel under kVariantAuto.
 uint64_t small_window_limit()
 {
-    return (uint64_t)sm_count() * kSmallCtasPerSm * kSmallThreads * 4;
+    return (uint64_t)sm_count() * SmallShape<false>::ctas_per_sm * kSmallThreads * 4;
 }
 
 // Opts kernel `fn` in to `bytes` of dynamic shared memory on the current
@@ -935,9 +953,25 @@ void launch_fused_w(const FusedArgs& a, int variant, cudaStream_t s)
     }
 }
 
+template <int DT, bool LIGHT>
+void launch_small_shape(const FusedArgs& a, const QuadSplit& qs, uint64_t want, int sms,
+                        cudaStream_t s)
+{
+    const uint64_t cap = (uint64_t)sms * SmallShape<LIGHT>::ctas_per_sm;
+    const dim3 grid((unsigned)(want < cap ? (want ? want : 1) : cap));
+    const dim3 block(kSmallThreads);
+    switch (store_width(a.gath + qs.head)) {
+    case 16:
+    case 8: launch_k(k_step_fused_small<DT, 8, LIGHT>, grid, block, 0, s, a, qs); break;
+    case 4: launch_k(k_step_fused_small<DT, 4, LIGHT>, grid, block, 0, s, a, qs); break;
+    default: launch_k(k_step_fused_small<DT, 2, LIGHT>, grid, block, 0, s, a, qs); break;
+    }
+}
+
 // The short-window kernel over one window: quad split from the rows' phase,
-// store width from the gathered slot's (at most 8 bytes), and a CTA for every
-// 256 groups up to one wave (then a grid-stride loop).
+// store width from the gathered slot's (at most 8 bytes), a CTA for every 256
+// groups up to one wave (then a grid-stride loop), and the light shape for up
+// to 16 rows while the window needs at most 2 CTAs a SM.
 template <int DT>
 void launch_small(const FusedArgs& a, uint64_t row_phase, cudaStream_t s)
 {
@@ -948,14 +982,11 @@ void launch_small(const FusedArgs& a, uint64_t row_phase, cudaStream_t s)
     const uint64_t nscalar = a.sp.len - 4 * qs.nquad;
     const uint64_t work = qs.nquad > nscalar ? qs.nquad : nscalar;
     const uint64_t want = (work + kSmallThreads - 1) / kSmallThreads;
-    const uint64_t cap = (uint64_t)sm_count() * kSmallCtasPerSm;
-    const dim3 grid((unsigned)(want < cap ? (want ? want : 1) : cap));
-    switch (store_width(a.gath + qs.head)) {
-    case 16:
-    case 8: launch_k(k_step_fused_small<DT, 8>, grid, dim3(kSmallThreads), 0, s, a, qs); break;
-    case 4: launch_k(k_step_fused_small<DT, 4>, grid, dim3(kSmallThreads), 0, s, a, qs); break;
-    default: launch_k(k_step_fused_small<DT, 2>, grid, dim3(kSmallThreads), 0, s, a, qs); break;
-    }
+    const int sms = sm_count();
+    if (a.nd <= kSmallLightMaxNd && want <= (uint64_t)sms * kSmallLightCtasPerSm)
+        launch_small_shape<DT, true>(a, qs, want, sms, s);
+    else
+        launch_small_shape<DT, false>(a, qs, want, sms, s);
 }
 
 template <int DT, bool V8>
@@ -1145,9 +1176,12 @@ void load_fused_dt(int variant)
 {
     if (variant == kVariantSmall || variant == kVariantAuto) {
         cudaFuncAttributes fa;
-        (void)cudaFuncGetAttributes(&fa, k_step_fused_small<DT, 8>);
-        (void)cudaFuncGetAttributes(&fa, k_step_fused_small<DT, 4>);
-        (void)cudaFuncGetAttributes(&fa, k_step_fused_small<DT, 2>);
+        (void)cudaFuncGetAttributes(&fa, k_step_fused_small<DT, 8, false>);
+        (void)cudaFuncGetAttributes(&fa, k_step_fused_small<DT, 4, false>);
+        (void)cudaFuncGetAttributes(&fa, k_step_fused_small<DT, 2, false>);
+        (void)cudaFuncGetAttributes(&fa, k_step_fused_small<DT, 8, true>);
+        (void)cudaFuncGetAttributes(&fa, k_step_fused_small<DT, 4, true>);
+        (void)cudaFuncGetAttributes(&fa, k_step_fused_small<DT, 2, true>);
         if (variant == kVariantSmall)
             return;
         variant = 1;
