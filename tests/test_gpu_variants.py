@@ -182,36 +182,46 @@ def test_reductions_over_several_launch_windows_match_oracle(variant):
     assert int(flag.item()) == 1
 
 
-def test_default_choice_at_the_one_wave_boundary(monkeypatch):
+def _boundary_cases():
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    wave = sms * 3 * 256 * 4          # one wave of the short-window kernel's wide shape
+    light = sms * 2 * 256 * 4         # the light shape's limit: 2 CTAs a SM
+    # (rows, shard elements): each side of the ring / short-window cut (by
+    # elements), of the light / wide cut (by CTAs: 4-element groups, hence
+    # + 4) and of the light shape's 16-row limit
+    return [(3, wave), (3, wave + 1), (4, light), (4, light + 4), (16, 5_003), (17, 5_003)]
+
+
+@pytest.mark.parametrize("case", range(6))
+def test_default_choice_at_its_boundaries(case, monkeypatch):
     """By default a shard that one wave of the short-window kernel covers
     (SMs x 3 x 256 x 4 elements) runs on that kernel and one element more on
-    the ring: both sides of the boundary, and the same shards on each kernel
-    named explicitly, against the oracle element by element (3 fp16 rows;
-    rank 1 writes its slot of the flat gathered buffer, 16-byte aligned at
-    the boundary and 2 bytes past a line one element later)."""
-    monkeypatch.delenv("ZERO_FUSED_VARIANT", raising=False)
-    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    wave = sms * 3 * 256 * 4
-    for s in (wave, wave + 1):
-        w = dataclasses.replace(synth.WORKLOADS["c2"], psi=3 * s - 1, nd=3, plant=None,
-                                bucket=1 << 30)
-        f, rp, rm, rv, rparams = oracle_shard_step(w, 1)
-        assert f == 0
-        for v in (None, "small", "ring"):
-            if v is None:
-                monkeypatch.delenv("ZERO_FUSED_VARIANT", raising=False)
-            else:
-                monkeypatch.setenv("ZERO_FUSED_VARIANT", v)
-            dps = make_group(w, ranks=[1], gathered="full")
-            buf, desc = shard_rows(w, dps, 1, 0)
-            assert not dps.step(desc)
-            n = int(dps.layouts[1].length)
-            assert n == s
-            got = [t.cpu().numpy() for t in dps.state[1].tensors("cur")]
-            for g, ref, name, tau in zip(got, (rp, rm, rv), ("master", "m", "v"),
-                                         (1e-12, 1e-20, 1e-20)):
-                assert_state_close(g, ref, tau, f"{v} n={n} {name}")
-            b = int(dps.layouts[1].begin)
-            assert_params_close(u16(dps.gathered_view(1)[b:b + n]), rparams,
-                                f"{v} n={n} params")
-            del dps, buf, desc
+    the ring, and within it shards of up to 16 rows that need at most 2 CTAs
+    a SM run on the kernel's light shape.  Both sides of each boundary, and
+    the same shards on the short-window and ring kernels named explicitly,
+    against the oracle element by element (fp16 rows; rank 1 writes its slot
+    of the flat gathered buffer, whose 16-byte phase moves with the shard's
+    length)."""
+    nd, s = _boundary_cases()[case]
+    w = dataclasses.replace(synth.WORKLOADS["c2"], psi=nd * s - 1, nd=nd, plant=None,
+                            bucket=1 << 30)
+    f, rp, rm, rv, rparams = oracle_shard_step(w, 1)
+    assert f == 0
+    for v in (None, "small", "ring"):
+        if v is None:
+            monkeypatch.delenv("ZERO_FUSED_VARIANT", raising=False)
+        else:
+            monkeypatch.setenv("ZERO_FUSED_VARIANT", v)
+        dps = make_group(w, ranks=[1], gathered="full")
+        buf, desc = shard_rows(w, dps, 1, 0)
+        assert not dps.step(desc)
+        n = int(dps.layouts[1].length)
+        assert n == s
+        got = [t.cpu().numpy() for t in dps.state[1].tensors("cur")]
+        for g, ref, name, tau in zip(got, (rp, rm, rv), ("master", "m", "v"),
+                                     (1e-12, 1e-20, 1e-20)):
+            assert_state_close(g, ref, tau, f"{v} nd={nd} n={n} {name}")
+        b = int(dps.layouts[1].begin)
+        assert_params_close(u16(dps.gathered_view(1)[b:b + n]), rparams,
+                            f"{v} nd={nd} n={n} params")
+        del dps, buf, desc
