@@ -78,7 +78,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
         with open(stamp, "w") as f:
             f.write(key)
     headers = [os.path.join(INCLUDE, "zero.h"), os.path.join(csrc, "zero_internal.h"),
-               os.path.join(csrc, "zero_device.cuh"), os.path.join(csrc, "zero_ring.cuh")]
+               os.path.join(csrc, "zero_device.cuh"), os.path.join(csrc, "zero_ring.cuh"),
+               os.path.join(csrc, "zero_small.cuh")]
     objs, procs = [], []
     for src, cmd in SOURCES.items():
         path = os.path.join(csrc, src)
