@@ -70,9 +70,10 @@ constexpr int kSmallThreads = 256;
 //  - light: 4 rows back to back, the state loaded before the fold (its
 //    latency then hides behind the rows'), at most 64 registers, 4 CTAs a SM.
 // Measured over 1 to 64 rows of 65,536 to 466,944 elements (graph-timed
-// back-to-back steps): light is 10-22% faster on up to 16 rows while the
-// window needs at most 2 CTAs a SM, wide is faster on 64 rows (light up to
-// 32% slower) and once the window fills a wave of 3 CTAs a SM.
+// back-to-back steps): light is up to 22% faster on up to 16 rows while the
+// window needs at most 2 CTAs a SM (level on 8 rows of 131,072), wide is
+// faster on 64 rows (light up to 31% slower) and once the window fills a wave
+// of 3 CTAs a SM.
 template <bool LIGHT>
 struct SmallShape {
     static constexpr int ctas_per_sm = LIGHT ? 4 : 3;
