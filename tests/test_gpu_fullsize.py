@@ -9,8 +9,9 @@ windows of the fused step (the 7.5B shard runs as 12 windows).
 Workloads: GPT-2-small-sized ZeRO-2 shard (psi = 124,439,808, Nd = 8, bf16,
 10 steps); padding and overflow (psi = 350,000,017, Nd = 16, fp16 x 1024,
 all 16 ranks, +inf planted at step 5); GPT-2 1.5B shard view (Nd = 64, fp16,
-20 steps); 7.5B shard view (Nd = 64, bf16, bucket 5e8, 20 steps); the
-end-to-end forms (rows in pinned host memory) on the 1.5B shard view.
+20 steps); 7.5B shard view (Nd = 64, bf16, bucket 5e8, 20 steps), and its
+bucket-ready step in 16 launch groups; the end-to-end forms (rows in pinned
+host memory) on the 1.5B shard view.
 """
 import dataclasses
 import gc
@@ -241,3 +242,44 @@ def test_7p5b_shard_at_nd_1024():
     assert_state_close(gm, m, 1e-20, "m")
     assert_state_close(gv, v, 1e-20, "v")
     assert_params_close(_slot_params(dps, rank, idx), params, "params")
+
+
+def test_7p5b_bucket_ready_step_sampled():
+    """The bucket-ready step on the 7.5B shard view (rank 0, Nd = 64 bf16
+    rows resident, 15 GB) in the configuration `bench.py --op streamed` times:
+    16 transfer buckets, every ready word already set, dealt into launch
+    groups of about 1 GB of step traffic, each group behind its own wait
+    kernel.  Two steps, sampled against the oracle, with the 16 elements on
+    each side of every group boundary in the sample."""
+    w = synth.WORKLOADS["c4"]
+    rank = 0
+    dps = make_group(w, ranks=[rank], gathered="slot")
+    L = dps.layouts[rank]
+    n, pitch = int(L.length), int(L.row_pitch)
+    sb = max(8, -(-(-(-n // 16)) // 8) * 8)            # bench.py's transfer bucket
+    groups = z._abi.stream_groups(n, sb, w.nd)
+    assert len(groups) == 16 and groups[-1][0] + groups[-1][1] == n
+    s, b, _ = synth.shard_of(w.psi, w.nd, rank)
+    edges = [b + g0 + d for g0, _ in groups[1:] for d in range(-16, 16)]
+    idx = sample_indices(w.psi, w.nd, [rank], 1024, seed=77, extra=edges)
+    _, hist = oracle_trajectory(w, idx, 2)
+    buf, desc = shard_rows(w, dps, rank, 0)
+    ready = torch.ones(-(-n // sb), dtype=torch.int32, device=dps.device)
+    status = torch.zeros(1, dtype=torch.int32, device=dps.device)
+    st = dps.state[rank]
+    for k in range(2):
+        gbuf, goff = dps._gathered_target(rank, 1 - dps.gcur)
+        dps.h.step = dps.t + 1
+        z.zero_step_shard_streamed(desc[rank], L, st.states[st.cur], st.states[1 - st.cur], gbuf,
+                                   goff, sb, dps.loss_scale, dps.h, ready, 1, 10 ** 10, dps.flag,
+                                   status, dps.stream)
+        assert not dps.decide()
+        dps.commit(False)
+        assert int(status.item()) == 0
+        p, m, v, params, t = hist[k]
+        (gp, gm, gv), _ = _sampled_state(dps, idx, with_params=False)
+        assert_state_close(gp, p, 1e-12, f"master step {k}")
+        assert_state_close(gm, m, 1e-20, f"m step {k}")
+        assert_state_close(gv, v, 1e-20, f"v step {k}")
+        assert_params_close(_slot_params(dps, rank, idx), params, f"params step {k}")
+        assert dps.t == t
