@@ -10,8 +10,8 @@ Workloads: GPT-2-small-sized ZeRO-2 shard (psi = 124,439,808, Nd = 8, bf16,
 10 steps); padding and overflow (psi = 350,000,017, Nd = 16, fp16 x 1024,
 all 16 ranks, +inf planted at step 5); GPT-2 1.5B shard view (Nd = 64, fp16,
 20 steps); 7.5B shard view (Nd = 64, bf16, bucket 5e8, 20 steps), and its
-bucket-ready step in 16 launch groups; the end-to-end forms (rows in pinned
-host memory) on the 1.5B shard view.
+bucket-ready step in 16 launch groups and its unfused step; the end-to-end
+forms (rows in pinned host memory) on the 1.5B shard view.
 """
 import dataclasses
 import gc
@@ -276,6 +276,31 @@ def test_7p5b_bucket_ready_step_sampled():
         assert not dps.decide()
         dps.commit(False)
         assert int(status.item()) == 0
+        p, m, v, params, t = hist[k]
+        (gp, gm, gv), _ = _sampled_state(dps, idx, with_params=False)
+        assert_state_close(gp, p, 1e-12, f"master step {k}")
+        assert_state_close(gm, m, 1e-20, f"m step {k}")
+        assert_state_close(gv, v, 1e-20, f"v step {k}")
+        assert_params_close(_slot_params(dps, rank, idx), params, f"params step {k}")
+        assert dps.t == t
+
+
+def test_7p5b_unfused_step_sampled():
+    """The unfused step on the 7.5B shard view (rank 0, Nd = 64 bf16 rows) in
+    the configuration `bench.py --op unfused` times: one bucket of the whole
+    shard through the fusion buffer (469 MB), reduced in 12 launch windows,
+    then AdamW and the cast.  Two steps, sampled against the oracle (every
+    window cut in the sample)."""
+    w = synth.WORKLOADS["c4"]
+    rank = 0
+    dps = make_group(w, ranks=[rank], gathered="slot", fused=False)
+    n = int(dps.layouts[rank].length)
+    assert z._abi.unfused_launch_count(n, w.bucket, 0) == 12 + 2
+    idx = sample_indices(w.psi, w.nd, [rank], 1024, seed=78)
+    _, hist = oracle_trajectory(w, idx, 2)
+    buf, desc = shard_rows(w, dps, rank, 0)
+    for k in range(2):
+        assert not dps.step(desc)
         p, m, v, params, t = hist[k]
         (gp, gm, gv), _ = _sampled_state(dps, idx, with_params=False)
         assert_state_close(gp, p, 1e-12, f"master step {k}")
