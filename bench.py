@@ -276,7 +276,7 @@ def measure_config(key: str, rank: int, gathered: str, dev, stream, peak: float,
         # back-to-back steps (the last measurement on this driver).
         try:
             gms = time_graph(torch, stream, dev, call, reps)
-        except RuntimeError as e:      # a capture this torch build refuses: no figure
+        except Exception as e:         # a capture this torch build refuses: no figure
             out["graph"] = f"unavailable: {str(e).splitlines()[0][:200]}"
         else:
             gbs_graph = step_bytes / (gms * 1e-3) / 1e9
