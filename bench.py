@@ -1092,7 +1092,7 @@ def main():
     ap.add_argument("--variant", choices=["registers", "ring", "tma", "small"], default=None,
                     help="fused-step kernel for every window (sets ZERO_FUSED_VARIANT; "
                          "default: the ring, and the short-window kernel for a shard "
-                         "shorter than one pass of the ring's grid)")
+                         "that one wave of it covers, SMs x 3,072 elements)")
     ap.add_argument("--graph", action="store_true",
                     help="also time the back-to-back steps as one CUDA graph (kernel time "
                          "without host issue time)")

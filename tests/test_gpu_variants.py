@@ -1,8 +1,8 @@
 """Every variant of the fused step kernel gives the oracle's step bit for bit.
 
 zero_step_shard runs the cp.async-ring kernel by default, and the
-short-window kernel for windows shorter than one pass of the ring's grid; the
-environment variable ZERO_FUSED_VARIANT selects one kernel for every window:
+short-window kernel for windows that one wave of it covers (SMs x 3,072
+elements); the environment variable ZERO_FUSED_VARIANT selects one kernel for every window:
 the ring ("ring"), the short-window kernel ("small": 4 elements a thread),
 the register kernel ("registers", also the kernel for host-resident rows) or
 the bulk-copy kernel ("tma": a producer warp, mbarrier-tracked cp.async.bulk
