@@ -10,8 +10,9 @@ Workloads: GPT-2-small-sized ZeRO-2 shard (psi = 124,439,808, Nd = 8, bf16,
 10 steps); padding and overflow (psi = 350,000,017, Nd = 16, fp16 x 1024,
 all 16 ranks, +inf planted at step 5); GPT-2 1.5B shard view (Nd = 64, fp16,
 20 steps); 7.5B shard view (Nd = 64, bf16, bucket 5e8, 20 steps), and its
-bucket-ready step in 16 launch groups and its unfused step; the end-to-end
-forms (rows in pinned host memory) on the 1.5B shard view.
+bucket-ready step in 16 launch groups, its unfused step and its nonfinite
+pre-check; the end-to-end forms (rows in pinned host memory) on the 1.5B
+shard view.
 """
 import dataclasses
 import gc
@@ -308,3 +309,36 @@ def test_7p5b_unfused_step_sampled():
         assert_state_close(gv, v, 1e-20, f"v step {k}")
         assert_params_close(_slot_params(dps, rank, idx), params, f"params step {k}")
         assert dps.t == t
+
+
+def test_7p5b_precheck_flags_a_single_nonfinite_anywhere():
+    """The nonfinite pre-check (the read-only pass the benchmark's read
+    ceiling times) over the 7.5B shard view's 64 bf16 rows, in its 12 launch
+    windows: clean rows leave the flag 0; one +inf, -inf or NaN in any row, at
+    a window cut, the first or the last element, sets it."""
+    w = synth.WORKLOADS["c4"]
+    rank = 0
+    dps = make_group(w, ranks=[rank], gathered="slot")
+    n = int(dps.layouts[rank].length)
+    cuts = inner_cuts(n)
+    assert len(cuts) == 11
+    buf, desc = shard_rows(w, dps, rank, 0)
+    flag = dps.flag
+
+    def check() -> int:
+        flag.zero_()
+        z.zero_check_nonfinite(desc[rank], 0, n, flag)
+        torch.cuda.synchronize()
+        return int(flag.item())
+    assert check() == 0
+    bad = {"+inf": 0x7F80, "-inf": 0xFF80, "nan": 0x7FC1}
+    places = [(0, 0), (63, n - 1), (31, cuts[0] - 1), (32, cuts[0]), (17, cuts[5] + 3),
+              (63, cuts[-1])]
+    for k, (row, e) in enumerate(places):
+        code = list(bad.values())[k % 3]
+        old = buf[row, e].clone()
+        val = torch.from_numpy(np.array([code], np.uint16).view(np.int16)).view(torch.bfloat16)
+        buf[row, e] = val[0]
+        assert check() == 1, (row, e, hex(code))
+        buf[row, e] = old
+    assert check() == 0
