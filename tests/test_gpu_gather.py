@@ -124,3 +124,34 @@ def test_gather_from_and_into_host_memory():
         assert e.value.status == z.ZERO_ERR_INVALID_ARG
         torch.cuda.synchronize()
         assert bool((dst == 7).all()), "a refused gather wrote"
+
+
+def test_gather_ranges_of_the_7p5b_model():
+    """The ZeRO-3 range gather at the 7.5B model's full size: 64 shards of
+    117,187,500 fp16 parameters (15 GB, slots 8-element pitched), each slot
+    holding a closed-form function of the flat parameter index.  Ranges past
+    2^32 elements, across four shard boundaries, and ending on the model's
+    last parameter come back as exactly that function of their flat
+    indices."""
+    psi, nd = 7_500_000_000, 64
+    s = -(-psi // nd)
+    pitch = -(-s // 8) * 8
+    dev = torch.device("cuda")
+
+    def f(flat):   # the parameter at flat index `flat`, as 16 bits (no int64 overflow)
+        return ((flat * 331_804_481) >> 7) & 0xFFFF
+
+    shards = torch.zeros(nd * pitch, dtype=torch.int16, device=dev)
+    for r in range(nd):
+        n = min(s, psi - r * s)
+        idx = torch.arange(r * s, r * s + n, dtype=torch.int64, device=dev)
+        shards[r * pitch:r * pitch + n] = f(idx).to(torch.int32).to(torch.int16)
+        del idx
+    for begin, length in [(60 * s - 12_345, 3 * s + 77), (psi - 1_000, 1_000),
+                          ((1 << 32) + 13, 5_000_000), (s - 1, 2)]:
+        out = torch.empty(length, dtype=torch.int16, device=dev)
+        z.zero_gather_range(shards, pitch, psi, nd, begin, length, 2, out)
+        want = f(torch.arange(begin, begin + length, dtype=torch.int64, device=dev))
+        torch.cuda.synchronize()
+        assert torch.equal(out.to(torch.int64) & 0xFFFF, want), (begin, length)
+        del out, want
