@@ -301,7 +301,8 @@ zero_status_t zero_check_nonfinite(const zero_grads_t* g, uint64_t begin, uint64
  * one-thread kernel waits until d_ready[b] >= epoch (wrap-around comparison)
  * for each of its buckets, then the fused step's launches for the group follow
  * on the same stream (as zero_step_shard: launch windows of about
- * ZERO_FUSED_WINDOW_ELEMS elements at most, the same kernel variant).  The producer
+ * ZERO_FUSED_WINDOW_ELEMS elements at most, the same choice of kernel, the
+ * short-window kernel for a group that one wave of it covers).  The producer
  * of bucket b
  * writes d_ready[b] after the bucket's contributions are in place -- e.g. a
  * cudaMemcpyAsync of the word on the copy stream that copied the data.  The
